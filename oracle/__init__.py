@@ -1,0 +1,8 @@
+"""CPU oracle for the MoE SwiGLU layer forward.
+
+Test infrastructure only: the tests, the package smoke check and the benchmark's CPU
+baseline leg are its only users.  It shares no code with the CUDA path.
+"""
+from .moe_oracle import (DENOM_MIN, SCORES, affinity, forward, permute, round_to_bf16,
+                         route, router_logits, sigmoid, silu, softmax, softplus,
+                         sqrt_softplus, swiglu_expert)
