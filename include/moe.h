@@ -1,0 +1,198 @@
+/*
+ * moe.h -- C ABI of a single-GPU Mixture-of-Experts SwiGLU FFN layer forward (sm_103a).
+ *
+ * The layer (source pages, by title and section):
+ *   router   l = W_r x, W_r [E, d]            "DeepSeek-V4 MoE source analysis (SGLang)", sec. 二
+ *                                             (MoEGate weight [n_routed_experts, hidden_size])
+ *   scores   softmax | sigmoid | sqrt(softplus) "MoE compute and communication", sec. 二.2;
+ *                                             "DeepSeek-V4 MoE", eq. dsv4-moe-softplus
+ *   select   top-k of (score + bias); optional group-limited top-k (sum of each group's top
+ *            group_topk keys, keep topk_groups groups)  "MoE compute and communication",
+ *            sec. 五.3 and 七.3; "DeepSeek-V4 MoE", sec. "V3 的节点路由约束"
+ *            or HashTopK ids = tid2eid[token_id]    SGLang analysis, sec. 二 (HashTopK)
+ *   weights  g_i = s_i / sum_{TopK} s_j (unbiased s); softmax of the k logits for
+ *            MOE_SCORE_SOFTMAX_TOPK               "Mixture of Experts: router, token dispatch,
+ *                                                 grouped GEMM", sec. "Router 的选择过程"
+ *   dispatch expert-major rows, tokens_per_expert  same page, sec. "Token Dispatch"
+ *   experts  FFN_e(x) = W2_e (SiLU(W1_e x) * W3_e x), gate/up fused as w13
+ *                                                 SGLang analysis, sec. 四
+ *   combine  y_t = sum_j g_{t,j} FFN_{e_j}(x_t) + FFN_shared(x_t)
+ *                                                 "MoE compute and communication", sec. 二.2;
+ *                                                 router page, sec. "Token Combine"
+ *
+ * Conventions (every entry point):
+ *   - Tensors are row-major and contiguous.  Unless stated, pointers are DEVICE pointers on
+ *     the current CUDA device, owned by the caller, and must be 16-byte aligned.
+ *       x, out     [T, d]           bf16 (moe_bf16 = raw bf16 bits)
+ *       w_r        [E, d]           bf16
+ *       w13        [E, 2*d_ff, d]   bf16; rows 0..d_ff-1 of an expert = gate (W1),
+ *                                   rows d_ff..2*d_ff-1 = up (W3)
+ *       w2         [E, d, d_ff]     bf16 (W2, down projection)
+ *       w13_sh     [2*d_ff, d], w2_sh [d, d_ff]   bf16, shared expert (n_shared = 1)
+ *       bias       [E]              fp32 selection bias (NULL = none)
+ *       token_ids  [T]              int32 (hash routing only)
+ *       topk_ids   [T, k] int32, topk_w [T, k] fp32
+ *   - All work is enqueued on `stream` (NULL = legacy default stream); calls return without
+ *     waiting for the GPU.  The library never allocates device memory: scratch lives in the
+ *     caller's workspace `ws` of at least moe_workspace_bytes(plan, T) bytes (256-byte
+ *     aligned).  A plan may be used from one host thread at a time, one stream at a time;
+ *     two calls that share a workspace must not overlap on the GPU.
+ *   - Argument and shape errors are returned synchronously before anything is enqueued.
+ *     Launch failures return MOE_ERR_CUDA.  Bad device DATA (token id outside [0, vocab),
+ *     tid2eid entry or topk id outside [0, E)) is clamped into range, computed, and flagged
+ *     in the workspace error word; moe_check_status() reports it as MOE_ERR_DEVICE_INPUT.
+ *     A kernel whose internal pipeline wait exceeds ~2 s stops, flags MOE_ERR_TIMEOUT in the
+ *     same word and returns (no GPU trap).
+ *   - T = 0 is valid and enqueues nothing.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+typedef struct CUevent_st* moe_event_t;   /* same type as cudaEvent_t  */
+typedef uint16_t moe_bf16;                /* raw bfloat16 bits          */
+typedef struct moe_plan moe_plan;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, T > max_tokens, bad config        */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but outside this build's limits (see moe_config)    */
+  MOE_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned (workspace: 256-byte)    */
+  MOE_ERR_WORKSPACE = 4,    /* ws_bytes < moe_workspace_bytes(plan, T)                    */
+  MOE_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed             */
+  MOE_ERR_DEVICE_INPUT = 6, /* device data out of range (clamped); from moe_check_status */
+  MOE_ERR_TIMEOUT = 7       /* a kernel pipeline wait timed out; from moe_check_status   */
+} moe_status;
+
+typedef enum {
+  MOE_SCORE_SOFTMAX_TOPK = 0, /* select top-k on logits (+bias); weights = softmax of the
+                                 k selected logits (router page, "Router 的选择过程")        */
+  MOE_SCORE_SOFTMAX = 1,      /* p = softmax over all E; select top-k of p (+bias);
+                                 weights = p renormalised over the k (Mixtral)              */
+  MOE_SCORE_SIGMOID = 2,      /* s = 1/(1+e^-l) (DeepSeek-V3)                               */
+  MOE_SCORE_SQRT_SOFTPLUS = 3 /* s = sqrt(ln(1+e^l)) (DeepSeek-V4)                          */
+} moe_score;
+
+/* Layer configuration.  Limits of this build: d and d_ff multiples of 64, 1 <= E <= 512,
+ * 1 <= top_k <= 8 and top_k <= E, n_shared in {0,1} (the shared expert has d_ff rows),
+ * n_groups in {0} U [1, 32] with E % n_groups == 0, max_tokens <= 2^20. */
+typedef struct {
+  int32_t d;            /* hidden size                                                    */
+  int32_t d_ff;         /* expert intermediate size                                       */
+  int32_t n_experts;    /* E, routed experts                                              */
+  int32_t top_k;        /* k                                                              */
+  int32_t n_shared;     /* 0 or 1 always-on shared expert, added with weight 1            */
+  int32_t max_tokens;   /* upper bound on T for every call with this plan                 */
+  int32_t score;        /* moe_score                                                      */
+  int32_t n_groups;     /* 0 = plain top-k; else group-limited over n_groups contiguous    */
+  int32_t topk_groups;  /*   groups of E/n_groups experts: keep topk_groups groups ranked  */
+  int32_t group_topk;   /*   by the fp32 sum of their group_topk largest selection keys    */
+  const int32_t* tid2eid; /* device [vocab, top_k]; non-NULL selects HashTopK routing:
+                             ids = tid2eid[token_id] in table order, bias ignored, weights
+                             from the unbiased scores of those experts' logits.  Owned by
+                             the caller; must stay valid while the plan is used.           */
+  int32_t vocab;        /* rows of tid2eid (hash routing only)                            */
+} moe_config;
+
+/* Validate `cfg` and create a host-side plan (no device memory, no CUDA call).
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a bad config. */
+moe_status moe_plan_create(const moe_config* cfg, moe_plan** out_plan);
+
+/* Free a plan (host memory only).  NULL is accepted. */
+moe_status moe_plan_destroy(moe_plan* plan);
+
+/* Bytes of workspace a call with T tokens needs (0 if plan is NULL or T is out of range).
+ * Host-only.  The same workspace serves moe_route, moe_permute, moe_forward,
+ * moe_forward_routed and moe_forward_host. */
+size_t moe_workspace_bytes(const moe_plan* plan, int32_t T);
+
+/* Router: logits = x W_r^T (bf16 inputs, fp32 accumulation, tensor cores), then scoring,
+ * optional bias / groups / hash lookup, top-k and gate weights.
+ *   topk_ids [T,k] int32 out: descending selection key, ties -> lower expert id (hash: table
+ *   order); topk_w [T,k] fp32 out.  logits [T,E] fp32 out, optional (NULL = not exported).
+ *   token_ids is required iff the plan uses hash routing; bias may be NULL. */
+moe_status moe_route(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
+                     const moe_bf16* w_r, const float* bias, int32_t* topk_ids, float* topk_w,
+                     float* logits, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Dispatch permutation of given topk_ids [T,k] (router page, "Token Dispatch"):
+ *   counts [E] (tokens_per_expert), offsets [E+1] (exclusive prefix sum),
+ *   perm_tok [T*k] (permuted_token_ids: token of each expert-major row),
+ *   inv [T*k] (row of assignment t*k+j).  Rows are ordered by expert, then by t*k+j.
+ * Any output pointer may be NULL (not written).  Integer-exact and deterministic. */
+moe_status moe_permute(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32_t* counts,
+                       int32_t* offsets, int32_t* perm_tok, int32_t* inv, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Whole layer forward: route, dispatch, grouped SwiGLU GEMMs (routed + shared expert),
+ * combine.  out [T,d] bf16.  Deterministic: no atomics in any floating-point reduction.
+ * w13_sh / w2_sh are required iff n_shared = 1.  Intermediates (routing result, dispatch
+ * rows, activations) stay in the workspace; see moe_workspace_views(). */
+moe_status moe_forward(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
+                       const moe_bf16* w_r, const float* bias, const moe_bf16* w13,
+                       const moe_bf16* w2, const moe_bf16* w13_sh, const moe_bf16* w2_sh,
+                       moe_bf16* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Layer forward with the routing given by the caller (topk_ids [T,k] int32 in [0,E),
+ * topk_w [T,k] fp32): dispatch, grouped GEMMs and combine only. */
+moe_status moe_forward_routed(moe_plan* plan, int32_t T, const moe_bf16* x,
+                              const int32_t* topk_ids, const float* topk_w,
+                              const moe_bf16* w13, const moe_bf16* w2, const moe_bf16* w13_sh,
+                              const moe_bf16* w2_sh, moe_bf16* out, void* ws, size_t ws_bytes,
+                              moe_stream_t stream);
+
+/* moe_forward with HOST activations: x_host [T,d] bf16 and token_ids_host [T] (hash only)
+ * are copied to the workspace, the layer runs, and out_host [T,d] receives the result, all
+ * enqueued on `stream` (pinned host memory makes the copies asynchronous; the caller
+ * synchronises `stream` before reading out_host).  Weights stay device pointers. */
+moe_status moe_forward_host(moe_plan* plan, int32_t T, const moe_bf16* x_host,
+                            const int32_t* token_ids_host, const moe_bf16* w_r,
+                            const float* bias, const moe_bf16* w13, const moe_bf16* w2,
+                            const moe_bf16* w13_sh, const moe_bf16* w2_sh, moe_bf16* out_host,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream` and read the workspace error word written by the last call that used
+ * `ws`: MOE_OK, MOE_ERR_DEVICE_INPUT (clamped bad ids) or MOE_ERR_TIMEOUT. */
+moe_status moe_check_status(moe_plan* plan, const void* ws, moe_stream_t stream);
+
+/* Device addresses, inside `ws`, of the intermediates of the last forward with T tokens.
+ * Valid until the next call that uses `ws`.  Any output may be NULL. */
+typedef struct {
+  int32_t* topk_ids;   /* [T, k]                                                      */
+  float* topk_w;       /* [T, k]                                                      */
+  float* logits;       /* [T, E] router logits                                        */
+  int32_t* counts;     /* [E]                                                         */
+  int32_t* offsets;    /* [E+1]                                                       */
+  int32_t* perm_tok;   /* [T*k]                                                       */
+  int32_t* inv;        /* [T*k]                                                       */
+  moe_bf16* h;         /* [T*k + n_shared*T, d_ff] SwiGLU activations (routed rows first,
+                          expert-major; then the shared expert's T rows)               */
+  float* o;            /* [T*k + n_shared*T, d] gate-weighted expert outputs          */
+} moe_ws_views;
+moe_status moe_workspace_views(const moe_plan* plan, int32_t T, void* ws, moe_ws_views* out);
+
+/* Stage timing.  With events set, moe_forward / moe_forward_routed record events[0] before
+ * the first launch and events[i] after stage i (stages: 1 router GEMM, 2 top-k,
+ * 3 dispatch (histogram, scan, scatter, row gather), 4 gate/up grouped GEMM, 5 down grouped
+ * GEMM, 6 combine; moe_forward_routed records the stages it runs).  n_events must be
+ * >= moe_forward_stage_count() + 1; NULL / 0 disables.  Events are the caller's. */
+int32_t moe_forward_stage_count(void);
+moe_status moe_plan_set_events(moe_plan* plan, moe_event_t* events, int32_t n_events);
+
+/* Kernel launches one moe_forward enqueues (memsets and event records not counted). */
+int32_t moe_forward_launch_count(const moe_plan* plan, int32_t T);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,45 @@
+// Combine: y_t = sum_{j<k} O[inv[t*k+j]] + O_shared[t], accumulated in fp32 in slot order and
+// rounded once to bf16 ("Mixture of Experts: router, token dispatch, grouped GEMM", section
+// "Token Combine": every position's weighted output is added into its token's row; "MoE compute
+// and communication", sec. 二.2: the shared expert is added with weight 1).  The gate weight is
+// already applied by the down-projection epilogue, so this is a pure gather-sum: one block per
+// token, no atomics, fixed order -> bitwise deterministic.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ o, const int32_t* __restrict__ inv,
+                                                      int k, int d4, int N, int n_shared, uint2* __restrict__ out) {
+  __shared__ int rows[MAX_TOPK + 1];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) rows[threadIdx.x] = __ldg(inv + (size_t)t * k + threadIdx.x);
+  if (threadIdx.x == 0 && n_shared) rows[k] = N + t;
+  __syncthreads();
+  const int nr = k + n_shared;
+  for (int c = threadIdx.x; c < d4; c += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < nr; ++j) {
+      const float4 v = __ldg(o + (size_t)rows[j] * d4 + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    out[(size_t)t * d4 + c] = packed;
+  }
+}
+
+cudaError_t launch_combine(const CombineLaunch& L, cudaStream_t s) {
+  const int d4 = L.d / 4;
+  combine_kernel<<<L.T, 256, 0, s>>>(static_cast<const float4*>(static_cast<const void*>(L.o)), L.inv, L.k, d4, L.N,
+                                     L.n_shared, static_cast<uint2*>(L.out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,400 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// One persistent kernel serves the three dense contractions of the layer:
+//   * router      logits[t, e]  = sum_i x[t, i] W_r[e, i]                       (fp32 out)
+//   * gate/up     H[r, j]       = SiLU(sum_i X[r,i] W1_e[j,i]) * sum_i X[r,i] W3_e[j,i]  (bf16 out)
+//   * down        O[r, c]       = g_r * sum_j H[r, j] W2_e[c, j]                 (fp32 out)
+// ("Mixture of Experts: router, token dispatch, grouped GEMM", section "为什么不能一个一个
+// GEMM 地算": many GEMMs with different weights and different row counts M, same K/N, one
+// launch that schedules their tiles across SMs.)
+//
+// Layout: weights are the MMA's A operand (M = 128 output features per tile), the token rows
+// of one group are the B operand (N = up to TN rows, rounded up to 16).  Each tile therefore
+// streams a 128-row weight slab exactly once and reuses it for every token row of its group,
+// which is what the weight-bandwidth-bound MoE layer needs.  D = A * B^T lands in TMEM with one
+// lane per output feature and one column per token row.
+//
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer,
+// warps 2..9 = epilogue (two warps per TMEM lane quadrant, splitting the columns).
+// Tiles: for group g with R_g = ceil(rows_g / TN) row tiles, tile ids run m-block-major
+// (all row tiles of one weight slab are adjacent, so a slab re-read hits L2).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int BLOCK_M = 128;
+constexpr int BLOCK_K = 64;          // one 128-byte swizzle row of bf16
+constexpr int B_BOX = 16;            // rows per TMA box of the B operand
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = (2 + NUM_EPI_WARPS) * 32;
+enum { EPI_SWIGLU = 0, EPI_F32 = 1 };
+
+struct GemmParams {
+  int K;
+  int num_mblocks;
+  int a_rows_per_group;
+  int a_up_offset;
+  int out_features;
+  int out_ld;
+  void* out;
+  const float* row_scale;
+  int n_routed;
+  int shared_b_shift;
+  const int4* grp;      // {row_base, rows, first row tile, 0}; grp[G].z = total row tiles
+  const int* rt2g;
+  int n_groups_total;   // G (index of the total entry)
+  int dense_rows;
+  int* err;
+};
+
+template <int EPI, int TN>
+struct GemmShape {
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
+  static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : 1;
+  static constexpr int B_BYTES = TN * BLOCK_K * 2;
+  static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = NUM_A * TN;
+  static constexpr int NUM_ACC = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int USED_COLS = NUM_ACC * ACC_COLS;
+  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
+                                   : USED_COLS <= 256 ? 256 : 512;
+  static_assert(USED_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(TN % B_BOX == 0 && TN <= 256, "token tile");
+};
+
+template <int STAGES>
+constexpr int gemm_smem_bytes(int stage_bytes) {
+  return STAGES * stage_bytes + 1024 /* alignment slack */ + 256 /* barriers, flags */;
+}
+
+struct Tile {
+  int g, mb, b_row, out_row, rows, n_mma;
+  bool shared;
+};
+
+template <int TN>
+__device__ __forceinline__ Tile decode_tile(int tile, const GemmParams& p) {
+  Tile t;
+  const int rt_glob = tile / p.num_mblocks;
+  int row_base, rows_g, rt_start;
+  if (p.grp != nullptr) {
+    t.g = __ldg(p.rt2g + rt_glob);
+    const int4 gi = __ldg(p.grp + t.g);
+    row_base = gi.x;
+    rows_g = gi.y;
+    rt_start = gi.z;
+  } else {
+    t.g = 0;
+    row_base = 0;
+    rows_g = p.dense_rows;
+    rt_start = 0;
+  }
+  const int R = (rows_g + TN - 1) / TN;
+  const int local = tile - rt_start * p.num_mblocks;
+  t.mb = local / R;
+  const int rt = local - t.mb * R;
+  t.rows = min(TN, rows_g - rt * TN);
+  t.n_mma = max(16, (t.rows + 15) & ~15);
+  t.out_row = row_base + rt * TN;
+  t.shared = (p.grp != nullptr) && (t.g == p.n_routed);
+  t.b_row = t.out_row + (t.shared ? p.shared_b_shift : 0);
+  return t;
+}
+
+template <int EPI, int TN, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
+                        const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b_sh,
+                        const GemmParams p) {
+  using S = GemmShape<EPI, TN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), NUM_EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_a_sh);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_b_sh);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int total_tiles;
+  if (p.grp != nullptr) {
+    total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks;
+  } else {
+    total_tiles = ((p.dense_rows + TN - 1) / TN) * p.num_mblocks;
+  }
+  const int KB = p.K / BLOCK_K;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        const CUtensorMap* ta = t.shared ? &tm_a_sh : &tm_a;
+        const CUtensorMap* tb = t.shared ? &tm_b_sh : &tm_b;
+        const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * BLOCK_M;
+        const uint32_t bytes = S::NUM_A * S::A_BYTES + t.n_mma * BLOCK_K * 2;
+        const int nbox = t.n_mma / B_BOX;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, bytes);
+          tma_load_2d(sa, ta, fb, kb * BLOCK_K, a_row);
+          if (EPI == EPI_SWIGLU) tma_load_2d(sa + S::A_BYTES, ta, fb, kb * BLOCK_K, a_row + p.a_up_offset);
+          const uint32_t sb = sa + S::NUM_A * S::A_BYTES;
+          for (int b = 0; b < nbox; ++b) tma_load_2d(sb + b * (B_BOX * 128), tb, fb, kb * BLOCK_K, t.b_row + b * B_BOX);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(t.n_mma);
+        const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
+        const uint32_t d1 = d0 + TN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
+          const uint64_t da = smem_desc_sw128(sa);
+          const uint64_t du = smem_desc_sw128(sa + S::A_BYTES);
+          const uint64_t db = smem_desc_sw128(sa + S::NUM_A * S::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            // advance 16 bf16 = 32 bytes along K inside the swizzle row: +2 in the >>4 field
+            tc_mma(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
+            if (EPI == EPI_SWIGLU) tc_mma(d1, du + 2 * kk, db + 2 * kk, idesc, accum);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(acc));
+        if (++acc == S::NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quad = warp & 3;      // TMEM lanes this warp may access: 32*quad .. 32*quad+31
+    const int half = ew >> 2;       // which 16-column chunks: half, half+2, half+4, ...
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int feat = t.mb * BLOCK_M + quad * 32 + lane;
+      const bool fvalid = feat < p.out_features;
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + acc * S::ACC_COLS;
+      for (int c0 = half * 16; c0 < t.rows; c0 += 32) {
+        if (EPI == EPI_SWIGLU) {
+          uint32_t rg[16], ru[16];
+          tmem_ld16(tq + c0, rg);
+          tmem_ld16(tq + TN + c0, ru);
+          tmem_ld_wait();
+          reg_fence16(rg);
+          reg_fence16(ru);
+          if (fvalid) {
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+            const int nr = min(16, t.rows - c0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (j < nr) {
+                const float g = __uint_as_float(rg[j]);
+                const float u = __uint_as_float(ru[j]);
+                const float h = g / (1.0f + expf(-g)) * u;
+                out[(size_t)j * p.out_ld] = __float2bfloat16_rn(h);
+              }
+            }
+          }
+        } else {
+          uint32_t r[16];
+          tmem_ld16(tq + c0, r);
+          tmem_ld_wait();
+          reg_fence16(r);
+          if (fvalid) {
+            float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+            const bool scaled = (p.row_scale != nullptr) && !t.shared;
+            const int nr = min(16, t.rows - c0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (j < nr) {
+                const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
+                out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (++acc == S::NUM_ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// ----------------------------------------------------------------------------- host side
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols innermost, contiguous), box 64 x box_rows, 128-byte swizzle.
+static bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BLOCK_K, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI, int TN, int STAGES>
+static cudaError_t launch_variant(const GemmLaunch& L, const GemmParams& p, const CUtensorMap& a,
+                                  const CUtensorMap& ash, const CUtensorMap& b, const CUtensorMap& bsh,
+                                  cudaStream_t s) {
+  using Sh = GemmShape<EPI, TN>;
+  constexpr int smem = gemm_smem_bytes<STAGES>(Sh::STAGE_BYTES);
+  static_assert(smem <= 232448, "dynamic shared memory per block");
+  auto kern = grouped_gemm_kernel<EPI, TN, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = L.num_sms;
+  if (L.max_tiles < grid) grid = L.max_tiles;
+  if (grid < 1) grid = 1;
+  kern<<<grid, NUM_THREADS, smem, s>>>(a, ash, b, bsh, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
+  CUtensorMap ta, tash, tb, tbsh;
+  if (!make_tmap(&ta, L.a_ptr, L.a_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, L.b_ptr, L.b_rows, L.K, B_BOX)) return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr) {
+    if (!make_tmap(&tash, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
+  } else {
+    tash = ta;
+  }
+  if (L.b_sh_ptr != nullptr) {
+    if (!make_tmap(&tbsh, L.b_sh_ptr, L.b_sh_rows, L.K, B_BOX)) return cudaErrorInvalidValue;
+  } else {
+    tbsh = tb;
+  }
+  GemmParams p;
+  p.K = L.K;
+  p.num_mblocks = L.num_mblocks;
+  p.a_rows_per_group = L.a_rows_per_group;
+  p.a_up_offset = L.a_up_offset;
+  p.out_features = L.out_features;
+  p.out_ld = L.out_ld;
+  p.out = L.out;
+  p.row_scale = L.row_scale;
+  p.n_routed = L.n_routed;
+  p.shared_b_shift = L.shared_b_shift;
+  p.grp = L.grp;
+  p.rt2g = L.rt2g;
+  p.n_groups_total = L.n_routed + (L.a_sh_ptr != nullptr ? 1 : 0);
+  p.dense_rows = L.dense_rows;
+  p.err = L.err;
+  if (L.epi == EPI_SWIGLU) {
+    if (L.TN == 256) return launch_variant<EPI_SWIGLU, 256, 3>(L, p, ta, tash, tb, tbsh, s);
+    return launch_variant<EPI_SWIGLU, 64, 5>(L, p, ta, tash, tb, tbsh, s);
+  }
+  if (L.TN == 256) return launch_variant<EPI_F32, 256, 4>(L, p, ta, tash, tb, tbsh, s);
+  return launch_variant<EPI_F32, 64, 8>(L, p, ta, tash, tb, tbsh, s);
+}
+
+}  // namespace moe

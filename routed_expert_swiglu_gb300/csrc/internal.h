@@ -1,0 +1,87 @@
+// Host-side declarations shared by the translation units of the library: workspace layout,
+// kernel launchers and the configuration they need.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int MAX_EXPERTS = 512;
+constexpr int MAX_TOPK = 8;
+constexpr int MAX_GROUPS = 32;
+constexpr int MAX_TOKENS = 1 << 20;
+constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch kernels
+
+// Token-tile width (B-operand rows per tile) of the grouped GEMMs for a batch of T tokens.
+inline int token_tile_for(int T) { return T <= 64 ? 64 : 256; }
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Byte offsets of every scratch buffer inside the caller's workspace (256-byte aligned).
+struct WsLayout {
+  int T, N, G, TN, nblk, max_rt;
+  size_t err, topk_ids, topk_w, logits, blockhist, counts, offsets, grp, rt2g, perm_tok, inv,
+      row_w, xd, h, o, x_stage, out_stage, tok_stage, total;
+};
+
+WsLayout ws_layout(const moe_config& c, int T);
+
+// Launchers.  Each returns cudaSuccess or the launch error; none synchronises.
+struct GemmLaunch {
+  int epi;                 // 0 = SwiGLU dual accumulator -> bf16, 1 = fp32 (x optional row scale)
+  int TN;                  // token tile (64 or 256)
+  // A (weights) routed / shared, B (activations) routed / shared: 2-D bf16, K innermost.
+  const void* a_ptr; int64_t a_rows;
+  const void* a_sh_ptr; int64_t a_sh_rows;
+  const void* b_ptr; int64_t b_rows;
+  const void* b_sh_ptr; int64_t b_sh_rows;
+  int K;
+  int num_mblocks, a_rows_per_group, a_up_offset, out_features, out_ld;
+  void* out;
+  const float* row_scale;
+  int n_routed, shared_b_shift;
+  const int4* grp; const int* rt2g;
+  int dense_rows;
+  int max_tiles;           // upper bound on the tile count (grid sizing)
+  int* err;
+  int num_sms;
+};
+cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s);
+
+struct TopkLaunch {
+  const float* logits; const float* bias; int T, E, k, score;
+  int n_groups, topk_groups, group_topk;
+  const int32_t* token_ids; const int32_t* tid2eid; int vocab;
+  int32_t* topk_ids; float* topk_w; int* err;
+};
+cudaError_t launch_topk(const TopkLaunch& L, cudaStream_t s);
+
+struct PermuteLaunch {
+  const int32_t* topk_ids; const float* topk_w; int T, k, E, n_shared, TN, nblk;
+  int32_t* blockhist; int32_t* counts; int32_t* offsets; int4* grp; int32_t* rt2g;
+  int32_t* perm_tok; int32_t* inv; float* row_w; int* err;
+  // optional row gather x -> xd ([N, d] bf16); skipped when xd is null
+  const void* x; void* xd; int d; int num_sms;
+};
+cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s);
+int permute_launch_count(bool gather);
+
+struct CombineLaunch {
+  const float* o; const int32_t* inv; int T, k, d, N, n_shared; void* out;
+};
+cudaError_t launch_combine(const CombineLaunch& L, cudaStream_t s);
+
+// cuTensorMapEncodeTiled resolved through the runtime (no link-time libcuda dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_fn();
+
+}  // namespace moe

@@ -1,0 +1,525 @@
+// C ABI of the MoE layer (declared in include/moe.h): argument validation, workspace layout,
+// and the launch sequence router GEMM -> top-k -> dispatch -> gate/up GEMM -> down GEMM ->
+// combine on the caller's stream.  No device allocation, no host synchronisation (except
+// moe_check_status).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+struct moe_plan {
+  moe_config cfg;
+  moe_event_t* events;
+  int n_events;
+};
+
+namespace moe {
+
+WsLayout ws_layout(const moe_config& c, int T) {
+  WsLayout L;
+  memset(&L, 0, sizeof(L));
+  const int E = c.n_experts, k = c.top_k, d = c.d, f = c.d_ff, sh = c.n_shared;
+  L.T = T;
+  L.N = T * k;
+  L.G = E + sh;
+  L.TN = token_tile_for(T);
+  L.nblk = ceil_div(L.N > 0 ? L.N : 1, PERMUTE_CHUNK);
+  L.max_rt = E + ceil_div(L.N, L.TN) + sh * ceil_div(T, L.TN) + 1;
+  const size_t rows_h = (size_t)L.N + (size_t)sh * T;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + (bytes ? bytes : 1), 256);
+    return at;
+  };
+  L.err = take(256);
+  L.topk_ids = take((size_t)T * k * 4);
+  L.topk_w = take((size_t)T * k * 4);
+  L.logits = take((size_t)T * E * 4);
+  L.blockhist = take((size_t)L.nblk * E * 4);
+  L.counts = take((size_t)E * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.grp = take((size_t)(L.G + 1) * 16);
+  L.rt2g = take((size_t)L.max_rt * 4);
+  L.perm_tok = take((size_t)L.N * 4);
+  L.inv = take((size_t)L.N * 4);
+  L.row_w = take((size_t)L.N * 4);
+  L.xd = take((size_t)L.N * d * 2);
+  L.h = take(rows_h * f * 2);
+  L.o = take(rows_h * d * 4);
+  L.x_stage = take((size_t)T * d * 2);
+  L.out_stage = take((size_t)T * d * 2);
+  L.tok_stage = take((size_t)T * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+enum Stage { ST_START = 0, ST_ROUTER_GEMM = 1, ST_TOPK = 2, ST_DISPATCH = 3, ST_GATE_UP = 4, ST_DOWN = 5,
+             ST_COMBINE = 6, ST_COUNT = 6 };
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status validate_config(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->d <= 0 || c->d_ff <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->max_tokens <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0 || c->n_shared > 1) return MOE_ERR_UNSUPPORTED;
+  if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->score < MOE_SCORE_SOFTMAX_TOPK || c->score > MOE_SCORE_SQRT_SOFTPLUS) return MOE_ERR_INVALID_ARG;
+  if (c->d % 64 != 0 || c->d_ff % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->n_experts > MAX_EXPERTS || c->top_k > MAX_TOPK || c->max_tokens > MAX_TOKENS) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->n_experts * 2 * c->d_ff >= (1ll << 31) || (int64_t)c->n_experts * c->d >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->max_tokens * c->top_k * (c->d > c->d_ff ? c->d : c->d_ff) >= (1ll << 40))
+    return MOE_ERR_UNSUPPORTED;
+  if (c->n_groups < 0 || c->topk_groups < 0 || c->group_topk < 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_groups > 0) {
+    if (c->n_groups > MAX_GROUPS) return MOE_ERR_UNSUPPORTED;
+    if (c->n_experts % c->n_groups != 0) return MOE_ERR_INVALID_ARG;
+    const int gsz = c->n_experts / c->n_groups;
+    if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+    if (c->group_topk < 1 || c->group_topk > gsz) return MOE_ERR_INVALID_ARG;
+    if (c->group_topk > 8) return MOE_ERR_UNSUPPORTED;
+    if (c->top_k > c->topk_groups * gsz) return MOE_ERR_INVALID_ARG;
+  }
+  if (c->tid2eid != nullptr) {
+    if (c->vocab <= 0) return MOE_ERR_INVALID_ARG;
+    if (!aligned(c->tid2eid, 4)) return MOE_ERR_ALIGNMENT;
+  }
+  return MOE_OK;
+}
+
+moe_status check_common(const moe_plan* p, int32_t T, const void* ws, size_t ws_bytes) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > p->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < ws_layout(p->cfg, T).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status need16(const void* ptr) {
+  if (ptr == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ptr, 16)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                    \
+  do {                                   \
+    const moe_status st_ = (expr);       \
+    if (st_ != MOE_OK) return st_;       \
+  } while (0)
+#define MOE_CUDA(expr)                              \
+  do {                                              \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status num_sms(int* out) {
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  MOE_CUDA(cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev));
+  return MOE_OK;
+}
+
+void record(const moe_plan* p, int stage, cudaStream_t s) {
+  if (p->events != nullptr && stage < p->n_events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(p->events[stage]), s);
+}
+
+// Router GEMM + top-k into the given outputs.
+moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t* token_ids, const moe_bf16* w_r,
+                     const float* bias, float* logits, int32_t* ids, float* w, void* ws, int sms, cudaStream_t s) {
+  const moe_config& c = p->cfg;
+  const WsLayout L = ws_layout(c, T);
+  int* err = at<int>(ws, L.err);
+  GemmLaunch g;
+  memset(&g, 0, sizeof(g));
+  g.epi = 1;
+  g.TN = L.TN;
+  g.a_ptr = w_r;
+  g.a_rows = c.n_experts;
+  g.b_ptr = x;
+  g.b_rows = T;
+  g.K = c.d;
+  g.num_mblocks = ceil_div(c.n_experts, 128);
+  g.out_features = c.n_experts;
+  g.out_ld = c.n_experts;
+  g.out = logits;
+  g.n_routed = 1;
+  g.dense_rows = T;
+  g.max_tiles = ceil_div(T, L.TN) * g.num_mblocks;
+  g.err = err;
+  g.num_sms = sms;
+  MOE_CUDA(launch_grouped_gemm(g, s));
+  record(p, ST_ROUTER_GEMM, s);
+  TopkLaunch tk;
+  tk.logits = logits;
+  tk.bias = bias;
+  tk.T = T;
+  tk.E = c.n_experts;
+  tk.k = c.top_k;
+  tk.score = c.score;
+  tk.n_groups = c.n_groups;
+  tk.topk_groups = c.topk_groups;
+  tk.group_topk = c.group_topk;
+  tk.token_ids = token_ids;
+  tk.tid2eid = c.tid2eid;
+  tk.vocab = c.vocab;
+  tk.topk_ids = ids;
+  tk.topk_w = w;
+  tk.err = err;
+  MOE_CUDA(launch_topk(tk, s));
+  record(p, ST_TOPK, s);
+  return MOE_OK;
+}
+
+// Dispatch + grouped GEMMs + combine, from routing in the workspace or the caller's buffers.
+moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_t* ids, const float* w,
+                       const moe_bf16* w13, const moe_bf16* w2, const moe_bf16* w13_sh, const moe_bf16* w2_sh,
+                       moe_bf16* out, void* ws, int sms, cudaStream_t s) {
+  const moe_config& c = p->cfg;
+  const WsLayout L = ws_layout(c, T);
+  int* err = at<int>(ws, L.err);
+  const int E = c.n_experts, d = c.d, f = c.d_ff, sh = c.n_shared;
+  PermuteLaunch pm;
+  pm.topk_ids = ids;
+  pm.topk_w = w;
+  pm.T = T;
+  pm.k = c.top_k;
+  pm.E = E;
+  pm.n_shared = sh;
+  pm.TN = L.TN;
+  pm.nblk = L.nblk;
+  pm.blockhist = at<int32_t>(ws, L.blockhist);
+  pm.counts = at<int32_t>(ws, L.counts);
+  pm.offsets = at<int32_t>(ws, L.offsets);
+  pm.grp = at<int4>(ws, L.grp);
+  pm.rt2g = at<int32_t>(ws, L.rt2g);
+  pm.perm_tok = at<int32_t>(ws, L.perm_tok);
+  pm.inv = at<int32_t>(ws, L.inv);
+  pm.row_w = at<float>(ws, L.row_w);
+  pm.err = err;
+  pm.x = x;
+  pm.xd = at<void>(ws, L.xd);
+  pm.d = d;
+  pm.num_sms = sms;
+  MOE_CUDA(launch_permute(pm, s));
+  record(p, ST_DISPATCH, s);
+
+  const int64_t rows_h = (int64_t)L.N + (int64_t)sh * T;
+  GemmLaunch g1;
+  memset(&g1, 0, sizeof(g1));
+  g1.epi = 0;
+  g1.TN = L.TN;
+  g1.a_ptr = w13;
+  g1.a_rows = (int64_t)E * 2 * f;
+  g1.a_sh_ptr = sh ? w13_sh : nullptr;
+  g1.a_sh_rows = 2 * f;
+  g1.b_ptr = pm.xd;
+  g1.b_rows = L.N;
+  g1.b_sh_ptr = sh ? x : nullptr;
+  g1.b_sh_rows = T;
+  g1.K = d;
+  g1.num_mblocks = ceil_div(f, 128);
+  g1.a_rows_per_group = 2 * f;
+  g1.a_up_offset = f;
+  g1.out_features = f;
+  g1.out_ld = f;
+  g1.out = at<void>(ws, L.h);
+  g1.n_routed = E;
+  g1.shared_b_shift = -L.N;
+  g1.grp = pm.grp;
+  g1.rt2g = pm.rt2g;
+  g1.max_tiles = L.max_rt * g1.num_mblocks;
+  g1.err = err;
+  g1.num_sms = sms;
+  MOE_CUDA(launch_grouped_gemm(g1, s));
+  record(p, ST_GATE_UP, s);
+
+  GemmLaunch g2;
+  memset(&g2, 0, sizeof(g2));
+  g2.epi = 1;
+  g2.TN = L.TN;
+  g2.a_ptr = w2;
+  g2.a_rows = (int64_t)E * d;
+  g2.a_sh_ptr = sh ? w2_sh : nullptr;
+  g2.a_sh_rows = d;
+  g2.b_ptr = at<void>(ws, L.h);
+  g2.b_rows = rows_h;
+  g2.K = f;
+  g2.num_mblocks = ceil_div(d, 128);
+  g2.a_rows_per_group = d;
+  g2.out_features = d;
+  g2.out_ld = d;
+  g2.out = at<void>(ws, L.o);
+  g2.row_scale = pm.row_w;
+  g2.n_routed = E;
+  g2.shared_b_shift = 0;
+  g2.grp = pm.grp;
+  g2.rt2g = pm.rt2g;
+  g2.max_tiles = L.max_rt * g2.num_mblocks;
+  g2.err = err;
+  g2.num_sms = sms;
+  MOE_CUDA(launch_grouped_gemm(g2, s));
+  record(p, ST_DOWN, s);
+
+  CombineLaunch cb;
+  cb.o = at<float>(ws, L.o);
+  cb.inv = pm.inv;
+  cb.T = T;
+  cb.k = c.top_k;
+  cb.d = d;
+  cb.N = L.N;
+  cb.n_shared = sh;
+  cb.out = out;
+  MOE_CUDA(launch_combine(cb, s));
+  record(p, ST_COMBINE, s);
+  return MOE_OK;
+}
+
+moe_status check_forward_ptrs(const moe_plan* p, const moe_bf16* w13, const moe_bf16* w2, const moe_bf16* w13_sh,
+                              const moe_bf16* w2_sh) {
+  MOE_TRY(need16(w13));
+  MOE_TRY(need16(w2));
+  if (p->cfg.n_shared) {
+    MOE_TRY(need16(w13_sh));
+    MOE_TRY(need16(w2_sh));
+  }
+  return MOE_OK;
+}
+
+moe_status check_route_ptrs(const moe_plan* p, const moe_bf16* x, const int32_t* token_ids, const moe_bf16* w_r,
+                            const float* bias) {
+  MOE_TRY(need16(x));
+  MOE_TRY(need16(w_r));
+  if (bias != nullptr && !aligned(bias, 4)) return MOE_ERR_ALIGNMENT;
+  if (p->cfg.tid2eid != nullptr) {
+    if (token_ids == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned(token_ids, 4)) return MOE_ERR_ALIGNMENT;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_plan_create(const moe_config* cfg, moe_plan** out_plan) {
+  if (out_plan == nullptr) return MOE_ERR_INVALID_ARG;
+  *out_plan = nullptr;
+  MOE_TRY(validate_config(cfg));
+  moe_plan* p = static_cast<moe_plan*>(calloc(1, sizeof(moe_plan)));
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  p->cfg = *cfg;
+  *out_plan = p;
+  return MOE_OK;
+}
+
+moe_status moe_plan_destroy(moe_plan* plan) {
+  free(plan);
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_plan* plan, int32_t T) {
+  if (plan == nullptr || T < 0 || T > plan->cfg.max_tokens) return 0;
+  return ws_layout(plan->cfg, T).total;
+}
+
+moe_status moe_route(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids, const moe_bf16* w_r,
+                     const float* bias, int32_t* topk_ids, float* topk_w, float* logits, void* ws, size_t ws_bytes,
+                     moe_stream_t stream) {
+  MOE_TRY(check_common(plan, T, ws, ws_bytes));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(check_route_ptrs(plan, x, token_ids, w_r, bias));
+  if (topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_ids, 4) || !aligned(topk_w, 4) || (logits != nullptr && !aligned(logits, 16)))
+    return MOE_ERR_ALIGNMENT;
+  int sms = 0;
+  MOE_TRY(num_sms(&sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(plan->cfg, T);
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  float* lg = logits != nullptr ? logits : at<float>(ws, L.logits);
+  return run_route(plan, T, x, token_ids, w_r, bias, lg, topk_ids, topk_w, ws, sms, s);
+}
+
+moe_status moe_permute(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32_t* counts, int32_t* offsets,
+                       int32_t* perm_tok, int32_t* inv, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_common(plan, T, ws, ws_bytes));
+  if (T == 0) return MOE_OK;
+  if (topk_ids == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_ids, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm_tok, 4) ||
+      !aligned(inv, 4))
+    return MOE_ERR_ALIGNMENT;
+  int sms = 0;
+  MOE_TRY(num_sms(&sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const moe_config& c = plan->cfg;
+  const WsLayout L = ws_layout(c, T);
+  int* err = at<int>(ws, L.err);
+  MOE_CUDA(cudaMemsetAsync(err, 0, sizeof(int), s));
+  PermuteLaunch pm;
+  memset(&pm, 0, sizeof(pm));
+  pm.topk_ids = topk_ids;
+  pm.T = T;
+  pm.k = c.top_k;
+  pm.E = c.n_experts;
+  pm.n_shared = c.n_shared;
+  pm.TN = L.TN;
+  pm.nblk = L.nblk;
+  pm.blockhist = at<int32_t>(ws, L.blockhist);
+  pm.counts = counts != nullptr ? counts : at<int32_t>(ws, L.counts);
+  pm.offsets = offsets != nullptr ? offsets : at<int32_t>(ws, L.offsets);
+  pm.grp = at<int4>(ws, L.grp);
+  pm.rt2g = at<int32_t>(ws, L.rt2g);
+  pm.perm_tok = perm_tok != nullptr ? perm_tok : at<int32_t>(ws, L.perm_tok);
+  pm.inv = inv != nullptr ? inv : at<int32_t>(ws, L.inv);
+  pm.err = err;
+  pm.num_sms = sms;
+  MOE_CUDA(launch_permute(pm, s));
+  return MOE_OK;
+}
+
+moe_status moe_forward(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids, const moe_bf16* w_r,
+                       const float* bias, const moe_bf16* w13, const moe_bf16* w2, const moe_bf16* w13_sh,
+                       const moe_bf16* w2_sh, moe_bf16* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_common(plan, T, ws, ws_bytes));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(check_route_ptrs(plan, x, token_ids, w_r, bias));
+  MOE_TRY(check_forward_ptrs(plan, w13, w2, w13_sh, w2_sh));
+  MOE_TRY(need16(out));
+  int sms = 0;
+  MOE_TRY(num_sms(&sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(plan->cfg, T);
+  record(plan, ST_START, s);
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  int32_t* ids = at<int32_t>(ws, L.topk_ids);
+  float* w = at<float>(ws, L.topk_w);
+  MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
+  return run_experts(plan, T, x, ids, w, w13, w2, w13_sh, w2_sh, out, ws, sms, s);
+}
+
+moe_status moe_forward_routed(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* topk_ids,
+                              const float* topk_w, const moe_bf16* w13, const moe_bf16* w2, const moe_bf16* w13_sh,
+                              const moe_bf16* w2_sh, moe_bf16* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_common(plan, T, ws, ws_bytes));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(need16(x));
+  if (topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_ids, 4) || !aligned(topk_w, 4)) return MOE_ERR_ALIGNMENT;
+  MOE_TRY(check_forward_ptrs(plan, w13, w2, w13_sh, w2_sh));
+  MOE_TRY(need16(out));
+  int sms = 0;
+  MOE_TRY(num_sms(&sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(plan->cfg, T);
+  record(plan, ST_START, s);
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  record(plan, ST_ROUTER_GEMM, s);
+  record(plan, ST_TOPK, s);
+  return run_experts(plan, T, x, topk_ids, topk_w, w13, w2, w13_sh, w2_sh, out, ws, sms, s);
+}
+
+moe_status moe_forward_host(moe_plan* plan, int32_t T, const moe_bf16* x_host, const int32_t* token_ids_host,
+                            const moe_bf16* w_r, const float* bias, const moe_bf16* w13, const moe_bf16* w2,
+                            const moe_bf16* w13_sh, const moe_bf16* w2_sh, moe_bf16* out_host, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_common(plan, T, ws, ws_bytes));
+  if (T == 0) return MOE_OK;
+  if (x_host == nullptr || out_host == nullptr) return MOE_ERR_INVALID_ARG;
+  if (plan->cfg.tid2eid != nullptr && token_ids_host == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(need16(w_r));
+  MOE_TRY(check_forward_ptrs(plan, w13, w2, w13_sh, w2_sh));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(plan->cfg, T);
+  const size_t xbytes = (size_t)T * plan->cfg.d * 2;
+  moe_bf16* xd = at<moe_bf16>(ws, L.x_stage);
+  moe_bf16* od = at<moe_bf16>(ws, L.out_stage);
+  int32_t* td = nullptr;
+  MOE_CUDA(cudaMemcpyAsync(xd, x_host, xbytes, cudaMemcpyHostToDevice, s));
+  if (plan->cfg.tid2eid != nullptr) {
+    td = at<int32_t>(ws, L.tok_stage);
+    MOE_CUDA(cudaMemcpyAsync(td, token_ids_host, (size_t)T * 4, cudaMemcpyHostToDevice, s));
+  }
+  MOE_TRY(moe_forward(plan, T, xd, td, w_r, bias, w13, w2, w13_sh, w2_sh, od, ws, ws_bytes, stream));
+  MOE_CUDA(cudaMemcpyAsync(out_host, od, xbytes, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
+moe_status moe_check_status(moe_plan* plan, const void* ws, moe_stream_t stream) {
+  if (plan == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaStreamSynchronize(s));
+  int v = 0;
+  MOE_CUDA(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost));  // the error word is at offset 0
+  if (v & DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (v != 0) return MOE_ERR_DEVICE_INPUT;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_views(const moe_plan* plan, int32_t T, void* ws, moe_ws_views* out) {
+  if (plan == nullptr || ws == nullptr || out == nullptr || T < 0 || T > plan->cfg.max_tokens)
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(plan->cfg, T);
+  out->topk_ids = at<int32_t>(ws, L.topk_ids);
+  out->topk_w = at<float>(ws, L.topk_w);
+  out->logits = at<float>(ws, L.logits);
+  out->counts = at<int32_t>(ws, L.counts);
+  out->offsets = at<int32_t>(ws, L.offsets);
+  out->perm_tok = at<int32_t>(ws, L.perm_tok);
+  out->inv = at<int32_t>(ws, L.inv);
+  out->h = at<moe_bf16>(ws, L.h);
+  out->o = at<float>(ws, L.o);
+  return MOE_OK;
+}
+
+int32_t moe_forward_stage_count(void) { return ST_COUNT; }
+
+moe_status moe_plan_set_events(moe_plan* plan, moe_event_t* events, int32_t n_events) {
+  if (plan == nullptr) return MOE_ERR_INVALID_ARG;
+  if (events == nullptr || n_events <= 0) {
+    plan->events = nullptr;
+    plan->n_events = 0;
+    return MOE_OK;
+  }
+  if (n_events < ST_COUNT + 1) return MOE_ERR_INVALID_ARG;
+  plan->events = events;
+  plan->n_events = n_events;
+  return MOE_OK;
+}
+
+int32_t moe_forward_launch_count(const moe_plan* plan, int32_t T) {
+  if (plan == nullptr || T <= 0) return 0;
+  return 2 /* router GEMM, top-k */ + permute_launch_count(true) + 2 /* grouped GEMMs */ + 1 /* combine */;
+}
+
+const char* moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_INPUT: return "device input out of range (clamped)";
+    case MOE_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+// Token dispatch: token-major assignments -> expert-major rows, with the inverse map kept
+// ("Mixture of Experts: router, token dispatch, grouped GEMM", section "Token Dispatch":
+// permuted_token_ids, tokens_per_expert; SGLang analysis page, sec. 三/四: the mapping back to
+// each token's output row must be kept).
+//
+// Assignment i = t*k + j.  Rows are ordered by expert and, inside an expert, by i.  Integer
+// only, so the result is exact and independent of scheduling:
+//   1. hist     per-chunk expert histograms (chunk = 1024 consecutive assignments)
+//   2. scan     per-expert prefix over chunks, exclusive scan over experts (offsets), and the
+//               grouped-GEMM schedule: row tiles per group and the row-tile -> group map
+//   3. scatter  rank inside the chunk from warp match masks + per-warp prefix, so row =
+//               chunk base + warp prefix + rank among equal ids in the warp
+//   4. gather   X_dispatch[row] = x[token(row)], 16-byte vectors, one warp per row
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ int clamp_expert(int e, int E, int* err) {
+  if (e < 0 || e >= E) {
+    atomicOr(err, DEVERR_TOPK_ID);
+    e = min(max(e, 0), E - 1);
+  }
+  return e;
+}
+
+__global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ ids, int N, int E,
+                                                   int32_t* __restrict__ blockhist, int* err) {
+  __shared__ int h[MAX_EXPERTS];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * PERMUTE_CHUNK;
+  const int end = min(base + PERMUTE_CHUNK, N);
+  for (int i = base + threadIdx.x; i < end; i += blockDim.x) atomicAdd(&h[clamp_expert(__ldg(ids + i), E, err)], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blockhist[(size_t)blockIdx.x * E + e] = h[e];
+}
+
+// Exclusive scan of one int per thread over a block of exactly 1024 threads.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = (warp > 0) ? s_warp[warp - 1] : 0;
+  total = s_warp[31];
+  __syncthreads();
+  return prefix + x - v;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ blockhist, int nblk, int E, int n_shared,
+                                                    int T, int N, int TN, int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ offsets, int4* __restrict__ grp,
+                                                    int32_t* __restrict__ rt2g) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int c = blockhist[(size_t)b * E + e];
+      blockhist[(size_t)b * E + e] = cnt;  // rows of expert e in earlier chunks
+      cnt += c;
+    }
+  }
+  int total_rows;
+  const int off = block_excl_scan(cnt, s_warp, total_rows);
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = off;
+    for (int b = 0; b < nblk; ++b) blockhist[(size_t)b * E + e] += off;  // chunk base row per expert
+  }
+  if (e == 0) offsets[E] = total_rows;
+  // grouped-GEMM schedule: groups 0..E-1 routed, group E shared (rows N .. N+T-1)
+  const int G = E + n_shared;
+  int rows = 0, row_base = 0;
+  if (e < E) {
+    rows = cnt;
+    row_base = off;
+  } else if (e < G) {
+    rows = T;
+    row_base = N;
+  }
+  const int R = (rows + TN - 1) / TN;
+  int total_rt;
+  const int rt_start = block_excl_scan(R, s_warp, total_rt);
+  if (e < G) {
+    grp[e] = make_int4(row_base, rows, rt_start, 0);
+    for (int j = 0; j < R; ++j) rt2g[rt_start + j] = e;
+  }
+  if (e == 0) grp[G] = make_int4(0, 0, total_rt, 0);
+}
+
+__global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* __restrict__ ids,
+                                                                const float* __restrict__ w, int N, int k, int E,
+                                                                const int32_t* __restrict__ blockbase,
+                                                                int32_t* __restrict__ perm_tok,
+                                                                int32_t* __restrict__ inv, float* __restrict__ row_w,
+                                                                int* err) {
+  extern __shared__ int wcnt[];  // [32 warps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int x = threadIdx.x; x < 32 * E; x += blockDim.x) wcnt[x] = 0;
+  __syncthreads();
+  const int i = blockIdx.x * PERMUTE_CHUNK + threadIdx.x;
+  const bool valid = i < N;
+  const int e = valid ? clamp_expert(__ldg(ids + i), E, err) : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int run = 0;
+    for (int v = 0; v < 32; ++v) {
+      const int c = wcnt[v * E + x];
+      wcnt[v * E + x] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (valid) {
+    const int row = blockbase[(size_t)blockIdx.x * E + e] + wcnt[warp * E + e] + rank;
+    if (perm_tok) perm_tok[row] = i / k;
+    if (inv) inv[i] = row;
+    if (row_w) row_w[row] = __ldg(w + i);
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(const int4* __restrict__ x, int4* __restrict__ xd,
+                                                          const int32_t* __restrict__ perm_tok, int N,
+                                                          int vec_per_row) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += nwarps) {
+    const int t = __ldg(perm_tok + r);
+    const int4* src = x + (size_t)t * vec_per_row;
+    int4* dst = xd + (size_t)r * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+int permute_launch_count(bool gather) { return gather ? 4 : 3; }
+
+cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s) {
+  const int N = L.T * L.k;
+  hist_kernel<<<L.nblk, 256, 0, s>>>(L.topk_ids, N, L.E, L.blockhist, L.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  scan_kernel<<<1, 1024, 0, s>>>(L.blockhist, L.nblk, L.E, L.n_shared, L.T, N, L.TN, L.counts, L.offsets, L.grp,
+                                 L.rt2g);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int smem = 32 * L.E * (int)sizeof(int);
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  scatter_kernel<<<L.nblk, PERMUTE_CHUNK, smem, s>>>(L.topk_ids, L.topk_w, N, L.k, L.E, L.blockhist, L.perm_tok,
+                                                      L.inv, L.row_w, L.err);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (L.xd != nullptr) {
+    const int vec = L.d / 8;
+    int blocks = (N + 7) / 8;
+    const int cap = L.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const int4*>(L.x), static_cast<int4*>(L.xd), L.perm_tok,
+                                              N, vec);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace moe

@@ -1,0 +1,237 @@
+// Router epilogue: per-token scoring, optional selection bias, group-limited or hash
+// selection, top-k and gate weights, from the fp32 logits the router GEMM produced.
+//
+//   scores   softmax | sigmoid | sqrt(softplus)     ("MoE compute and communication", sec. 二.2;
+//                                                  "DeepSeek-V4 MoE", eq. dsv4-moe-softplus)
+//   bias     selection key = score + b_e, weights from the unbiased score (same page, sec. 七.3)
+//   groups   group score = sum of its group_topk largest keys; keep topk_groups groups
+//            ("DeepSeek-V4 MoE", sec. "V3 的节点路由约束")
+//   hash     ids = tid2eid[token_id]               (SGLang analysis page, sec. 二, HashTopK)
+//   top-k then softmax over the selected logits  (router page, sec. "Router 的选择过程")
+//
+// One warp per token; expert e lives in lane e % 32, register slot e / 32.  Top-k is k rounds
+// of a warp arg-max (larger key wins, equal keys -> lower expert id), so ids come out in
+// descending key order.  All reductions use a fixed shuffle tree: results are deterministic.
+#include <float.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int TOPK_WARPS = 8;
+constexpr int MAX_PER_LANE = MAX_EXPERTS / 32;
+constexpr int MAX_GROUP_TOPK = 8;
+
+__device__ __forceinline__ float score_fn(float l, int mode) {
+  if (mode == MOE_SCORE_SIGMOID) return 1.0f / (1.0f + expf(-l));
+  if (mode == MOE_SCORE_SQRT_SOFTPLUS) {
+    const float sp = (l > 0.0f) ? l + log1pf(expf(-l)) : log1pf(expf(l));
+    return sqrtf(sp);
+  }
+  return l;  // softmax modes are handled by the caller
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Value of register slot `i` without dynamic register indexing.
+__device__ __forceinline__ float pick(const float (&a)[MAX_PER_LANE], int i) {
+  float v = 0.0f;
+#pragma unroll
+  for (int s = 0; s < MAX_PER_LANE; ++s)
+    if (s == i) v = a[s];
+  return v;
+}
+
+__global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
+  __shared__ float s_keys[TOPK_WARPS][MAX_EXPERTS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * TOPK_WARPS + warp;
+  if (t >= a.T) return;  // whole warp leaves together
+  const int E = a.E, k = a.k, mode = a.score;
+  const float* lrow = a.logits + (size_t)t * E;
+
+  float l[MAX_PER_LANE], sc[MAX_PER_LANE], key[MAX_PER_LANE];
+#pragma unroll
+  for (int i = 0; i < MAX_PER_LANE; ++i) {
+    const int e = lane + 32 * i;
+    l[i] = (e < E) ? __ldg(lrow + e) : -INFINITY;
+  }
+  // unbiased scores (softmax_topk: the logits themselves)
+  if (mode == MOE_SCORE_SOFTMAX) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) m = fmaxf(m, l[i]);
+    m = warp_max(m);
+    float ex[MAX_PER_LANE], s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) {
+      ex[i] = (lane + 32 * i < E) ? expf(l[i] - m) : 0.0f;
+      s += ex[i];
+    }
+    s = warp_sum(s);
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) sc[i] = ex[i] / s;
+  } else {
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) sc[i] = score_fn(l[i], mode);
+  }
+
+  int ids[MAX_TOPK];
+  float sel[MAX_TOPK];   // unbiased score (or logit) of each selected expert
+  if (a.tid2eid != nullptr) {
+    // ---------------------------------------------------------------- HashTopK
+    int tok = __ldg(a.token_ids + t);
+    if (tok < 0 || tok >= a.vocab) {
+      if (lane == 0) atomicOr(a.err, DEVERR_TOKEN_ID);
+      tok = min(max(tok, 0), a.vocab - 1);
+    }
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j) {
+      if (j < k) {
+        int e = __ldg(a.tid2eid + (size_t)tok * k + j);
+        if (e < 0 || e >= E) {
+          if (lane == 0) atomicOr(a.err, DEVERR_TID2EID);
+          e = min(max(e, 0), E - 1);
+        }
+        ids[j] = e;
+        sel[j] = __shfl_sync(0xffffffffu, pick(sc, e >> 5), e & 31);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- learned top-k
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = (e < E) ? sc[i] + (a.bias != nullptr ? __ldg(a.bias + e) : 0.0f) : -INFINITY;
+    }
+    if (a.n_groups > 0) {
+      const int gsz = E / a.n_groups;
+#pragma unroll
+      for (int i = 0; i < MAX_PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) s_keys[warp][e] = key[i];
+      }
+      __syncwarp();
+      float gscore = -INFINITY;
+      if (lane < a.n_groups) {
+        float top[MAX_GROUP_TOPK];
+#pragma unroll
+        for (int j = 0; j < MAX_GROUP_TOPK; ++j) top[j] = -INFINITY;
+        const float* gk = &s_keys[warp][lane * gsz];
+        for (int x = 0; x < gsz; ++x) {
+          float v = gk[x];
+          // insert v into the descending list top[0..group_topk) (strictly larger moves up)
+#pragma unroll
+          for (int j = 0; j < MAX_GROUP_TOPK; ++j) {
+            if (j < a.group_topk && v > top[j]) {
+              const float tmp = top[j];
+              top[j] = v;
+              v = tmp;
+            }
+          }
+        }
+        float acc = top[0];
+#pragma unroll
+        for (int j = 1; j < MAX_GROUP_TOPK; ++j)
+          if (j < a.group_topk) acc = acc + top[j];
+        gscore = acc;
+      }
+      int rank = 0;
+      for (int h = 0; h < a.n_groups; ++h) {
+        const float o = __shfl_sync(0xffffffffu, gscore, h);
+        if (o > gscore || (o == gscore && h < lane)) ++rank;
+      }
+      const unsigned keep = __ballot_sync(0xffffffffu, lane < a.n_groups && rank < a.topk_groups);
+#pragma unroll
+      for (int i = 0; i < MAX_PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((keep >> (e / gsz)) & 1u)) key[i] = -INFINITY;
+      }
+    }
+    unsigned taken = 0;
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j) {
+      if (j < k) {
+        float bk = -INFINITY;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < MAX_PER_LANE; ++i) {
+          const bool avail = (lane + 32 * i < E) && !((taken >> i) & 1u);
+          if (avail && (key[i] > bk || bi < 0)) {
+            bk = key[i];
+            bi = i;
+          }
+        }
+        int be = (bi >= 0) ? lane + 32 * bi : 0x7fffffff;
+        if (bi < 0) bk = -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ok > bk || (ok == bk && oe < be)) {
+            bk = ok;
+            be = oe;
+          }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        ids[j] = be;
+        sel[j] = __shfl_sync(0xffffffffu, pick(sc, be >> 5), be & 31);
+      }
+    }
+  }
+
+  // gate weights
+  float w[MAX_TOPK];
+  if (mode == MOE_SCORE_SOFTMAX_TOPK) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j < k) m = fmaxf(m, sel[j]);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j < k) {
+        w[j] = expf(sel[j] - m);
+        s += w[j];
+      }
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j < k) w[j] = w[j] / s;
+  } else {
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j < k) s += sel[j];
+    s = fmaxf(s, 1e-30f);
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j < k) w[j] = sel[j] / s;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j)
+      if (j < k) {
+        a.topk_ids[(size_t)t * k + j] = ids[j];
+        a.topk_w[(size_t)t * k + j] = w[j];
+      }
+  }
+}
+
+cudaError_t launch_topk(const TopkLaunch& L, cudaStream_t s) {
+  const int blocks = (L.T + TOPK_WARPS - 1) / TOPK_WARPS;
+  topk_kernel<<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
