@@ -27,10 +27,10 @@ What the layer computes (source pages, by title and section):
 Readings where the pages are silent (each is listed with its reason in the design notes):
   * Selection keys are compared in fp32 (the kernel's precision), ties go to the lower
     expert id, and the k ids are returned in descending key order.
-  * The SwiGLU activation h is cast to bf16 (round to nearest even) before the down
-    projection: the stage table of "DeepSeek-V4 MoE" (Wave-Scheduled EP, "Activation + FP8
-    Cast") re-quantises h to the second GEMM's input format; here that format is bf16.
-    Pass cast_h=False for the unrounded fp64 definition.
+  * The expert FFN is the plain definition, with no rounding of the activation h between the
+    two projections (the layer definition on "MoE compute and communication", sec. 二.1/二.2,
+    has none; the FP8 re-quantisation in the "DeepSeek-V4 MoE" stage table belongs to that
+    system's FP8 kernels).  cast_h=True evaluates the variant that rounds h to bf16.
   * Gate weights come from the unbiased scores; for softmax_topk they are the softmax of the
     selected logits; the renormalising denominator is clamped to >= 1e-30.
   * Group membership is contiguous: group g holds experts [g*E/G, (g+1)*E/G).
@@ -201,7 +201,7 @@ def silu(g):
         return g / (1.0 + np.exp(-g))
 
 
-def swiglu_expert(xr, w13, w2, cast_h=True):
+def swiglu_expert(xr, w13, w2, cast_h=False):
     """FFN(x) = W2 (SiLU(W1 x) * (W3 x)) for the rows of xr [m, d].
 
     w13 is [2f, d]: rows 0..f-1 are W1 (gate), rows f..2f-1 are W3 (up); w2 is [d, f]."""
@@ -217,7 +217,7 @@ def swiglu_expert(xr, w13, w2, cast_h=True):
     return h @ w2.T
 
 
-def forward(x, topk_ids, topk_w, expert_weights, shared_weights=None, tokens=None, cast_h=True):
+def forward(x, topk_ids, topk_w, expert_weights, shared_weights=None, tokens=None, cast_h=False):
     """Layer output y[t] = sum_j topk_w[t,j] * FFN_{topk_ids[t,j]}(x[t]) + FFN_shared(x[t]).
 
     expert_weights(e) -> (w13_e [2f, d], w2_e [d, f]); shared_weights: (w13_sh, w2_sh) or
