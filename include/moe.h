@@ -172,7 +172,9 @@ typedef struct {
   int32_t* offsets;    /* [E+1]                                                       */
   int32_t* perm_tok;   /* [T*k]                                                       */
   int32_t* inv;        /* [T*k]                                                       */
-  moe_bf16* h;         /* [T*k + n_shared*T, d_ff] SwiGLU activations (routed rows first,
+  moe_bf16* h;         /* [T*k + n_shared*T, 2*d_ff] SwiGLU activations h = hi + lo (bf16 pair;
+                          per 64-feature block b, hi in columns 128b..128b+63, lo in the next
+                          64); routed rows first,
                           expert-major; then the shared expert's T rows)               */
   float* o;            /* [T*k + n_shared*T, d] gate-weighted expert outputs          */
 } moe_ws_views;

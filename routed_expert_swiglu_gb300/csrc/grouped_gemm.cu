@@ -37,6 +37,8 @@ struct GemmParams {
   int num_mblocks;
   int a_rows_per_group;
   int a_up_offset;
+  int a_k_shift;        // A's K block = B's K block >> a_k_shift (1: each weight block serves two
+                        // consecutive activation blocks, the hi and lo halves of H)
   int out_features;
   int out_ld;
   void* out;
@@ -181,8 +183,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, bytes);
-          tma_load_2d(sa, ta, fb, kb * BLOCK_K, a_row);
-          if (EPI == EPI_SWIGLU) tma_load_2d(sa + S::A_BYTES, ta, fb, kb * BLOCK_K, a_row + p.a_up_offset);
+          const int ka = (kb >> p.a_k_shift) * BLOCK_K;
+          tma_load_2d(sa, ta, fb, ka, a_row);
+          if (EPI == EPI_SWIGLU) tma_load_2d(sa + S::A_BYTES, ta, fb, ka, a_row + p.a_up_offset);
           const uint32_t sb = sa + S::NUM_A * S::A_BYTES;
           for (int b = 0; b < nbox; ++b) tma_load_2d(sb + b * (B_BOX * 128), tb, fb, kb * BLOCK_K, t.b_row + b * B_BOX);
           if (++stage == STAGES) {
@@ -263,7 +266,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           reg_fence16(rg);
           reg_fence16(ru);
           if (fvalid) {
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+            // h is stored as an unevaluated pair hi + lo of bf16 values: hi = bf16(h),
+            // lo = bf16(h - hi), so the down projection sees h to ~16 significant bits.  Within
+            // each 64-feature block, hi occupies columns [128*b, 128*b + 64) and lo the next 64.
+            const int col = ((feat >> 6) << 7) + (feat & 63);
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
             const int nr = min(16, t.rows - c0);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -271,7 +278,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float g = __uint_as_float(rg[j]);
                 const float u = __uint_as_float(ru[j]);
                 const float h = g / (1.0f + expf(-g)) * u;
-                out[(size_t)j * p.out_ld] = __float2bfloat16_rn(h);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+                out[(size_t)j * p.out_ld] = hi;
+                out[(size_t)j * p.out_ld + 64] = lo;
               }
             }
           }
@@ -361,10 +371,11 @@ static cudaError_t launch_variant(const GemmLaunch& L, const GemmParams& p, cons
 
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   CUtensorMap ta, tash, tb, tbsh;
-  if (!make_tmap(&ta, L.a_ptr, L.a_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
+  const int ka = L.K >> L.a_k_shift;  // row length of the weight matrix
+  if (!make_tmap(&ta, L.a_ptr, L.a_rows, ka, BLOCK_M)) return cudaErrorInvalidValue;
   if (!make_tmap(&tb, L.b_ptr, L.b_rows, L.K, B_BOX)) return cudaErrorInvalidValue;
   if (L.a_sh_ptr != nullptr) {
-    if (!make_tmap(&tash, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tash, L.a_sh_ptr, L.a_sh_rows, ka, BLOCK_M)) return cudaErrorInvalidValue;
   } else {
     tash = ta;
   }
@@ -378,6 +389,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.num_mblocks = L.num_mblocks;
   p.a_rows_per_group = L.a_rows_per_group;
   p.a_up_offset = L.a_up_offset;
+  p.a_k_shift = L.a_k_shift;
   p.out_features = L.out_features;
   p.out_ld = L.out_ld;
   p.out = L.out;

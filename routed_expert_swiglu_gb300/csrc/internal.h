@@ -42,7 +42,7 @@ struct GemmLaunch {
   const void* b_ptr; int64_t b_rows;
   const void* b_sh_ptr; int64_t b_sh_rows;
   int K;
-  int num_mblocks, a_rows_per_group, a_up_offset, out_features, out_ld;
+  int num_mblocks, a_rows_per_group, a_up_offset, a_k_shift, out_features, out_ld;
   void* out;
   const float* row_scale;
   int n_routed, shared_b_shift;

@@ -48,7 +48,7 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.inv = take((size_t)L.N * 4);
   L.row_w = take((size_t)L.N * 4);
   L.xd = take((size_t)L.N * d * 2);
-  L.h = take(rows_h * f * 2);
+  L.h = take(rows_h * 2 * f * 2);  // hi/lo bf16 pair per activation
   L.o = take(rows_h * d * 4);
   L.x_stage = take((size_t)T * d * 2);
   L.out_stage = take((size_t)T * d * 2);
@@ -238,7 +238,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.a_rows_per_group = 2 * f;
   g1.a_up_offset = f;
   g1.out_features = f;
-  g1.out_ld = f;
+  g1.out_ld = 2 * f;
   g1.out = at<void>(ws, L.h);
   g1.n_routed = E;
   g1.shared_b_shift = -L.N;
@@ -260,7 +260,8 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.a_sh_rows = d;
   g2.b_ptr = at<void>(ws, L.h);
   g2.b_rows = rows_h;
-  g2.K = f;
+  g2.K = 2 * f;        // hi and lo halves of H, each against the same W2 block
+  g2.a_k_shift = 1;
   g2.num_mblocks = ceil_div(d, 128);
   g2.a_rows_per_group = d;
   g2.out_features = d;
