@@ -1,0 +1,420 @@
+"""Benchmark of the MoE SwiGLU layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one whole layer forward (router GEMM, top-k, dispatch, gate/up grouped GEMM, down
+grouped GEMM, combine) over one batch of T synthetic tokens whose inputs are resident in HBM.
+Default workload: the DeepSeek-V4-Flash-shaped layer at T=8192 (prefill); the same line
+carries a T=64 (decode) measurement.  Multi-GPU runs are independent replicas (one process
+per GPU, each with its own token batch; no collective on the data path).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on bounded
+samples of the same workload, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+_NCORES = len(os.sched_getaffinity(0))
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_NCORES))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from routed_expert_swiglu_gb300 import cost, inputs, workloads  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["router_gemm", "topk", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def time_layer(layer, x, token_ids, steps, warmup, stream, with_stages=True):
+    """Device time of `steps` forwards (after `warmup`), with per-stage event times."""
+    nstage = len(STAGES)
+    for _ in range(warmup):
+        layer.forward(x, token_ids, out=layer._out)
+    torch.cuda.synchronize()
+    evsets = []
+    if with_stages:
+        for _ in range(steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(nstage + 1)]
+            for e in evs:
+                e.record(stream)  # materialise the CUDA events before handing them to the library
+            evsets.append(evs)
+        torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        if with_stages:
+            layer.set_events(evsets[i])
+        layer.forward(x, token_ids, out=layer._out)
+    end.record(stream)
+    torch.cuda.synchronize()
+    layer.set_events(None)
+    total_ms = start.elapsed_time(end)
+    stage_ms = None
+    if with_stages:
+        stage_ms = [sum(evs[j].elapsed_time(evs[j + 1]) for evs in evsets) / steps for j in range(nstage)]
+    return total_ms, stage_ms
+
+
+def measure_workload(w, steps, warmup, device, seed, world, rank):
+    from routed_expert_swiglu_gb300 import binding
+    inp = inputs.make_layer_inputs(w, seed=seed, device=device)
+    layer = binding.MoELayer(w, inp)
+    layer._out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream()
+    barrier(world)
+    torch.cuda.synchronize()
+    total_ms, stage_ms = time_layer(layer, inp.x, inp.token_ids, steps, warmup, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    st = layer.check_status()
+    if st != 0:
+        raise RuntimeError(f"device status {binding.STATUS_NAMES.get(st, st)} on {w.name}")
+    counts = layer.views(w.T)["counts"].cpu().numpy()
+    active = int((counts > 0).sum())
+    launches = binding.moe_forward_launch_count(layer.plan, w.T)
+    return layer, inp, total_ms, stage_ms, active, launches
+
+
+def measure_e2e(layer, inp, w, steps, warmup, world):
+    """Same metric through moe_forward_host: pinned host x in, pinned host y out, copies timed."""
+    from routed_expert_swiglu_gb300 import binding
+    x_h = inp.x.cpu().pin_memory()
+    tok_h = inp.token_ids.cpu().pin_memory() if inp.token_ids is not None else None
+    y_h = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.moe_forward_host(layer.plan, w.T, x_h, tok_h, inp.w_r, inp.bias, inp.w13, inp.w2, inp.w13_sh,
+                                 inp.w2_sh, y_h, layer.ws, stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world)
+    h2d = w.T * w.d * 2 + (w.T * 4 if inp.token_ids is not None else 0)
+    d2h = w.T * w.d * 2
+    return ms, h2d, d2h
+
+
+def gate_up_bytes(w, active):
+    """Algorithmic HBM bytes of one gate/up grouped-GEMM launch: the w13 slabs of the active
+    experts (+ shared), the dispatched rows and x it reads, h it writes (bf16)."""
+    bf = 2
+    weights = (active + w.n_shared) * 2 * w.d * w.d_ff * bf
+    acts_in = (w.N + w.n_shared * w.T) * w.d * bf
+    h_out = (w.N + w.n_shared * w.T) * w.d_ff * bf
+    return weights + acts_in + h_out
+
+
+def run_ours(args, world, rank, local):
+    from routed_expert_swiglu_gb300 import binding, build
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    binding.load()
+    peaks, peak_src = load_peaks()
+    w = workloads.BY_NAME[args.workload]
+
+    with ClockSampler(local) as clk:
+        layer, inp, total_ms, stage_ms, active, launches = measure_workload(
+            w, args.steps, args.warmup, device, seed=rank, world=world, rank=rank)
+    clocks = clk.summary()
+    ms_max = max_over_ranks(total_ms, world)
+    ms_per_step = ms_max / args.steps
+    tokens_per_s = world * w.T * args.steps / (ms_max / 1e3)
+
+    # dominant kernel: the gate/up grouped GEMM
+    g1_ms = stage_ms[STAGES.index("gate_up_gemm")]
+    g1_bytes = gate_up_bytes(w, active)
+    g1_gbs = g1_bytes / (g1_ms / 1e3) / 1e9
+    hbm_peak = float(peaks["hbm_gbs"])
+    layer_flops = cost.layer_flops(w)
+    layer_bytes = cost.layer_bytes(w, active)
+    roof_s = cost.roofline_seconds(layer_flops, layer_bytes, float(peaks["bf16_tflops_sustained"]), hbm_peak)
+    gemm_ms = stage_ms[STAGES.index("gate_up_gemm")] + stage_ms[STAGES.index("down_gemm")]
+    e2e_ms, h2d, d2h = measure_e2e(layer, inp, w, args.steps, args.warmup, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, args.cpu_tokens)
+    layer.close()
+    del layer, inp
+    torch.cuda.empty_cache()
+
+    decode = None
+    if args.decode_workload and args.decode_workload != args.workload:
+        wd = workloads.BY_NAME[args.decode_workload]
+        dl, dinp, dms, dstage, dactive, _ = measure_workload(wd, max(args.steps, 10), args.warmup, device,
+                                                             seed=rank, world=world, rank=rank)
+        dms = max_over_ranks(dms, world) / max(args.steps, 10)
+        dbytes = cost.layer_bytes(wd, dactive)
+        decode = {"workload": wd.name, "T": wd.T, "ms_per_step": round(dms, 4),
+                  "tokens_per_s": round(world * wd.T / (dms / 1e3), 1), "active_experts": dactive,
+                  "layer_bytes": int(dbytes), "hbm_gbs_layer": round(dbytes / (dms / 1e3) / 1e9, 1),
+                  "hbm_frac_layer": round(dbytes / (dms / 1e3) / 1e9 / hbm_peak, 4),
+                  "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, dstage)}}
+        dl.close()
+        del dl, dinp
+        torch.cuda.empty_cache()
+
+    line = {
+        "metric": "MoE-layer tokens/s (V4-Flash shape)",
+        "value": round(tokens_per_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the layer's shapes)",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "d_ff": w.d_ff, "E": w.E, "k": w.k,
+                   "n_shared": w.n_shared, "score": w.score, "bias": w.use_bias,
+                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (expert weights "
+                   f"{(w.E + w.n_shared) * 3 * w.d * w.d_ff * 2 / 1e9:.1f} GB)"},
+        "roofline": {"kernel": "gate_up_gemm", "bound": "hbm", "achieved": round(g1_gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(g1_gbs / hbm_peak, 4),
+                     "peak_source": peak_src, "traffic": None, "algorithmic_bytes": int(g1_bytes),
+                     "avg_ms": round(g1_ms, 4)},
+        "layer_roofline": {"flops": int(layer_flops), "bytes": int(layer_bytes), "active_experts": active,
+                           "roofline_ms": round(roof_s * 1e3, 4), "frac": round(roof_s * 1e3 / ms_per_step, 4),
+                           "peaks": f"{peaks['bf16_tflops_sustained']} TFLOP/s sustained bf16, {hbm_peak} GB/s "
+                                    f"({peak_src})"},
+        "grouped_gemm_tflops": round(cost.expert_gemm_flops(w) / (gemm_ms / 1e3) / 1e12, 1),
+        "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, stage_ms)},
+        "e2e": {"value": round(world * w.T * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / args.steps, 4), "api": "moe_forward_host"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+        "decode": decode,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+class HostLayer:
+    """The layer's inputs copied to host memory as bf16 (what a CPU implementation holds);
+    the oracle widens what it touches to fp64 as part of its own work."""
+
+    def __init__(self, inp, ntok):
+        c = lambda t: None if t is None else t.detach().cpu()  # noqa: E731
+        self.x = inp.x[:ntok].detach().cpu()
+        self.w_r, self.w13, self.w2 = c(inp.w_r), c(inp.w13), c(inp.w2)
+        self.w13_sh, self.w2_sh, self.bias = c(inp.w13_sh), c(inp.w2_sh), c(inp.bias)
+        self.tid2eid = c(inp.tid2eid)
+        self.token_ids = None if inp.token_ids is None else inp.token_ids[:ntok].detach().cpu()
+
+
+def _oracle_sample(w, h: HostLayer):
+    """Oracle on the host copy: router logits, routing, every selected expert, shared, combine."""
+    import oracle
+    f64 = lambda t: None if t is None else t.to(torch.float64).numpy()  # noqa: E731
+    x64 = f64(h.x)
+    logits = oracle.router_logits(x64, f64(h.w_r))
+    ids, wts, _ = oracle.route(logits, w.k, w.score, bias=f64(h.bias), n_groups=w.n_groups,
+                               topk_groups=w.topk_groups, group_topk=w.group_topk,
+                               token_ids=None if h.token_ids is None else h.token_ids.numpy(),
+                               tid2eid=None if h.tid2eid is None else h.tid2eid.numpy())
+    shared = None if h.w13_sh is None else (f64(h.w13_sh), f64(h.w2_sh))
+    return oracle.forward(x64, ids, wts, lambda e: (f64(h.w13[e]), f64(h.w2[e])), shared)
+
+
+def cpu_baseline(w, inp, ntok):
+    h = HostLayer(inp, ntok)
+    t0 = time.perf_counter()
+    _oracle_sample(w, h)
+    dt = time.perf_counter() - t0
+    return {"value": round(ntok / dt, 3), "unit": "tokens/s", "cores": _NCORES, "kind": "oracle",
+            "sample": f"{ntok} tokens of {w.name} (routing + every selected expert + shared + combine), "
+                      f"fp64 numpy on host copies of the bf16 inputs", "seconds": round(dt, 2)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workloads.BY_NAME[args.workload]
+    ntok = args.cpu_tokens
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    inp = inputs.make_layer_inputs(w, seed=0, device=dev, T=ntok)   # input synthesis only
+    h = HostLayer(inp, ntok)
+    del inp
+    if dev != "cpu":
+        torch.cuda.empty_cache()
+    for _ in range(args.warmup):
+        hw = HostLayer.__new__(HostLayer)
+        hw.__dict__.update(h.__dict__)
+        hw.x = h.x[:1]
+        hw.token_ids = None if h.token_ids is None else h.token_ids[:1]
+        _oracle_sample(w, hw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sample(w, h)
+    dt = time.perf_counter() - t0
+    value = args.steps * ntok / dt
+    line = {"impl": "reference", "metric": "MoE-layer tokens/s (V4-Flash shape)", "value": round(value, 3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "d_ff": w.d_ff, "E": w.E, "k": w.k,
+                       "n_shared": w.n_shared, "sample_tokens_per_step": ntok},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": _NCORES, "kind": "oracle",
+                             "sample": f"{ntok} tokens of {w.name} per step"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="v4flash_T8192", choices=sorted(workloads.BY_NAME))
+    ap.add_argument("--decode-workload", default="v4flash_T64")
+    ap.add_argument("--cpu-tokens", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
