@@ -264,7 +264,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
 
     decode = None
-    if args.decode_workload and args.decode_workload != args.workload:
+    if args.decode_workload not in ("none", args.workload):
         wd = workloads.BY_NAME[args.decode_workload]
         dl, dinp, dms, dstage, dactive, _ = measure_workload(wd, max(args.steps, 10), args.warmup, device,
                                                              seed=rank, world=world, rank=rank)
@@ -398,7 +398,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v4flash_T8192", choices=sorted(workloads.BY_NAME))
-    ap.add_argument("--decode-workload", default="v4flash_T64")
+    ap.add_argument("--decode-workload", default="v4flash_T64", help="second (decode) workload, or none")
     ap.add_argument("--cpu-tokens", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

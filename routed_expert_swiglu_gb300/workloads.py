@@ -72,6 +72,10 @@ V4PRO_HASH_T16384 = Workload("v4pro_hash_T16384", T=16384, d=7168, d_ff=3072, E=
 V4PRO_LEARNED_T16384 = Workload("v4pro_learned_T16384", T=16384, d=7168, d_ff=3072, E=384,
                                 k=6, n_shared=1, score=SCORE_SQRT_SOFTPLUS, use_bias=True)
 
+# Profiling stand-in: the V4-Flash layer's shapes with 32 experts and T=1024, i.e. the same
+# 192 rows per expert as T=8192 over 256 experts, at 1.6 GB of expert weights (> L2).
+V4FLASH_E32_T1024 = dataclasses.replace(V4FLASH_T8192, name="v4flash_E32_T1024", E=32, T=1024)
+
 ALL = (TOY, MIXTRAL_T16, MIXTRAL_T2048, V3_T4096, V4FLASH_T64, V4FLASH_T8192,
-       V4FLASH_T64_ZIPF, V4FLASH_T8192_ZIPF, V4PRO_HASH_T16384, V4PRO_LEARNED_T16384)
+       V4FLASH_T64_ZIPF, V4FLASH_T8192_ZIPF, V4PRO_HASH_T16384, V4PRO_LEARNED_T16384, V4FLASH_E32_T1024)
 BY_NAME = {w.name: w for w in ALL}
