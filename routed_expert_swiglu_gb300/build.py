@@ -39,16 +39,19 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose_ptxas: bool = False, force: bool = False) -> str:
-    """Compile every translation unit for sm_103a and link the shared library; returns its path."""
+def build(verbose_ptxas: bool = False, force: bool = False, extra_flags=(), lib_path: str = LIB_PATH,
+          build_dir: str = BUILD_DIR) -> str:
+    """Compile every translation unit for sm_103a and link the shared library; returns its path.
+    `extra_flags` (e.g. -DMOE_TN_PREFILL=256) select compile-time kernel variants; give such a
+    build its own `lib_path` and `build_dir`."""
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         if force or _stale(o, s):
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", s, "-o", o]
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o]
             if verbose_ptxas:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
@@ -59,16 +62,16 @@ def build(verbose_ptxas: bool = False, force: bool = False) -> str:
                 if res.returncode != 0:
                     raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
                 outs.append(res.stderr)
-    objs = [os.path.join(BUILD_DIR, s.replace(".cu", ".o")) for s in SOURCES]
-    if jobs or not os.path.exists(LIB_PATH):
-        tmp = LIB_PATH + ".tmp"
+    objs = [os.path.join(build_dir, s.replace(".cu", ".o")) for s in SOURCES]
+    if jobs or not os.path.exists(lib_path):
+        tmp = lib_path + ".tmp"
         res = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-        os.replace(tmp, LIB_PATH)
+        os.replace(tmp, lib_path)
     if verbose_ptxas:
         sys.stderr.write("".join(outs))
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":

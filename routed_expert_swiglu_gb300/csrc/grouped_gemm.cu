@@ -19,6 +19,7 @@
 // Tiles: for group g with R_g = ceil(rows_g / TN) row tiles, tile ids run m-block-major
 // (all row tiles of one weight slab are adjacent, so a slab re-read hits L2).
 #include <cuda.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -30,15 +31,14 @@ constexpr int BLOCK_K = 64;          // one 128-byte swizzle row of bf16
 constexpr int B_BOX = 16;            // rows per TMA box of the B operand
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = (2 + NUM_EPI_WARPS) * 32;
+constexpr int SMEM_LIMIT = 232448;   // dynamic shared memory per block on sm_103a
 enum { EPI_SWIGLU = 0, EPI_F32 = 1 };
 
 struct GemmParams {
-  int K;
-  int num_mblocks;
+  int K;                // reduction length of the weight (A) operand, multiple of 64
+  int num_mblocks;      // output-feature blocks per group (128 features, or 128*MBLK for fp32)
   int a_rows_per_group;
-  int a_up_offset;
-  int a_k_shift;        // A's K block = B's K block >> a_k_shift (1: each weight block serves two
-                        // consecutive activation blocks, the hi and lo halves of H)
+  int a_up_offset;      // SwiGLU: row offset of the up rows (W3) after the gate rows (W1)
   int out_features;
   int out_ld;
   void* out;
@@ -48,39 +48,60 @@ struct GemmParams {
   const int4* grp;      // {row_base, rows, first row tile, 0}; grp[G].z = total row tiles
   const int* rt2g;
   int n_groups_total;   // G (index of the total entry)
+  int sched_tn;         // rows per row tile of the schedule (a multiple of the kernel's TN)
   int dense_rows;
   int* err;
 };
 
-template <int EPI, int TN>
-struct GemmShape {
-  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
-  static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : 1;
-  static constexpr int B_BYTES = TN * BLOCK_K * 2;
-  static constexpr int STAGE_BYTES = NUM_A * A_BYTES + B_BYTES;
-  static constexpr int ACC_COLS = NUM_A * TN;
-  static constexpr int NUM_ACC = (2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int USED_COLS = NUM_ACC * ACC_COLS;
-  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
-                                   : USED_COLS <= 256 ? 256 : 512;
-  static_assert(USED_COLS <= 512, "TMEM holds 512 columns");
-  static_assert(TN % B_BOX == 0 && TN <= 256, "token tile");
+// Tensor maps of one launch.  The B operand has one map per box height 16 << i (i < 5), so a
+// tile of n rows is loaded with at most five boxes (binary decomposition of n / 16).
+constexpr int NUM_BOX_H = 5;
+struct GemmMaps {
+  CUtensorMap a, a_sh;
+  CUtensorMap b[NUM_BOX_H], b_sh[NUM_BOX_H];
 };
 
-template <int STAGES>
-constexpr int gemm_smem_bytes(int stage_bytes) {
-  return STAGES * stage_bytes + 1024 /* alignment slack */ + 256 /* barriers, flags */;
-}
+// Compile-time shape of one kernel variant.
+//   EPI_SWIGLU: A = gate and up slabs of 128 features each, one B tile, two accumulators.
+//   EPI_F32:    A = MBLK slabs of 128 features, MBLK accumulators; with HILO the B operand
+//               is the activation pair (hi, lo), both multiplied by the same A tile.
+template <int EPI, int TN, int MBLK, bool HILO>
+struct GemmShape {
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
+  static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
+  static constexpr int NUM_B = HILO ? 2 : 1;
+  static constexpr int B_BYTES = TN * BLOCK_K * 2;
+  static constexpr int STAGE_BYTES = NUM_A * A_BYTES + NUM_B * B_BYTES;
+  static constexpr int NACC = NUM_A;                 // accumulators per buffer, TN columns each
+  static constexpr int ACC_COLS = NACC * TN;
+  static constexpr int NUM_BUF = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int USED_COLS = NUM_BUF * ACC_COLS;
+  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
+                                   : USED_COLS <= 256 ? 256 : 512;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 256) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256 /* barriers */;
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : BLOCK_M * MBLK;  // features per tile
+  static_assert(USED_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(TN % B_BOX == 0 && TN <= 256, "token tile");
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(EPI == EPI_F32 || (MBLK == 1 && !HILO), "SwiGLU variant");
+};
 
 struct Tile {
   int g, mb, b_row, out_row, rows, n_mma;
   bool shared;
 };
 
+// Tile id -> (group, m-block, row sub-tile).  The schedule counts row tiles of sched_tn rows;
+// a kernel with a smaller TN splits each into sched_tn / TN sub-tiles, some of which may be
+// empty (rows <= 0): every role skips those identically.
 template <int TN>
 __device__ __forceinline__ Tile decode_tile(int tile, const GemmParams& p) {
   Tile t;
-  const int rt_glob = tile / p.num_mblocks;
+  const int split = p.sched_tn / TN;
+  const int per_rt = p.num_mblocks * split;
+  const int rt_glob = tile / per_rt;
   int row_base, rows_g, rt_start;
   if (p.grp != nullptr) {
     t.g = __ldg(p.rt2g + rt_glob);
@@ -94,8 +115,8 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmParams& p) {
     rows_g = p.dense_rows;
     rt_start = 0;
   }
-  const int R = (rows_g + TN - 1) / TN;
-  const int local = tile - rt_start * p.num_mblocks;
+  const int R = ((rows_g + p.sched_tn - 1) / p.sched_tn) * split;
+  const int local = tile - rt_start * per_rt;
   t.mb = local / R;
   const int rt = local - t.mb * R;
   t.rows = min(TN, rows_g - rt * TN);
@@ -106,12 +127,11 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmParams& p) {
   return t;
 }
 
-template <int EPI, int TN, int STAGES>
+template <int EPI, int TN, int MBLK, bool HILO>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
-                        const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b_sh,
-                        const GemmParams p) {
-  using S = GemmShape<EPI, TN>;
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using S = GemmShape<EPI, TN, MBLK, HILO>;
+  constexpr int STAGES = S::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
@@ -140,10 +160,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_a);
-    tma_prefetch_desc(&tm_a_sh);
-    tma_prefetch_desc(&tm_b);
-    tma_prefetch_desc(&tm_b_sh);
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a_sh);
+    for (int i = 0; i < NUM_BOX_H; ++i) {
+      if ((16 << i) <= TN) {
+        tma_prefetch_desc(&maps.b[i]);
+        tma_prefetch_desc(&maps.b_sh[i]);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
@@ -156,9 +180,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   int total_tiles;
   if (p.grp != nullptr) {
-    total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks;
+    total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks * (p.sched_tn / TN);
   } else {
-    total_tiles = ((p.dense_rows + TN - 1) / TN) * p.num_mblocks;
+    total_tiles = ((p.dense_rows + p.sched_tn - 1) / p.sched_tn) * p.num_mblocks * (p.sched_tn / TN);
   }
   const int KB = p.K / BLOCK_K;
 
@@ -170,11 +194,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const Tile t = decode_tile<TN>(tile, p);
-        const CUtensorMap* ta = t.shared ? &tm_a_sh : &tm_a;
-        const CUtensorMap* tb = t.shared ? &tm_b_sh : &tm_b;
-        const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * BLOCK_M;
-        const uint32_t bytes = S::NUM_A * S::A_BYTES + t.n_mma * BLOCK_K * 2;
-        const int nbox = t.n_mma / B_BOX;
+        if (t.rows <= 0) continue;
+        const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
+        const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
+        const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * S::FEATS;
+        const uint32_t bytes = S::NUM_A * S::A_BYTES + S::NUM_B * t.n_mma * BLOCK_K * 2;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -183,11 +207,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, bytes);
-          const int ka = (kb >> p.a_k_shift) * BLOCK_K;
-          tma_load_2d(sa, ta, fb, ka, a_row);
-          if (EPI == EPI_SWIGLU) tma_load_2d(sa + S::A_BYTES, ta, fb, ka, a_row + p.a_up_offset);
-          const uint32_t sb = sa + S::NUM_A * S::A_BYTES;
-          for (int b = 0; b < nbox; ++b) tma_load_2d(sb + b * (B_BOX * 128), tb, fb, kb * BLOCK_K, t.b_row + b * B_BOX);
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) {
+            const int row = (EPI == EPI_SWIGLU) ? a_row + a * p.a_up_offset : a_row + a * BLOCK_M;
+            tma_load_2d(sa + a * S::A_BYTES, ta, fb, kb * BLOCK_K, row);
+          }
+#pragma unroll
+          for (int bp = 0; bp < S::NUM_B; ++bp) {
+            const uint32_t sb = sa + S::NUM_A * S::A_BYTES + bp * S::B_BYTES;
+            const int kc = HILO ? kb * 2 * BLOCK_K + bp * BLOCK_K : kb * BLOCK_K;
+            int off = 0;
+#pragma unroll
+            for (int i = NUM_BOX_H - 1; i >= 0; --i) {
+              const int h = B_BOX << i;
+              if (h <= TN && (t.n_mma - off) >= h) {
+                tma_load_2d(sb + off * 128, tb + i, fb, kc, t.b_row + off);
+                off += h;
+              }
+            }
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -201,16 +239,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      int buf = 0;
+      uint32_t buf_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const Tile t = decode_tile<TN>(tile, p);
-        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.err)) break;
+        if (t.rows <= 0) continue;
+        if (!mbar_wait(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(t.n_mma);
-        const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
-        const uint32_t d1 = d0 + TN;
+        const uint32_t d0 = tmem_base + buf * S::ACC_COLS;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err)) {
             ok = false;
@@ -218,15 +256,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
-          const uint64_t da = smem_desc_sw128(sa);
-          const uint64_t du = smem_desc_sw128(sa + S::A_BYTES);
-          const uint64_t db = smem_desc_sw128(sa + S::NUM_A * S::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
-            const uint32_t accum = (kb | kk) ? 1u : 0u;
-            // advance 16 bf16 = 32 bytes along K inside the swizzle row: +2 in the >>4 field
-            tc_mma(d0, da + 2 * kk, db + 2 * kk, idesc, accum);
-            if (EPI == EPI_SWIGLU) tc_mma(d1, du + 2 * kk, db + 2 * kk, idesc, accum);
+#pragma unroll
+            for (int a = 0; a < S::NUM_A; ++a) {
+              const uint64_t da = smem_desc_sw128(sa + a * S::A_BYTES) + 2 * kk;
+#pragma unroll
+              for (int bp = 0; bp < S::NUM_B; ++bp) {
+                // advance 16 bf16 = 32 bytes along K inside the swizzle row: +2 in the >>4 field
+                const uint64_t db = smem_desc_sw128(sa + S::NUM_A * S::A_BYTES + bp * S::B_BYTES) + 2 * kk;
+                const uint32_t accum = (kb | kk | bp) ? 1u : 0u;
+                tc_mma(d0 + a * TN, da, db, idesc, accum);
+              }
+            }
           }
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) {
@@ -235,10 +277,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!ok) break;
-        tc_commit(accf_bar(acc));
-        if (++acc == S::NUM_ACC) {
-          acc = 0;
-          acc_phase ^= 1u;
+        tc_commit(accf_bar(buf));
+        if (++buf == S::NUM_BUF) {
+          buf = 0;
+          buf_phase ^= 1u;
         }
       }
     }
@@ -248,17 +290,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - 2;
     const int quad = warp & 3;      // TMEM lanes this warp may access: 32*quad .. 32*quad+31
     const int half = ew >> 2;       // which 16-column chunks: half, half+2, half+4, ...
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    int buf = 0;
+    uint32_t buf_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<TN>(tile, p);
-      if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.err)) break;
+      if (t.rows <= 0) continue;
+      if (!mbar_wait(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
       tc_fence_after();
-      const int feat = t.mb * BLOCK_M + quad * 32 + lane;
-      const bool fvalid = feat < p.out_features;
-      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + acc * S::ACC_COLS;
-      for (int c0 = half * 16; c0 < t.rows; c0 += 32) {
-        if (EPI == EPI_SWIGLU) {
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
+      const int nchunk = (t.rows + 15) >> 4;
+      if (EPI == EPI_SWIGLU) {
+        const int feat = t.mb * BLOCK_M + quad * 32 + lane;
+        // h is stored as an unevaluated pair hi + lo of bf16 values: hi = bf16(h),
+        // lo = bf16(h - hi), so the down projection sees h to ~16 significant bits.  Within
+        // each 64-feature block, hi occupies columns [128*b, 128*b + 64) and lo the next 64.
+        const int col = ((feat >> 6) << 7) + (feat & 63);
+        const bool fvalid = feat < p.out_features;
+        for (int ci = half; ci < nchunk; ci += 2) {
+          const int c0 = ci * 16;
           uint32_t rg[16], ru[16];
           tmem_ld16(tq + c0, rg);
           tmem_ld16(tq + TN + c0, ru);
@@ -266,10 +315,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           reg_fence16(rg);
           reg_fence16(ru);
           if (fvalid) {
-            // h is stored as an unevaluated pair hi + lo of bf16 values: hi = bf16(h),
-            // lo = bf16(h - hi), so the down projection sees h to ~16 significant bits.  Within
-            // each 64-feature block, hi occupies columns [128*b, 128*b + 64) and lo the next 64.
-            const int col = ((feat >> 6) << 7) + (feat & 63);
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
             const int nr = min(16, t.rows - c0);
 #pragma unroll
@@ -277,7 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (j < nr) {
                 const float g = __uint_as_float(rg[j]);
                 const float u = __uint_as_float(ru[j]);
-                const float h = g / (1.0f + expf(-g)) * u;
+                const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
                 const __nv_bfloat16 hi = __float2bfloat16_rn(h);
                 const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
                 out[(size_t)j * p.out_ld] = hi;
@@ -285,14 +330,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
             }
           }
-        } else {
+        }
+      } else {
+        const bool scaled = (p.row_scale != nullptr) && !t.shared;
+        for (int w = half; w < S::NACC * nchunk; w += 2) {
+          const int a = w / nchunk;
+          const int c0 = (w - a * nchunk) * 16;
+          const int feat = t.mb * S::FEATS + a * BLOCK_M + quad * 32 + lane;
           uint32_t r[16];
-          tmem_ld16(tq + c0, r);
+          tmem_ld16(tq + a * TN + c0, r);
           tmem_ld_wait();
           reg_fence16(r);
-          if (fvalid) {
+          if (feat < p.out_features) {
             float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
-            const bool scaled = (p.row_scale != nullptr) && !t.shared;
             const int nr = min(16, t.rows - c0);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -306,10 +356,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(acc));
-      if (++acc == S::NUM_ACC) {
-        acc = 0;
-        acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+      if (++buf == S::NUM_BUF) {
+        buf = 0;
+        buf_phase ^= 1u;
       }
     }
   }
@@ -352,44 +402,50 @@ static bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t col
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, int TN, int STAGES>
-static cudaError_t launch_variant(const GemmLaunch& L, const GemmParams& p, const CUtensorMap& a,
-                                  const CUtensorMap& ash, const CUtensorMap& b, const CUtensorMap& bsh,
-                                  cudaStream_t s) {
-  using Sh = GemmShape<EPI, TN>;
-  constexpr int smem = gemm_smem_bytes<STAGES>(Sh::STAGE_BYTES);
-  static_assert(smem <= 232448, "dynamic shared memory per block");
-  auto kern = grouped_gemm_kernel<EPI, TN, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <int EPI, int TN, int MBLK, bool HILO>
+static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, const GemmMaps& maps, cudaStream_t s) {
+  using Sh = GemmShape<EPI, TN, MBLK, HILO>;
+  static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
+  if (p.sched_tn % TN != 0) return cudaErrorInvalidValue;
+  auto kern = grouped_gemm_kernel<EPI, TN, MBLK, HILO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int grid = L.num_sms;
-  if (L.max_tiles < grid) grid = L.max_tiles;
+  const int tiles = L.max_tiles * (p.sched_tn / TN);
+  if (tiles < grid) grid = tiles;
   if (grid < 1) grid = 1;
-  kern<<<grid, NUM_THREADS, smem, s>>>(a, ash, b, bsh, p);
+  kern<<<grid, NUM_THREADS, Sh::SMEM_BYTES, s>>>(maps, p);
   return cudaGetLastError();
 }
 
+int gemm_features_per_tile(int epi, int mblk) { return epi == EPI_SWIGLU ? BLOCK_M : BLOCK_M * mblk; }
+
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
-  CUtensorMap ta, tash, tb, tbsh;
-  const int ka = L.K >> L.a_k_shift;  // row length of the weight matrix
-  if (!make_tmap(&ta, L.a_ptr, L.a_rows, ka, BLOCK_M)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tb, L.b_ptr, L.b_rows, L.K, B_BOX)) return cudaErrorInvalidValue;
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  const int kb_cols = L.hilo ? 2 * L.K : L.K;  // row length of the activation matrix
+  const int kernel_tn = L.kernel_tn > 0 ? L.kernel_tn : L.TN;
+  if (!make_tmap(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
   if (L.a_sh_ptr != nullptr) {
-    if (!make_tmap(&tash, L.a_sh_ptr, L.a_sh_rows, ka, BLOCK_M)) return cudaErrorInvalidValue;
+    if (!make_tmap(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
   } else {
-    tash = ta;
+    m.a_sh = m.a;
   }
-  if (L.b_sh_ptr != nullptr) {
-    if (!make_tmap(&tbsh, L.b_sh_ptr, L.b_sh_rows, L.K, B_BOX)) return cudaErrorInvalidValue;
-  } else {
-    tbsh = tb;
+  for (int i = 0; i < NUM_BOX_H; ++i) {
+    const int h = B_BOX << i;
+    if (h > kernel_tn) break;
+    if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h)) return cudaErrorInvalidValue;
+    if (L.b_sh_ptr != nullptr) {
+      if (!make_tmap(&m.b_sh[i], L.b_sh_ptr, L.b_sh_rows, kb_cols, h)) return cudaErrorInvalidValue;
+    } else {
+      m.b_sh[i] = m.b[i];
+    }
   }
   GemmParams p;
   p.K = L.K;
   p.num_mblocks = L.num_mblocks;
   p.a_rows_per_group = L.a_rows_per_group;
   p.a_up_offset = L.a_up_offset;
-  p.a_k_shift = L.a_k_shift;
   p.out_features = L.out_features;
   p.out_ld = L.out_ld;
   p.out = L.out;
@@ -399,14 +455,26 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.grp = L.grp;
   p.rt2g = L.rt2g;
   p.n_groups_total = L.n_routed + (L.a_sh_ptr != nullptr ? 1 : 0);
+  p.sched_tn = L.TN;
   p.dense_rows = L.dense_rows;
   p.err = L.err;
+  constexpr int TNP = MOE_TN_PREFILL;
+  constexpr int TN2 = MOE_TN_DOWN;
   if (L.epi == EPI_SWIGLU) {
-    if (L.TN == 256) return launch_variant<EPI_SWIGLU, 256, 3>(L, p, ta, tash, tb, tbsh, s);
-    return launch_variant<EPI_SWIGLU, 64, 5>(L, p, ta, tash, tb, tbsh, s);
+    if (kernel_tn == TNP) return launch_variant<EPI_SWIGLU, TNP, 1, false>(L, p, m, s);
+    if (kernel_tn == 64) return launch_variant<EPI_SWIGLU, 64, 1, false>(L, p, m, s);
+    return cudaErrorInvalidValue;
   }
-  if (L.TN == 256) return launch_variant<EPI_F32, 256, 4>(L, p, ta, tash, tb, tbsh, s);
-  return launch_variant<EPI_F32, 64, 8>(L, p, ta, tash, tb, tbsh, s);
+  if (L.hilo) {
+    if (kernel_tn == TN2 && L.mblk == MOE_G2_MBLK) return launch_variant<EPI_F32, TN2, MOE_G2_MBLK, true>(L, p, m, s);
+    if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, true>(L, p, m, s);
+    return cudaErrorInvalidValue;
+  }
+  if (kernel_tn == TNP && L.mblk == 2) return launch_variant<EPI_F32, TNP, 2, false>(L, p, m, s);
+  if (kernel_tn == TNP && L.mblk == 1) return launch_variant<EPI_F32, TNP, 1, false>(L, p, m, s);
+  if (kernel_tn == 64 && L.mblk == 2) return launch_variant<EPI_F32, 64, 2, false>(L, p, m, s);
+  if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, false>(L, p, m, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

@@ -17,8 +17,20 @@ constexpr int MAX_GROUPS = 32;
 constexpr int MAX_TOKENS = 1 << 20;
 constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch kernels
 
+// Token-tile width of the grouped GEMMs for large batches, and m-blocks (128 output features
+// each) per down-projection tile.  Compile-time so that kernel variants can be swept.
+#ifndef MOE_TN_PREFILL
+#define MOE_TN_PREFILL 256
+#endif
+#ifndef MOE_TN_DOWN
+#define MOE_TN_DOWN 128
+#endif
+#ifndef MOE_G2_MBLK
+#define MOE_G2_MBLK 2
+#endif
+
 // Token-tile width (B-operand rows per tile) of the grouped GEMMs for a batch of T tokens.
-inline int token_tile_for(int T) { return T <= 64 ? 64 : 256; }
+inline int token_tile_for(int T) { return T <= 64 ? 64 : MOE_TN_PREFILL; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -35,14 +47,17 @@ WsLayout ws_layout(const moe_config& c, int T);
 // Launchers.  Each returns cudaSuccess or the launch error; none synchronises.
 struct GemmLaunch {
   int epi;                 // 0 = SwiGLU dual accumulator -> bf16, 1 = fp32 (x optional row scale)
-  int TN;                  // token tile (64 or 256)
+  int TN;                  // rows per row tile of the schedule (and of the kernel unless kernel_tn)
+  int kernel_tn;           // 0, or a divisor of TN: the kernel splits each row tile
   // A (weights) routed / shared, B (activations) routed / shared: 2-D bf16, K innermost.
   const void* a_ptr; int64_t a_rows;
   const void* a_sh_ptr; int64_t a_sh_rows;
   const void* b_ptr; int64_t b_rows;
   const void* b_sh_ptr; int64_t b_sh_rows;
   int K;
-  int num_mblocks, a_rows_per_group, a_up_offset, a_k_shift, out_features, out_ld;
+  int hilo;                // activation operand is the (hi, lo) pair: B rows hold 2*K values
+  int mblk;                // fp32 variant: 128-feature m-blocks per tile (1 or 2)
+  int num_mblocks, a_rows_per_group, a_up_offset, out_features, out_ld;
   void* out;
   const float* row_scale;
   int n_routed, shared_b_shift;
@@ -53,6 +68,7 @@ struct GemmLaunch {
   int num_sms;
 };
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s);
+int gemm_features_per_tile(int epi, int mblk);
 
 struct TopkLaunch {
   const float* logits; const float* bias; int T, E, k, score;

@@ -155,7 +155,8 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   g.b_ptr = x;
   g.b_rows = T;
   g.K = c.d;
-  g.num_mblocks = ceil_div(c.n_experts, 128);
+  g.mblk = c.n_experts > 128 ? 2 : 1;
+  g.num_mblocks = ceil_div(c.n_experts, gemm_features_per_tile(1, g.mblk));
   g.out_features = c.n_experts;
   g.out_ld = c.n_experts;
   g.out = logits;
@@ -234,7 +235,8 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.b_sh_ptr = sh ? x : nullptr;
   g1.b_sh_rows = T;
   g1.K = d;
-  g1.num_mblocks = ceil_div(f, 128);
+  g1.mblk = 1;
+  g1.num_mblocks = ceil_div(f, gemm_features_per_tile(0, 1));
   g1.a_rows_per_group = 2 * f;
   g1.a_up_offset = f;
   g1.out_features = f;
@@ -260,9 +262,11 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.a_sh_rows = d;
   g2.b_ptr = at<void>(ws, L.h);
   g2.b_rows = rows_h;
-  g2.K = 2 * f;        // hi and lo halves of H, each against the same W2 block
-  g2.a_k_shift = 1;
-  g2.num_mblocks = ceil_div(d, 128);
+  g2.K = f;
+  g2.hilo = 1;         // B rows hold the (hi, lo) pair: 2*f values, each pair against one W2 block
+  g2.mblk = L.TN == 64 ? 1 : MOE_G2_MBLK;
+  g2.kernel_tn = L.TN == 64 ? 64 : MOE_TN_DOWN;
+  g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
   g2.a_rows_per_group = d;
   g2.out_features = d;
   g2.out_ld = d;
