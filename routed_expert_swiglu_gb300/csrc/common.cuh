@@ -142,17 +142,18 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major operand tile stored as rows of 128 bytes
-// (64 bf16) with the 128-byte swizzle that TMA's CU_TENSOR_MAP_SWIZZLE_128B writes:
-// 8-row core-matrix groups 1024 bytes apart (stride byte offset), descriptor version 1,
-// layout type 2 (128B swizzle).  The tile base must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major operand tile stored as rows of `row_bytes`
+// (128 or 64 bytes: 64 or 32 bf16) with the matching swizzle that TMA's SWIZZLE_128B /
+// SWIZZLE_64B writes: 8-row core-matrix groups 8*row_bytes apart (stride byte offset),
+// descriptor version 1, layout type 2 (128B swizzle) or 4 (64B swizzle).  The tile base must
+// be aligned to 8*row_bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw(uint32_t saddr, uint32_t row_bytes) {
   uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);        // start address >> 4, bits [0,14)
-  d |= (uint64_t)(16u >> 4) << 16;                 // leading byte offset (unused here)
-  d |= (uint64_t)(1024u >> 4) << 32;               // stride byte offset, bits [32,46)
-  d |= (uint64_t)1 << 46;                          // descriptor version, bits [46,48)
-  d |= (uint64_t)2 << 61;                          // 128-byte swizzle, bits [61,64)
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);            // start address >> 4, bits [0,14)
+  d |= (uint64_t)(16u >> 4) << 16;                     // leading byte offset (unused here)
+  d |= (uint64_t)((8u * row_bytes) >> 4) << 32;        // stride byte offset, bits [32,46)
+  d |= (uint64_t)1 << 46;                              // descriptor version, bits [46,48)
+  d |= (uint64_t)(row_bytes == 128 ? 2 : 4) << 61;     // swizzle mode, bits [61,64)
   return d;
 }
 
@@ -206,6 +207,118 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                  "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                :
                : "memory");
+}
+
+// ----------------------------------------------------------------------------- CTA pairs
+// Helpers for kernels launched as clusters of two CTAs that share one 2-SM MMA
+// (tcgen05 .cta_group::2): each CTA holds half of A (M/2 rows) and half of B (N/2 rows) in its
+// own shared memory, and the even CTA of the pair issues the MMA for both.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address, in the cluster shared-memory window, of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster, releasing this thread's prior writes
+// (and, after tcgen05.fence::before_thread_sync, its completed TMEM reads) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire (for phases completed by arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  int* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        atomicOr(err, DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// 2-D tiled TMA load into this CTA's shared memory whose completion is counted on an mbarrier
+// of either CTA of the pair (`bar_cluster` is a cluster-window address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t c0,
+                                                 int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// TMEM allocation shared by the CTA pair: one warp of EACH CTA executes these together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Instruction descriptor for a 2-SM MMA: bf16 A/B, fp32 accumulator, K-major, M = 256.
+__device__ __forceinline__ uint32_t idesc_bf16_f32_m256(uint32_t n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((256u >> 4) << 24);
+}
+
+// D[tmem of both CTAs] (+)= A[smem of both] * B[smem of both]^T; issued by one thread of the
+// even CTA.
+__device__ __forceinline__ void tc_mma_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask` when all tcgen05
+// operations issued so far by this thread complete.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// Named barrier for `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 }  // namespace moe

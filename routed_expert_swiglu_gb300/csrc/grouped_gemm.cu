@@ -27,7 +27,6 @@
 namespace moe {
 
 constexpr int BLOCK_M = 128;
-constexpr int BLOCK_K = 64;          // one 128-byte swizzle row of bf16
 constexpr int B_BOX = 16;            // rows per TMA box of the B operand
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = (2 + NUM_EPI_WARPS) * 32;
@@ -65,8 +64,11 @@ struct GemmMaps {
 //   EPI_SWIGLU: A = gate and up slabs of 128 features each, one B tile, two accumulators.
 //   EPI_F32:    A = MBLK slabs of 128 features, MBLK accumulators; with HILO the B operand
 //               is the activation pair (hi, lo), both multiplied by the same A tile.
-template <int EPI, int TN, int MBLK, bool HILO>
+//   BK:         K elements per pipeline stage: 64 (128-byte swizzle rows) or 32 (64-byte).
+template <int EPI, int TN, int MBLK, bool HILO, int BK>
 struct GemmShape {
+  static constexpr int BLOCK_K = BK;
+  static constexpr int ROW_BYTES = BK * 2;
   static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
   static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
   static constexpr int NUM_B = HILO ? 2 : 1;
@@ -86,6 +88,7 @@ struct GemmShape {
   static_assert(TN % B_BOX == 0 && TN <= 256, "token tile");
   static_assert(STAGES >= 2, "pipeline needs two stages");
   static_assert(EPI == EPI_F32 || (MBLK == 1 && !HILO), "SwiGLU variant");
+  static_assert(BK == 64 || BK == 32, "stage K");
 };
 
 struct Tile {
@@ -127,10 +130,11 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmParams& p) {
   return t;
 }
 
-template <int EPI, int TN, int MBLK, bool HILO>
+template <int EPI, int TN, int MBLK, bool HILO, int BK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using S = GemmShape<EPI, TN, MBLK, HILO>;
+  using S = GemmShape<EPI, TN, MBLK, HILO, BK>;
+  constexpr int BLOCK_K = S::BLOCK_K;
   constexpr int STAGES = S::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -215,13 +219,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int bp = 0; bp < S::NUM_B; ++bp) {
             const uint32_t sb = sa + S::NUM_A * S::A_BYTES + bp * S::B_BYTES;
-            const int kc = HILO ? kb * 2 * BLOCK_K + bp * BLOCK_K : kb * BLOCK_K;
+            // the (hi, lo) pair: per 64 features, 64 hi columns then 64 lo columns
+            const int k0 = kb * BLOCK_K;
+            const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
             int off = 0;
 #pragma unroll
             for (int i = NUM_BOX_H - 1; i >= 0; --i) {
               const int h = B_BOX << i;
               if (h <= TN && (t.n_mma - off) >= h) {
-                tma_load_2d(sb + off * 128, tb + i, fb, kc, t.b_row + off);
+                tma_load_2d(sb + off * S::ROW_BYTES, tb + i, fb, kc, t.b_row + off);
                 off += h;
               }
             }
@@ -260,11 +266,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
 #pragma unroll
             for (int a = 0; a < S::NUM_A; ++a) {
-              const uint64_t da = smem_desc_sw128(sa + a * S::A_BYTES) + 2 * kk;
+              const uint64_t da = smem_desc_sw(sa + a * S::A_BYTES, S::ROW_BYTES) + 2 * kk;
 #pragma unroll
               for (int bp = 0; bp < S::NUM_B; ++bp) {
                 // advance 16 bf16 = 32 bytes along K inside the swizzle row: +2 in the >>4 field
-                const uint64_t db = smem_desc_sw128(sa + S::NUM_A * S::A_BYTES + bp * S::B_BYTES) + 2 * kk;
+                const uint64_t db = smem_desc_sw(sa + S::NUM_A * S::A_BYTES + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
                 const uint32_t accum = (kb | kk | bp) ? 1u : 0u;
                 tc_mma(d0 + a * TN, da, db, idesc, accum);
               }
@@ -372,6 +378,321 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ============================================================================ CTA-pair variant
+// The same contractions on the 2-SM MMA (tcgen05 .cta_group::2).  A cluster of two CTAs computes
+// one tile of 256 weight rows x N token rows: CTA r holds weight rows [128 r, 128 r + 128) of the
+// tile and token rows [r N/2, r N/2 + N/2) of B, the even CTA issues the MMAs, and each CTA's
+// TMEM receives its 128 accumulator rows for all N columns.  Each SM therefore stores and reads
+// only half of B, which keeps its shared-memory bandwidth below what the tensor pipe consumes.
+//   SwiGLU: the pair covers 128 features; CTA r's weight rows are the gate rows of features
+//           [64 r, 64 r + 64) followed by the up rows of the same features, so gate and up of
+//           one feature sit in TMEM lanes i and i + 64 of one CTA (exchanged through smem).
+//   fp32:   the pair covers 256 output features, CTA r the features [128 r, 128 r + 128).
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
+struct PairShape {
+  static constexpr int BLOCK_K = BK;
+  static constexpr int ROW_BYTES = BK * 2;
+  static constexpr int HALF = TN / 2;
+  static constexpr int A_BYTES = BLOCK_M * BK * 2;
+  static constexpr int NUM_B = HILO ? 2 : 1;
+  static constexpr int B_BYTES = HALF * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + NUM_B * B_BYTES;
+  static constexpr int XCH = (EPI == EPI_SWIGLU) ? 4 : 0;           // gate/up warp pairs
+  static constexpr int XBUF_BYTES = XCH * 2 * 16 * 32 * 4;          // 2 slots of 16 x 32 fp32
+  static constexpr int ACC_COLS = TN;
+  static constexpr int NUM_BUF = (TMEM_ALLOC / ACC_COLS) >= 2 ? 2 : 1;
+  static constexpr int NUM_BARS = 2 * 0 + 4 + 4 * XCH;              // + 2*STAGES at runtime layout
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 512 - XBUF_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + XBUF_BYTES + 1024 + 512;
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : 2 * BLOCK_M;
+  static_assert(TN % 32 == 0 && TN <= 256, "pair token tile");
+  static_assert(TMEM_ALLOC >= ACC_COLS && TMEM_ALLOC <= 512, "TMEM allocation");
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(BK == 64 || BK == 32, "stage K");
+};
+
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    pair_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
+  constexpr int STAGES = S::STAGES;
+  constexpr int BLOCK_K = S::BLOCK_K;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* xbuf = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES + S::XBUF_BYTES);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], xfull[XCH][2], xempty[XCH][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4 + 4 * S::XCH);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  auto xfull_bar = [&](int x, int sl) { return bar0 + 8u * (2 * STAGES + 4 + 2 * x + sl); };
+  auto xempty_bar = [&](int x, int sl) { return bar0 + 8u * (2 * STAGES + 4 + 2 * S::XCH + 2 * x + sl); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 2 * NUM_EPI_WARPS);
+    }
+    for (int x = 0; x < S::XCH; ++x)
+      for (int sl = 0; sl < 2; ++sl) {
+        mbar_init(xfull_bar(x, sl), 32);
+        mbar_init(xempty_bar(x, sl), 32);
+      }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a_sh);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_ALLOC);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  int total_tiles;
+  if (p.grp != nullptr) {
+    total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks * (p.sched_tn / TN);
+  } else {
+    total_tiles = ((p.dense_rows + p.sched_tn - 1) / p.sched_tn) * p.num_mblocks * (p.sched_tn / TN);
+  }
+  const int KB = p.K / BLOCK_K;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const int n_mma = max(32, (t.rows + 31) & ~31);
+        const int half = n_mma >> 1;
+        const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
+        const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
+        const int base = t.shared ? 0 : t.g * p.a_rows_per_group;
+        const int a_row = (EPI == EPI_SWIGLU) ? base + t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2)
+                                              : base + t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M;
+        const int b_row = t.b_row + (int)rank * half;
+        const uint32_t bytes_pair = 2u * (S::A_BYTES + S::NUM_B * half * BLOCK_K * 2);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
+          const uint32_t fbc = mapa_shared(full_bar(stage), 0);  // the even CTA's full barrier
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes_pair);
+          const int k0 = kb * BLOCK_K;
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d_pair(sa, ta, fbc, k0, a_row);
+            tma_load_2d_pair(sa + S::A_BYTES / 2, ta, fbc, k0, a_row + p.a_up_offset);
+          } else {
+            tma_load_2d_pair(sa, ta, fbc, k0, a_row);
+          }
+#pragma unroll
+          for (int bp = 0; bp < S::NUM_B; ++bp) {
+            const uint32_t sb = sa + S::A_BYTES + bp * S::B_BYTES;
+            const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
+            int off = 0;
+#pragma unroll
+            for (int i = NUM_BOX_H - 1; i >= 0; --i) {
+              const int h = B_BOX << i;
+              if (h <= S::HALF && (half - off) >= h) {
+                tma_load_2d_pair(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off);
+                off += h;
+              }
+            }
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t buf_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const int n_mma = max(32, (t.rows + 31) & ~31);
+        if (!mbar_wait_cluster(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32_m256(n_mma);
+        const uint32_t d = tmem_base + buf * S::ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_cluster(full_bar(stage), phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
+          const uint64_t da = smem_desc_sw(sa, S::ROW_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+#pragma unroll
+            for (int bp = 0; bp < S::NUM_B; ++bp) {
+              const uint64_t db = smem_desc_sw(sa + S::A_BYTES + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
+              tc_mma_pair(d, da + 2 * kk, db, idesc, (kb | kk | bp) ? 1u : 0u);
+            }
+          }
+          tc_commit_pair_mc(empty_bar(stage), 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(accf_bar(buf), 0x3);
+        if (++buf == S::NUM_BUF) {
+          buf = 0;
+          buf_phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    const int xch = half * 2 + (quad & 1);  // SwiGLU: exchange channel of this gate/up warp pair
+    int buf = 0;
+    uint32_t buf_phase = 0;
+    uint32_t xiter = 0;                      // SwiGLU: chunks exchanged so far on this channel
+    bool ok = true;
+    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
+    for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      if (!mbar_wait_cluster(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
+      const int nchunk = (t.rows + 15) >> 4;
+      if (EPI == EPI_SWIGLU) {
+        float* xb = xbuf + xch * (2 * 16 * 32);
+        for (int ci = half; ci < nchunk; ci += 2, ++xiter) {
+          const int sl = xiter & 1;
+          const uint32_t par = (xiter >> 1) & 1u;
+          const int c0 = ci * 16;
+          if (quad >= 2) {
+            // up lanes: hand the 16 up values of this chunk to the gate warp of the channel
+            uint32_t ru[16];
+            tmem_ld16(tq + c0, ru);
+            tmem_ld_wait();
+            reg_fence16(ru);
+            if (!mbar_wait(xempty_bar(xch, sl), par ^ 1u, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xb[(sl * 16 + j) * 32 + lane] = __uint_as_float(ru[j]);
+            mbar_arrive(xfull_bar(xch, sl));
+          } else {
+            uint32_t rg[16];
+            tmem_ld16(tq + c0, rg);
+            tmem_ld_wait();
+            reg_fence16(rg);
+            if (!mbar_wait(xfull_bar(xch, sl), par, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            float u[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
+            mbar_arrive(xempty_bar(xch, sl));
+            const int feat = t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
+            if (feat < p.out_features) {
+              const int col = ((feat >> 6) << 7) + (feat & 63);
+              __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
+              const int nr = min(16, t.rows - c0);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (j < nr) {
+                  const float g = __uint_as_float(rg[j]);
+                  const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
+                  const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+                  const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+                  out[(size_t)j * p.out_ld] = hi;
+                  out[(size_t)j * p.out_ld + 64] = lo;
+                }
+              }
+            }
+          }
+        }
+        if (!ok) break;
+      } else {
+        const bool scaled = (p.row_scale != nullptr) && !t.shared;
+        const int feat = t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
+        for (int ci = half; ci < nchunk; ci += 2) {
+          const int c0 = ci * 16;
+          uint32_t r[16];
+          tmem_ld16(tq + c0, r);
+          tmem_ld_wait();
+          reg_fence16(r);
+          if (feat < p.out_features) {
+            float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+            const int nr = min(16, t.rows - c0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (j < nr) {
+                const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
+                out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf == 0 ? acce_leader0 : acce_leader1);
+      if (++buf == S::NUM_BUF) {
+        buf = 0;
+        buf_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_ALLOC);
+  }
+}
+
 // ----------------------------------------------------------------------------- host side
 
 EncodeTiledFn get_encode_fn() {
@@ -388,59 +709,111 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows, cols] (cols innermost, contiguous), box 64 x box_rows, 128-byte swizzle.
-static bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+// 2-D bf16 tensor [rows, cols] (cols innermost, contiguous), box bk x box_rows, swizzle of
+// 2*bk bytes (bk = 64: 128-byte, bk = 32: 64-byte).
+static bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows, int bk) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BLOCK_K, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, int TN, int MBLK, bool HILO>
-static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, const GemmMaps& maps, cudaStream_t s) {
-  using Sh = GemmShape<EPI, TN, MBLK, HILO>;
+template <int EPI, int TN, int MBLK, bool HILO, int BK>
+static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
+  using Sh = GemmShape<EPI, TN, MBLK, HILO, BK>;
   static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
-  if (p.sched_tn % TN != 0) return cudaErrorInvalidValue;
-  auto kern = grouped_gemm_kernel<EPI, TN, MBLK, HILO>;
+  if (p.sched_tn % TN != 0 || L.K % BK != 0) return cudaErrorInvalidValue;
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  const int kb_cols = HILO ? 2 * L.K : L.K;  // row length of the activation matrix
+  if (!make_tmap(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M, BK)) return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr) {
+    if (!make_tmap(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M, BK)) return cudaErrorInvalidValue;
+  } else {
+    m.a_sh = m.a;
+  }
+  for (int i = 0; i < NUM_BOX_H; ++i) {
+    const int h = B_BOX << i;
+    if (h > TN) break;
+    if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h, BK)) return cudaErrorInvalidValue;
+    if (L.b_sh_ptr != nullptr) {
+      if (!make_tmap(&m.b_sh[i], L.b_sh_ptr, L.b_sh_rows, kb_cols, h, BK)) return cudaErrorInvalidValue;
+    } else {
+      m.b_sh[i] = m.b[i];
+    }
+  }
+  auto kern = grouped_gemm_kernel<EPI, TN, MBLK, HILO, BK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int grid = L.num_sms;
   const int tiles = L.max_tiles * (p.sched_tn / TN);
   if (tiles < grid) grid = tiles;
   if (grid < 1) grid = 1;
-  kern<<<grid, NUM_THREADS, Sh::SMEM_BYTES, s>>>(maps, p);
+  kern<<<grid, NUM_THREADS, Sh::SMEM_BYTES, s>>>(m, p);
+  return cudaGetLastError();
+}
+
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
+static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
+  using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
+  static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
+  if (p.sched_tn % TN != 0 || L.K % BK != 0) return cudaErrorInvalidValue;
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  const int kb_cols = HILO ? 2 * L.K : L.K;
+  const int a_box = (EPI == EPI_SWIGLU) ? BLOCK_M / 2 : BLOCK_M;
+  if (!make_tmap(&m.a, L.a_ptr, L.a_rows, L.K, a_box, BK)) return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr) {
+    if (!make_tmap(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, a_box, BK)) return cudaErrorInvalidValue;
+  } else {
+    m.a_sh = m.a;
+  }
+  for (int i = 0; i < NUM_BOX_H; ++i) {
+    const int h = B_BOX << i;
+    if (h > Sh::HALF) break;
+    if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h, BK)) return cudaErrorInvalidValue;
+    if (L.b_sh_ptr != nullptr) {
+      if (!make_tmap(&m.b_sh[i], L.b_sh_ptr, L.b_sh_rows, kb_cols, h, BK)) return cudaErrorInvalidValue;
+    } else {
+      m.b_sh[i] = m.b[i];
+    }
+  }
+  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int pairs = L.num_sms / 2;
+  const int tiles = L.max_tiles * (p.sched_tn / TN);
+  if (tiles < pairs) pairs = tiles;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Sh::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, m, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 int gemm_features_per_tile(int epi, int mblk) { return epi == EPI_SWIGLU ? BLOCK_M : BLOCK_M * mblk; }
 
 cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
-  GemmMaps m;
-  memset(&m, 0, sizeof(m));
-  const int kb_cols = L.hilo ? 2 * L.K : L.K;  // row length of the activation matrix
   const int kernel_tn = L.kernel_tn > 0 ? L.kernel_tn : L.TN;
-  if (!make_tmap(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
-  if (L.a_sh_ptr != nullptr) {
-    if (!make_tmap(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M)) return cudaErrorInvalidValue;
-  } else {
-    m.a_sh = m.a;
-  }
-  for (int i = 0; i < NUM_BOX_H; ++i) {
-    const int h = B_BOX << i;
-    if (h > kernel_tn) break;
-    if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h)) return cudaErrorInvalidValue;
-    if (L.b_sh_ptr != nullptr) {
-      if (!make_tmap(&m.b_sh[i], L.b_sh_ptr, L.b_sh_rows, kb_cols, h)) return cudaErrorInvalidValue;
-    } else {
-      m.b_sh[i] = m.b[i];
-    }
-  }
   GemmParams p;
   p.K = L.K;
   p.num_mblocks = L.num_mblocks;
@@ -460,20 +833,26 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.err = L.err;
   constexpr int TNP = MOE_TN_PREFILL;
   constexpr int TN2 = MOE_TN_DOWN;
+  if (L.pair) {
+    if (L.epi == EPI_SWIGLU && kernel_tn == TNP) return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM>(L, p, s);
+    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == TN2 && L.mblk == 2)
+      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM>(L, p, s);
+    return cudaErrorInvalidValue;
+  }
   if (L.epi == EPI_SWIGLU) {
-    if (kernel_tn == TNP) return launch_variant<EPI_SWIGLU, TNP, 1, false>(L, p, m, s);
-    if (kernel_tn == 64) return launch_variant<EPI_SWIGLU, 64, 1, false>(L, p, m, s);
+    if (kernel_tn == TNP) return launch_variant<EPI_SWIGLU, TNP, 1, false, MOE_G1_BK>(L, p, s);
+    if (kernel_tn == 64) return launch_variant<EPI_SWIGLU, 64, 1, false, 64>(L, p, s);
     return cudaErrorInvalidValue;
   }
   if (L.hilo) {
-    if (kernel_tn == TN2 && L.mblk == MOE_G2_MBLK) return launch_variant<EPI_F32, TN2, MOE_G2_MBLK, true>(L, p, m, s);
-    if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, true>(L, p, m, s);
+    if (kernel_tn == TN2 && L.mblk == MOE_G2_MBLK) return launch_variant<EPI_F32, TN2, MOE_G2_MBLK, true, MOE_G2_BK>(L, p, s);
+    if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, true, 64>(L, p, s);
     return cudaErrorInvalidValue;
   }
-  if (kernel_tn == TNP && L.mblk == 2) return launch_variant<EPI_F32, TNP, 2, false>(L, p, m, s);
-  if (kernel_tn == TNP && L.mblk == 1) return launch_variant<EPI_F32, TNP, 1, false>(L, p, m, s);
-  if (kernel_tn == 64 && L.mblk == 2) return launch_variant<EPI_F32, 64, 2, false>(L, p, m, s);
-  if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, false>(L, p, m, s);
+  if (kernel_tn == TNP && L.mblk == 2) return launch_variant<EPI_F32, TNP, 2, false, 64>(L, p, s);
+  if (kernel_tn == TNP && L.mblk == 1) return launch_variant<EPI_F32, TNP, 1, false, 64>(L, p, s);
+  if (kernel_tn == 64 && L.mblk == 2) return launch_variant<EPI_F32, 64, 2, false, 64>(L, p, s);
+  if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, false, 64>(L, p, s);
   return cudaErrorInvalidValue;
 }
 

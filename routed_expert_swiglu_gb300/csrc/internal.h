@@ -23,10 +23,26 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 #define MOE_TN_PREFILL 256
 #endif
 #ifndef MOE_TN_DOWN
-#define MOE_TN_DOWN 128
+#define MOE_TN_DOWN 256
 #endif
 #ifndef MOE_G2_MBLK
 #define MOE_G2_MBLK 2
+#endif
+#ifndef MOE_G1_BK
+#define MOE_G1_BK 64
+#endif
+#ifndef MOE_G2_BK
+#define MOE_G2_BK 64
+#endif
+// CTA-pair (2-SM MMA) variants of the prefill grouped GEMMs and their TMEM columns per CTA.
+#ifndef MOE_G1_PAIR
+#define MOE_G1_PAIR 1
+#endif
+#ifndef MOE_G2_PAIR
+#define MOE_G2_PAIR 1
+#endif
+#ifndef MOE_PAIR_TMEM
+#define MOE_PAIR_TMEM 512
 #endif
 
 // Token-tile width (B-operand rows per tile) of the grouped GEMMs for a batch of T tokens.
@@ -56,6 +72,7 @@ struct GemmLaunch {
   const void* b_sh_ptr; int64_t b_sh_rows;
   int K;
   int hilo;                // activation operand is the (hi, lo) pair: B rows hold 2*K values
+  int pair;                // run on CTA pairs (2-SM MMA, 256 weight rows per tile)
   int mblk;                // fp32 variant: 128-feature m-blocks per tile (1 or 2)
   int num_mblocks, a_rows_per_group, a_up_offset, out_features, out_ld;
   void* out;

@@ -236,6 +236,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.b_sh_rows = T;
   g1.K = d;
   g1.mblk = 1;
+  g1.pair = (L.TN != 64) && MOE_G1_PAIR;
   g1.num_mblocks = ceil_div(f, gemm_features_per_tile(0, 1));
   g1.a_rows_per_group = 2 * f;
   g1.a_up_offset = f;
@@ -266,6 +267,8 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.hilo = 1;         // B rows hold the (hi, lo) pair: 2*f values, each pair against one W2 block
   g2.mblk = L.TN == 64 ? 1 : MOE_G2_MBLK;
   g2.kernel_tn = L.TN == 64 ? 64 : MOE_TN_DOWN;
+  g2.pair = (L.TN != 64) && MOE_G2_PAIR;
+  if (g2.pair) g2.mblk = 2;  // a pair tile covers 256 output features
   g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
   g2.a_rows_per_group = d;
   g2.out_features = d;
