@@ -131,6 +131,18 @@ moe_status moe_permute(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32
                        int32_t* offsets, int32_t* perm_tok, int32_t* inv, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device memory: a plugin
+ * inside a host framework that owns all device memory through its own allocator, or a
+ * latency-critical loop where cudaMalloc (which can synchronise the device) is not allowed.
+ * The source pages have no counterpart: this is an interface convenience of this library.
+ * Same outputs as moe_permute (all four must be non-NULL).  Scratch lives in a fixed
+ * ~0.33 MB array of device memory inside the library (held by every GPU that loads it until
+ * exit); T * top_k above 131072 returns MOE_ERR_UNSUPPORTED.  Every call shares that array:
+ * calls whose work overlaps on the GPU (unordered streams) race.  The first call on a device
+ * looks up the array's address; make it before any stream capture.  Nothing is allocated. */
+moe_status moe_permute_noalloc(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32_t* counts,
+                               int32_t* offsets, int32_t* perm_tok, int32_t* inv, moe_stream_t stream);
+
 /* Whole layer forward: route, dispatch, grouped SwiGLU GEMMs (routed + shared expert),
  * combine.  out [T,d] bf16.  Deterministic: no atomics in any floating-point reduction.
  * w13_sh / w2_sh are required iff n_shared = 1.  Intermediates (routing result, dispatch

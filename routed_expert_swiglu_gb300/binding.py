@@ -27,7 +27,7 @@ SCORE_CODES = {W.SCORE_SOFTMAX_TOPK: 0, W.SCORE_SOFTMAX: 1, W.SCORE_SIGMOID: 2, 
 EXPORTED = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_route", "moe_permute",
             "moe_forward", "moe_forward_routed", "moe_forward_host", "moe_check_status",
             "moe_workspace_views", "moe_forward_stage_count", "moe_plan_set_events",
-            "moe_forward_launch_count", "moe_status_string")
+            "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -75,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_plan_set_events": ([P, V, I], I),
         "moe_forward_launch_count": ([P, I], I),
         "moe_status_string": ([I], ctypes.c_char_p),
+        "moe_permute_noalloc": ([P, I, V, V, V, V, V, V], I),
     }
     for name, (argt, rest) in sig.items():
         fn = getattr(lib, name)
@@ -136,6 +137,13 @@ def moe_route(plan, T, x, token_ids, w_r, bias, topk_ids, topk_w, logits, ws, st
 def moe_permute(plan, T, topk_ids, counts, offsets, perm_tok, inv, ws, stream=None):
     _check(load().moe_permute(plan, T, _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(perm_tok), _ptr(inv),
                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(plan, T, topk_ids, counts, offsets, perm_tok, inv, stream=None):
+    """moe_permute without a workspace, for callers that may not allocate device memory (the
+    library keeps a fixed scratch array on each device; T * top_k <= 131072)."""
+    _check(load().moe_permute_noalloc(plan, T, _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(perm_tok),
+                                      _ptr(inv), _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_forward(plan, T, x, token_ids, w_r, bias, w13, w2, w13_sh, w2_sh, out, ws, stream=None):

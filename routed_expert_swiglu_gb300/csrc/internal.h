@@ -60,6 +60,9 @@ struct WsLayout {
 
 WsLayout ws_layout(const moe_config& c, int T);
 
+// The configuration a plan was created with.
+const moe_config* plan_config(const moe_plan* p);
+
 // Launchers.  Each returns cudaSuccess or the launch error; none synchronises.
 struct GemmLaunch {
   int epi;                 // 0 = SwiGLU dual accumulator -> bf16, 1 = fp32 (x optional row scale)

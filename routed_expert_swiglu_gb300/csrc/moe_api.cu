@@ -57,6 +57,8 @@ WsLayout ws_layout(const moe_config& c, int T) {
   return L;
 }
 
+const moe_config* plan_config(const moe_plan* p) { return &p->cfg; }
+
 }  // namespace moe
 
 using namespace moe;
