@@ -111,16 +111,20 @@ def _fp32_sum_sequential(vals32):
 
 
 def route(logits, k, score, bias=None, n_groups=0, topk_groups=0, group_topk=0,
-          token_ids=None, tid2eid=None):
-    """Top-k routing.  Returns (topk_ids [T,k] int32, topk_w [T,k] fp64, margin [T] fp64).
+          token_ids=None, tid2eid=None, return_order_margin=False):
+    """Top-k routing.  Returns (topk_ids [T,k] int32, topk_w [T,k] fp64, margin [T] fp64)
+    and, with return_order_margin, also order_margin [T] fp64.
 
     margin[t] is the gap between the k-th and (k+1)-th selection key (and, when groups are
     used, between the last kept and the first dropped group score), the smallest one that
-    decides the selection; +inf when nothing is decided by a comparison (hash routing, E=k).
+    decides WHICH experts are selected; order_margin[t] is the smallest gap between two
+    consecutive selected keys, which decides the ORDER they are listed in.  Both are +inf
+    when nothing is decided by a comparison (hash routing, E=k, k=1).
     """
     logits = np.asarray(logits, np.float64)
     T, E = logits.shape
     s = affinity(logits, score)
+    order_margin = np.full(T, np.inf)
     if tid2eid is not None:
         # HashTopK: ids looked up by token id, in table order; no comparison decides them.
         ids = np.asarray(tid2eid)[np.asarray(token_ids, np.int64)].astype(np.int32)
@@ -145,6 +149,9 @@ def route(logits, k, score, bias=None, n_groups=0, topk_groups=0, group_topk=0,
             expert_mask = np.repeat(group_mask, gsize, axis=1)
             key32 = np.where(expert_mask, key32, np.float32(-np.inf))
         ids = _topk_desc(key32, k).astype(np.int32)
+        sel_keys = np.take_along_axis(key32, ids.astype(np.int64), axis=1).astype(np.float64)
+        if k > 1:
+            order_margin = np.min(sel_keys[:, :-1] - sel_keys[:, 1:], axis=1)
         if k < E:
             ks = -np.sort(-key32, axis=1)
             kth, nxt = ks[:, k - 1].astype(np.float64), ks[:, k].astype(np.float64)
@@ -156,6 +163,8 @@ def route(logits, k, score, bias=None, n_groups=0, topk_groups=0, group_topk=0,
     else:
         sel = s[rows, ids]
         w = sel / np.maximum(sel.sum(axis=1, keepdims=True), DENOM_MIN)
+    if return_order_margin:
+        return ids, w, margin, order_margin
     return ids, w, margin
 
 

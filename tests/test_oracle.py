@@ -108,6 +108,18 @@ def test_bias_selects_but_does_not_weight():
     assert ids0[0].tolist() == [0, 1]
 
 
+def test_order_margin_is_the_smallest_gap_between_selected_keys():
+    g = golden("router_worked_example.json")
+    _, _, margin, om = oracle.route(np.array([g["scores"]]), 2, "softmax_topk", return_order_margin=True)
+    assert om[0] == pytest.approx(2.1 - 1.2, abs=1e-6) and margin[0] == pytest.approx(0.4, abs=1e-6)
+    ids, _, margin, om = oracle.route(np.array([[3.0, 2.0, 2.0005, 0.0]]), 3, "softmax_topk",
+                                      return_order_margin=True)
+    assert ids[0].tolist() == [0, 2, 1]
+    assert om[0] == pytest.approx(0.0005, abs=1e-6) and margin[0] == pytest.approx(2.0, abs=1e-6)
+    _, _, _, om = oracle.route(np.array([[1.0, 0.0]]), 1, "softmax_topk", return_order_margin=True)
+    assert np.isinf(om[0])
+
+
 def test_topk_ties_go_to_lower_id_and_order_is_descending():
     ids, _, margin = oracle.route(np.array([[1.0, 2.0, 2.0, 0.0, 2.0]]), 2, "softmax_topk")
     assert ids[0].tolist() == [1, 2] and margin[0] == 0.0
