@@ -64,8 +64,8 @@ def test_full_size_layer(w):
     gids = v["topk_ids"].cpu().numpy()
     check_permutation(w, gids, v["counts"].cpu().numpy(), v["offsets"].cpu().numpy(),
                       v["perm_tok"].cpu().numpy(), v["inv"].cpu().numpy())
-    _, rids, rw, margin = oracle_route(w, inp)
-    same = check_routing(w, gids, v["topk_w"].cpu().numpy(), rids, rw, margin)
+    _, rids, rw, margin, omargin = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, gids, v["topk_w"].cpu().numpy(), rids, rw, margin, omargin)
     rng = np.random.default_rng(1234)
     cand = np.nonzero(same)[0]
     tok = np.sort(rng.choice(cand, size=min(SAMPLE, cand.size), replace=False))

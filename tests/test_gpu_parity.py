@@ -49,12 +49,12 @@ def test_router_logits_and_routing(w):
     layer = binding.MoELayer(w, inp)
     ids, wts, logits = layer.route(inp.x, inp.token_ids, with_logits=True)
     assert layer.check_status() == 0
-    ref_logits, rids, rw, margin = oracle_route(w, inp)
+    ref_logits, rids, rw, margin, omargin = oracle_route(w, inp, with_order=True)
     # fp32 accumulation of d bf16 products: error bounded by a few ulps of sum |x_i w_i|
     bound = np.abs(to64(inp.x)) @ np.abs(to64(inp.w_r)).T
     err = np.abs(logits.double().cpu().numpy() - ref_logits)
     assert (err <= 1e-5 * bound + 1e-6).all(), f"logit error {(err / (bound + 1e-6)).max():.3e} of sum|xw|"
-    same = check_routing(w, ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, margin)
+    same = check_routing(w, ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, margin, omargin)
     print(f"{w.name}: {int((~same).sum())} tokens inside the margin routed differently; "
           f"{int((margin <= 1e-3).sum())} tokens within margin")
     layer.close()
@@ -128,8 +128,8 @@ def test_forward_vs_oracle(w):
     y = layer.forward(inp.x, inp.token_ids)
     assert layer.check_status() == 0
     v = layer.views(w.T)
-    _, rids, rw, margin = oracle_route(w, inp)
-    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin)
+    _, rids, rw, margin, omargin = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, omargin)
     fetch = ExpertFetcher(inp)
     tok = np.nonzero(same)[0]
     ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
