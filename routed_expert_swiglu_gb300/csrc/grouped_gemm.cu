@@ -211,10 +211,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, bytes);
+          if (EPI == EPI_SWIGLU) {
+            // gate and up slabs in one 3-D box: (k, row within the gate/up half, 2*expert + half)
+            tma_load_3d(sa, ta, fb, kb * BLOCK_K, t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);
+          } else {
 #pragma unroll
-          for (int a = 0; a < S::NUM_A; ++a) {
-            const int row = (EPI == EPI_SWIGLU) ? a_row + a * p.a_up_offset : a_row + a * BLOCK_M;
-            tma_load_2d(sa + a * S::A_BYTES, ta, fb, kb * BLOCK_K, row);
+            for (int a = 0; a < S::NUM_A; ++a) tma_load_2d(sa + a * S::A_BYTES, ta, fb, kb * BLOCK_K, a_row + a * BLOCK_M);
           }
 #pragma unroll
           for (int bp = 0; bp < S::NUM_B; ++bp) {
@@ -507,8 +509,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes_pair);
           const int k0 = kb * BLOCK_K;
           if (EPI == EPI_SWIGLU) {
-            tma_load_2d_pair(sa, ta, fbc, k0, a_row);
-            tma_load_2d_pair(sa + S::A_BYTES / 2, ta, fbc, k0, a_row + p.a_up_offset);
+            // this CTA's gate and up slabs (64 features each) in one 3-D box
+            tma_load_3d_pair(sa, ta, fbc, k0, t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2), t.shared ? 0 : 2 * t.g);
           } else {
             tma_load_2d_pair(sa, ta, fbc, k0, a_row);
           }
@@ -725,6 +727,36 @@ static bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t col
   return r == CUDA_SUCCESS;
 }
 
+// The fused gate/up weight [groups, 2*d_ff, K] viewed as 3-D (K, d_ff, 2*groups): one box of
+// (bk, box_rows, 2) brings the gate rows and the up rows of the same features.
+static bool make_tmap_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t cols,
+                             int box_rows, int bk) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(d_ff * cols * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)bk, (cuuint32_t)box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// A-operand maps of a launch: 2-D row slabs, or the gate/up 3-D view for SwiGLU.
+static bool make_a_maps(GemmMaps& m, const GemmLaunch& L, bool swiglu, int box_rows, int bk) {
+  if (swiglu) {
+    const int64_t f = L.a_up_offset;
+    if (!make_tmap_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, L.K, box_rows, bk)) return false;
+    if (L.a_sh_ptr != nullptr) return make_tmap_gateup(&m.a_sh, L.a_sh_ptr, 1, f, L.K, box_rows, bk);
+  } else {
+    if (!make_tmap(&m.a, L.a_ptr, L.a_rows, L.K, box_rows, bk)) return false;
+    if (L.a_sh_ptr != nullptr) return make_tmap(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, box_rows, bk);
+  }
+  m.a_sh = m.a;
+  return true;
+}
+
 template <int EPI, int TN, int MBLK, bool HILO, int BK>
 static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
   using Sh = GemmShape<EPI, TN, MBLK, HILO, BK>;
@@ -733,12 +765,7 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   GemmMaps m;
   memset(&m, 0, sizeof(m));
   const int kb_cols = HILO ? 2 * L.K : L.K;  // row length of the activation matrix
-  if (!make_tmap(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M, BK)) return cudaErrorInvalidValue;
-  if (L.a_sh_ptr != nullptr) {
-    if (!make_tmap(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M, BK)) return cudaErrorInvalidValue;
-  } else {
-    m.a_sh = m.a;
-  }
+  if (!make_a_maps(m, L, EPI == EPI_SWIGLU, BLOCK_M, BK)) return cudaErrorInvalidValue;
   for (int i = 0; i < NUM_BOX_H; ++i) {
     const int h = B_BOX << i;
     if (h > TN) break;
@@ -769,12 +796,7 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
   memset(&m, 0, sizeof(m));
   const int kb_cols = HILO ? 2 * L.K : L.K;
   const int a_box = (EPI == EPI_SWIGLU) ? BLOCK_M / 2 : BLOCK_M;
-  if (!make_tmap(&m.a, L.a_ptr, L.a_rows, L.K, a_box, BK)) return cudaErrorInvalidValue;
-  if (L.a_sh_ptr != nullptr) {
-    if (!make_tmap(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, a_box, BK)) return cudaErrorInvalidValue;
-  } else {
-    m.a_sh = m.a;
-  }
+  if (!make_a_maps(m, L, EPI == EPI_SWIGLU, a_box, BK)) return cudaErrorInvalidValue;
   for (int i = 0; i < NUM_BOX_H; ++i) {
     const int h = B_BOX << i;
     if (h > Sh::HALF) break;
