@@ -48,6 +48,9 @@ struct GemmParams {
   const int* rt2g;
   int n_groups_total;   // G (index of the total entry)
   int sched_tn;         // rows per row tile of the schedule (a multiple of the kernel's TN)
+  int ksplit;           // dense (router) schedule only: K split into ksplit slices, slice s
+                        // writing its partial result at out + s * split_stride
+  long long split_stride;
   int dense_rows;
   int* err;
 };
@@ -188,7 +191,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     total_tiles = ((p.dense_rows + p.sched_tn - 1) / p.sched_tn) * p.num_mblocks * (p.sched_tn / TN);
   }
-  const int KB = p.K / BLOCK_K;
+  // split-K (dense schedule only): tile id = base tile * ksplit + slice
+  const int ksplit = p.ksplit;
+  total_tiles *= ksplit;
+  const int KBS = p.K / BLOCK_K / ksplit;  // k-blocks per slice
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -197,13 +203,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile<TN>(tile, p);
+        const Tile t = decode_tile<TN>(tile / ksplit, p);
         if (t.rows <= 0) continue;
+        const int kb0 = (tile % ksplit) * KBS;
         const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
         const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
         const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * S::FEATS;
         const uint32_t bytes = S::NUM_A * S::A_BYTES + S::NUM_B * t.n_mma * BLOCK_K * 2;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb0 + KBS; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
@@ -215,8 +222,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // gate and up slabs in one 3-D box: (k, row within the gate/up half, 2*expert + half)
             tma_load_3d(sa, ta, fb, kb * BLOCK_K, t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);
           } else {
-#pragma unroll
-            for (int a = 0; a < S::NUM_A; ++a) tma_load_2d(sa + a * S::A_BYTES, ta, fb, kb * BLOCK_K, a_row + a * BLOCK_M);
+            // the MBLK weight slabs are consecutive rows: one box of MBLK * 128 rows
+            tma_load_2d(sa, ta, fb, kb * BLOCK_K, a_row);
           }
 #pragma unroll
           for (int bp = 0; bp < S::NUM_B; ++bp) {
@@ -251,13 +258,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t buf_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile<TN>(tile, p);
+        const Tile t = decode_tile<TN>(tile / ksplit, p);
         if (t.rows <= 0) continue;
         if (!mbar_wait(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(t.n_mma);
         const uint32_t d0 = tmem_base + buf * S::ACC_COLS;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = 0; kb < KBS; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err)) {
             ok = false;
             break;
@@ -301,8 +308,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int buf = 0;
     uint32_t buf_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile<TN>(tile, p);
+      const Tile t = decode_tile<TN>(tile / ksplit, p);
       if (t.rows <= 0) continue;
+      const long long out_shift = (long long)(tile % ksplit) * p.split_stride;
       if (!mbar_wait(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
@@ -350,7 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           reg_fence16(r);
           if (feat < p.out_features) {
-            float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+            float* out = static_cast<float*>(p.out) + out_shift + (size_t)(t.out_row + c0) * p.out_ld + feat;
             const int nr = min(16, t.rows - c0);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -765,7 +773,10 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   GemmMaps m;
   memset(&m, 0, sizeof(m));
   const int kb_cols = HILO ? 2 * L.K : L.K;  // row length of the activation matrix
-  if (!make_a_maps(m, L, EPI == EPI_SWIGLU, BLOCK_M, BK)) return cudaErrorInvalidValue;
+  if (!make_a_maps(m, L, EPI == EPI_SWIGLU, EPI == EPI_SWIGLU ? BLOCK_M : BLOCK_M * MBLK, BK))
+    return cudaErrorInvalidValue;
+  const int KB = L.K / BK;
+  if (p.ksplit < 1 || KB % p.ksplit != 0 || (p.ksplit > 1 && p.grp != nullptr)) return cudaErrorInvalidValue;
   for (int i = 0; i < NUM_BOX_H; ++i) {
     const int h = B_BOX << i;
     if (h > TN) break;
@@ -780,7 +791,7 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int grid = L.num_sms;
-  const int tiles = L.max_tiles * (p.sched_tn / TN);
+  const int tiles = L.max_tiles * (p.sched_tn / TN) * p.ksplit;
   if (tiles < grid) grid = tiles;
   if (grid < 1) grid = 1;
   kern<<<grid, NUM_THREADS, Sh::SMEM_BYTES, s>>>(m, p);
@@ -851,6 +862,8 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.rt2g = L.rt2g;
   p.n_groups_total = L.n_routed + (L.a_sh_ptr != nullptr ? 1 : 0);
   p.sched_tn = L.TN;
+  p.ksplit = L.ksplit > 0 ? L.ksplit : 1;
+  p.split_stride = L.split_stride;
   p.dense_rows = L.dense_rows;
   p.err = L.err;
   constexpr int TNP = MOE_TN_PREFILL;
@@ -869,6 +882,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   if (L.hilo) {
     if (kernel_tn == TN2 && L.mblk == MOE_G2_MBLK) return launch_variant<EPI_F32, TN2, MOE_G2_MBLK, true, MOE_G2_BK>(L, p, s);
     if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, true, 64>(L, p, s);
+    if (kernel_tn == 64 && L.mblk == 2) return launch_variant<EPI_F32, 64, 2, true, 64>(L, p, s);
     return cudaErrorInvalidValue;
   }
   if (kernel_tn == TNP && L.mblk == 2) return launch_variant<EPI_F32, TNP, 2, false, 64>(L, p, s);

@@ -60,6 +60,10 @@ struct WsLayout {
 
 WsLayout ws_layout(const moe_config& c, int T);
 
+// K slices of the router GEMM for a batch of T tokens: few token tiles -> split K so that
+// enough SMs stream the router weight; partial logits are summed in slice order by top-k.
+int router_ksplit(const moe_config& c, int T);
+
 // The configuration a plan was created with.
 const moe_config* plan_config(const moe_plan* p);
 
@@ -83,6 +87,8 @@ struct GemmLaunch {
   int n_routed, shared_b_shift;
   const int4* grp; const int* rt2g;
   int dense_rows;
+  int ksplit;              // dense schedule: split K into this many slices (0 or 1: none)
+  long long split_stride;  // elements between the partial outputs of consecutive slices
   int max_tiles;           // upper bound on the tile count (grid sizing)
   int* err;
   int num_sms;
@@ -91,7 +97,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s);
 int gemm_features_per_tile(int epi, int mblk);
 
 struct TopkLaunch {
-  const float* logits; const float* bias; int T, E, k, score;
+  const float* logits;     // nsplit partial [T, E] slabs, split_stride elements apart
+  int nsplit; long long split_stride;
+  float* logits_out;       // optional: the summed logits (only written when nsplit > 1)
+  const float* bias; int T, E, k, score;
   int n_groups, topk_groups, group_topk;
   const int32_t* token_ids; const int32_t* tid2eid; int vocab;
   int32_t* topk_ids; float* topk_w; int* err;

@@ -38,7 +38,7 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.err = take(256);
   L.topk_ids = take((size_t)T * k * 4);
   L.topk_w = take((size_t)T * k * 4);
-  L.logits = take((size_t)T * E * 4);
+  L.logits = take((size_t)router_ksplit(c, T) * T * E * 4);  // partial logits of the K slices
   L.blockhist = take((size_t)L.nblk * E * 4);
   L.counts = take((size_t)E * 4);
   L.offsets = take((size_t)(E + 1) * 4);
@@ -58,6 +58,20 @@ WsLayout ws_layout(const moe_config& c, int T) {
 }
 
 const moe_config* plan_config(const moe_plan* p) { return &p->cfg; }
+
+int router_ksplit(const moe_config& c, int T) {
+  if (T <= 0) return 1;
+  const int mblk = c.n_experts > 128 ? 2 : 1;
+  const int base_tiles = ceil_div(T, token_tile_for(T)) * ceil_div(c.n_experts, gemm_features_per_tile(1, mblk));
+  if (base_tiles >= 64) return 1;
+  int want = 128 / base_tiles;
+  if (want > 16) want = 16;
+  const int KB = c.d / 64;
+  int ks = 1;
+  for (int q = 1; q <= want; ++q)
+    if (KB % q == 0) ks = q;
+  return ks;
+}
 
 }  // namespace moe
 
@@ -164,13 +178,20 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   g.out = logits;
   g.n_routed = 1;
   g.dense_rows = T;
+  g.ksplit = router_ksplit(c, T);
+  g.split_stride = (long long)T * c.n_experts;
+  if (g.ksplit > 1) g.out = at<float>(ws, L.logits);  // partial slabs; top-k sums them
   g.max_tiles = ceil_div(T, L.TN) * g.num_mblocks;
   g.err = err;
   g.num_sms = sms;
   MOE_CUDA(launch_grouped_gemm(g, s));
   record(p, ST_ROUTER_GEMM, s);
   TopkLaunch tk;
-  tk.logits = logits;
+  tk.nsplit = g.ksplit;
+  tk.split_stride = g.split_stride;
+  tk.logits = g.ksplit > 1 ? at<float>(ws, L.logits) : logits;
+  // summed logits go to the caller's buffer, or in place into slab 0 of the workspace
+  tk.logits_out = g.ksplit > 1 ? logits : nullptr;
   tk.bias = bias;
   tk.T = T;
   tk.E = c.n_experts;
@@ -267,7 +288,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.b_rows = rows_h;
   g2.K = f;
   g2.hilo = 1;         // B rows hold the (hi, lo) pair: 2*f values, each pair against one W2 block
-  g2.mblk = L.TN == 64 ? 1 : MOE_G2_MBLK;
+  g2.mblk = L.TN == 64 ? 2 : MOE_G2_MBLK;
   g2.kernel_tn = L.TN == 64 ? 64 : MOE_TN_DOWN;
   g2.pair = (L.TN != 64) && MOE_G2_PAIR;
   if (g2.pair) g2.mblk = 2;  // a pair tile covers 256 output features

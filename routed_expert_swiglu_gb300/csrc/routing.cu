@@ -59,13 +59,34 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
   const int t = blockIdx.x * TOPK_WARPS + warp;
   if (t >= a.T) return;  // whole warp leaves together
   const int E = a.E, k = a.k, mode = a.score;
-  const float* lrow = a.logits + (size_t)t * E;
+  const float* lrow = a.logits + (size_t)t * E;  // slab 0; slab s at + s * split_stride
 
   float l[MAX_PER_LANE], sc[MAX_PER_LANE], key[MAX_PER_LANE];
+  // Router logits; with split-K the partial slabs are summed in slice order (slice-outer loop:
+  // the loads of one slice are independent).  Plain loads: the sum may be written back over
+  // slab 0 of this row.
 #pragma unroll
   for (int i = 0; i < MAX_PER_LANE; ++i) {
     const int e = lane + 32 * i;
-    l[i] = (e < E) ? __ldg(lrow + e) : -INFINITY;
+    l[i] = (e < E) ? lrow[e] : -INFINITY;
+  }
+  for (int sp = 1; sp < a.nsplit; ++sp) {
+    const float* q = lrow + (size_t)sp * a.split_stride;
+    float pv[MAX_PER_LANE];
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      pv[i] = (e < E) ? q[e] : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) l[i] += pv[i];
+  }
+  if (a.nsplit > 1 && a.logits_out != nullptr) {
+#pragma unroll
+    for (int i = 0; i < MAX_PER_LANE; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) a.logits_out[(size_t)t * E + e] = l[i];
+    }
   }
   // unbiased scores (softmax_topk: the logits themselves)
   if (mode == MOE_SCORE_SOFTMAX) {
