@@ -23,6 +23,9 @@ What the layer computes (source pages, by title and section):
   * Dispatch: expert-major rows, permuted_token_ids / tokens_per_expert -- "Mixture of
     Experts: router, token dispatch, grouped GEMM", section "Token Dispatch".
   * Combine: y[token] += weight * expert_output[position] -- same page, "Token Combine".
+  * Selection-bias update (aux-loss-free balancing): after a step, an overloaded expert's bias
+    drops by gamma and an underloaded one's rises by gamma (gamma = 0.001) -- "MoE compute and
+    communication", section 七.3; "DeepSeek-V4 MoE", section "负载均衡为什么要 Auxiliary-Loss-Free".
 
 Readings where the pages are silent (each is listed with its reason in the design notes):
   * Selection keys are compared in fp32 (the kernel's precision), ties go to the lower
@@ -35,6 +38,9 @@ Readings where the pages are silent (each is listed with its reason in the desig
     selected logits; the renormalising denominator is clamped to >= 1e-30.
   * Group membership is contiguous: group g holds experts [g*E/G, (g+1)*E/G).
   * Shared experts are added with weight 1 after the routed sum.
+  * Bias update: "overloaded" / "underloaded" are relative to the mean load T*k/E (compared
+    exactly in integers); an expert exactly at the mean keeps its bias; the bias is fp32 and
+    the update is one fp32 addition (the kernel's precision).
 """
 from __future__ import annotations
 
@@ -251,3 +257,17 @@ def forward(x, topk_ids, topk_w, expert_weights, shared_weights=None, tokens=Non
     if shared_weights is not None:
         y += swiglu_expert(x_s, shared_weights[0], shared_weights[1], cast_h)
     return y
+
+
+# ----------------------------------------------------------------------------- balancing
+
+def bias_update(counts, bias, total_assignments, gamma=0.001):
+    """Aux-loss-free bias step: b_e - gamma if expert e received more than the mean load,
+    b_e + gamma if fewer, unchanged at the mean.  counts [E] int, bias [E] fp32; returns the
+    new fp32 bias (one fp32 addition per expert)."""
+    counts = np.asarray(counts, np.int64)
+    E = counts.shape[0]
+    b = np.asarray(bias, np.float32)
+    excess = counts * E - int(total_assignments)          # sign of count - T*k/E, exactly
+    step = np.where(excess > 0, -gamma, np.where(excess < 0, gamma, 0.0)).astype(np.float32)
+    return (b + step).astype(np.float32)

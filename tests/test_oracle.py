@@ -358,3 +358,33 @@ def test_cost_model_matches_printed_tables():
     for name, tab in g["expected_active_experts"].items():
         for B, v in zip(tab["B"], tab["value"]):
             assert cost.expected_active_experts(tab["E"], tab["k"], B) == pytest.approx(v, abs=g["printed_precision"])
+
+
+# ----------------------------------------------------------------------------- balancing
+
+def test_bias_update_direction_and_step():
+    """'MoE compute and communication' 七.3: overloaded b - gamma, underloaded b + gamma, 0.001."""
+    counts = np.array([5, 1, 2, 0])            # T*k = 8 over E = 4: mean load 2
+    bias = np.array([0.5, -0.25, 0.125, 0.0], np.float32)
+    new = oracle.bias_update(counts, bias, total_assignments=8)
+    assert new.dtype == np.float32
+    assert new[0] == np.float32(0.5) - np.float32(0.001)     # overloaded
+    assert new[1] == np.float32(-0.25) + np.float32(0.001)   # underloaded
+    assert new[2] == np.float32(0.125)                       # exactly at the mean
+    assert new[3] == np.float32(0.001)
+
+
+def test_bias_update_moves_selection_towards_balance():
+    """Repeated steps on a skewed router reduce the load spread (the loop the pages describe)."""
+    rng = np.random.default_rng(21)
+    T, E, k = 512, 16, 2
+    logits = rng.normal(size=(T, E)) + np.linspace(1.0, -1.0, E)   # hot low-id experts
+    bias = np.zeros(E, np.float32)
+    spread0 = None
+    for step in range(300):
+        ids, _, _ = oracle.route(logits, k, "sigmoid", bias=bias)
+        counts = np.bincount(ids.reshape(-1), minlength=E)
+        if spread0 is None:
+            spread0 = counts.max() - counts.min()
+        bias = oracle.bias_update(counts, bias, T * k, gamma=0.01)
+    assert counts.max() - counts.min() < spread0 / 2
