@@ -143,6 +143,15 @@ moe_status moe_permute(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32
 moe_status moe_permute_noalloc(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32_t* counts,
                                int32_t* offsets, int32_t* perm_tok, int32_t* inv, moe_stream_t stream);
 
+/* Aux-loss-free selection-bias step ("MoE compute and communication", sec. 七.3; "DeepSeek-V4
+ * MoE", aux-loss-free balancing, update speed 0.001): for each expert e with load counts[e]
+ * (tokens_per_expert of a T-token step, e.g. from moe_permute or moe_workspace_views),
+ * bias[e] -= gamma if counts[e] > T*k/E, bias[e] += gamma if counts[e] < T*k/E, unchanged at
+ * the mean (compared exactly in integers; one fp32 addition).  counts [E] int32 and bias [E]
+ * fp32 (updated in place) are device pointers; gamma >= 0 (0.001 in the pages). */
+moe_status moe_update_bias(moe_plan* plan, int32_t T, const int32_t* counts, float* bias, float gamma,
+                           moe_stream_t stream);
+
 /* Whole layer forward: route, dispatch, grouped SwiGLU GEMMs (routed + shared expert),
  * combine.  out [T,d] bf16.  Deterministic: no atomics in any floating-point reduction.
  * w13_sh / w2_sh are required iff n_shared = 1.  Intermediates (routing result, dispatch

@@ -27,7 +27,8 @@ SCORE_CODES = {W.SCORE_SOFTMAX_TOPK: 0, W.SCORE_SOFTMAX: 1, W.SCORE_SIGMOID: 2, 
 EXPORTED = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_route", "moe_permute",
             "moe_forward", "moe_forward_routed", "moe_forward_host", "moe_check_status",
             "moe_workspace_views", "moe_forward_stage_count", "moe_plan_set_events",
-            "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc")
+            "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc",
+            "moe_update_bias")
 
 
 class MoEError(RuntimeError):
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward_launch_count": ([P, I], I),
         "moe_status_string": ([I], ctypes.c_char_p),
         "moe_permute_noalloc": ([P, I, V, V, V, V, V, V], I),
+        "moe_update_bias": ([P, I, V, V, ctypes.c_float, V], I),
     }
     for name, (argt, rest) in sig.items():
         fn = getattr(lib, name)
@@ -144,6 +146,12 @@ def moe_permute_noalloc(plan, T, topk_ids, counts, offsets, perm_tok, inv, strea
     library keeps a fixed scratch array on each device; T * top_k <= 131072)."""
     _check(load().moe_permute_noalloc(plan, T, _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(perm_tok),
                                       _ptr(inv), _stream(stream)), "moe_permute_noalloc")
+
+
+def moe_update_bias(plan, T, counts, bias, gamma=0.001, stream=None):
+    """In-place aux-loss-free bias step from the per-expert loads of a T-token step."""
+    _check(load().moe_update_bias(plan, T, _ptr(counts), _ptr(bias), ctypes.c_float(gamma), _stream(stream)),
+           "moe_update_bias")
 
 
 def moe_forward(plan, T, x, token_ids, w_r, bias, w13, w2, w13_sh, w2_sh, out, ws, stream=None):
