@@ -422,7 +422,12 @@ struct PairShape {
   static_assert(BK == 64 || BK == 32, "stage K");
 };
 
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
+// NP = CTA pairs per cluster.  With NP = 2 the two pairs of a cluster work on the same token
+// rows and on adjacent feature blocks; each CTA TMA-loads a quarter of the token rows and
+// multicasts it to the CTA holding the same half in the other pair, so each SM requests only
+// half of its B half.  The multicast's bytes are counted on each destination pair's even-CTA
+// barrier, and a stage is refilled only after both pairs' MMAs released it.
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
@@ -445,13 +450,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = crank & 1u;    // position in the CTA pair
+  const uint32_t pp = crank >> 1;      // which pair of the cluster
+  const uint32_t lrank = crank & ~1u;  // cluster rank of this pair's even CTA
   const bool leader = (rank == 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(full_bar(s), 1);      // the even CTA's expect-tx arrival
+      mbar_init(empty_bar(s), NP);  // one commit per pair of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
@@ -479,8 +487,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
+  const int pair = blockIdx.x / (2 * NP);   // cluster index
+  const int npairs = gridDim.x / (2 * NP);  // clusters
   int total_tiles;
   if (p.grp != nullptr) {
     total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks * (p.sched_tn / TN);
@@ -498,40 +506,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
         const Tile t = decode_tile<TN>(tile, p);
         if (t.rows <= 0) continue;
-        const int n_mma = max(32, (t.rows + 31) & ~31);
-        const int half = n_mma >> 1;
+        const int mb = t.mb * NP + (int)pp;  // this pair's feature block
+        const int unit = 32 * NP;
+        const int n_mma = max(unit, (t.rows + unit - 1) / unit * unit);
+        const int half = n_mma >> 1;         // token rows per CTA
+        const int qh = half / NP;            // token rows this CTA loads (NP = 2: multicast)
         const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
         const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
         const int base = t.shared ? 0 : t.g * p.a_rows_per_group;
-        const int a_row = (EPI == EPI_SWIGLU) ? base + t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2)
-                                              : base + t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M;
-        const int b_row = t.b_row + (int)rank * half;
-        const uint32_t bytes_pair = 2u * (S::A_BYTES + S::NUM_B * half * BLOCK_K * 2);
+        const int a_row = (EPI == EPI_SWIGLU) ? base + mb * BLOCK_M + (int)rank * (BLOCK_M / 2)
+                                              : base + mb * 2 * BLOCK_M + (int)rank * BLOCK_M;
+        const int b_off = (NP == 2) ? (int)pp * qh : 0;  // rows into this CTA's half
+        const int b_row = t.b_row + (int)rank * half + b_off;
+        const uint32_t b_land = S::NUM_B * half * BLOCK_K * 2;  // B bytes landing in one CTA
+        const uint32_t expect = 2u * (S::A_BYTES + b_land);  // both CTAs' A and B, on the even CTA
+        const uint16_t mc_mask = (uint16_t)((1u << rank) | (1u << (2 + rank)));
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
-          const uint32_t fbc = mapa_shared(full_bar(stage), 0);  // the even CTA's full barrier
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), bytes_pair);
+          const uint32_t fbc = mapa_shared(full_bar(stage), lrank);  // the pair's even CTA's full barrier
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), expect);
           const int k0 = kb * BLOCK_K;
           if (EPI == EPI_SWIGLU) {
             // this CTA's gate and up slabs (64 features each) in one 3-D box
-            tma_load_3d_pair(sa, ta, fbc, k0, t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2), t.shared ? 0 : 2 * t.g);
+            tma_load_3d_pair(sa, ta, fbc, k0, mb * BLOCK_M + (int)rank * (BLOCK_M / 2), t.shared ? 0 : 2 * t.g);
           } else {
             tma_load_2d_pair(sa, ta, fbc, k0, a_row);
           }
 #pragma unroll
           for (int bp = 0; bp < S::NUM_B; ++bp) {
-            const uint32_t sb = sa + S::A_BYTES + bp * S::B_BYTES;
+            const uint32_t sb = sa + S::A_BYTES + bp * S::B_BYTES + b_off * S::ROW_BYTES;
             const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
             int off = 0;
 #pragma unroll
             for (int i = NUM_BOX_H - 1; i >= 0; --i) {
               const int h = B_BOX << i;
-              if (h <= S::HALF && (half - off) >= h) {
-                tma_load_2d_pair(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off);
+              if (h <= S::HALF && (qh - off) >= h) {
+                if (NP == 2)
+                  tma_load_2d_pair_mc(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off, mc_mask);
+                else
+                  tma_load_2d_pair(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off);
                 off += h;
               }
             }
@@ -555,7 +572,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
         const Tile t = decode_tile<TN>(tile, p);
         if (t.rows <= 0) continue;
-        const int n_mma = max(32, (t.rows + 31) & ~31);
+        const int unit = 32 * NP;
+        const int n_mma = max(unit, (t.rows + unit - 1) / unit * unit);
         if (!mbar_wait_cluster(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32_m256(n_mma);
@@ -576,14 +594,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tc_mma_pair(d, da + 2 * kk, db, idesc, (kb | kk | bp) ? 1u : 0u);
             }
           }
-          tc_commit_pair_mc(empty_bar(stage), 0x3);
+          tc_commit_pair_mc(empty_bar(stage), (uint16_t)((1u << (2 * NP)) - 1u));  // every CTA
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair_mc(accf_bar(buf), 0x3);
+        tc_commit_pair_mc(accf_bar(buf), (uint16_t)(0x3u << lrank));
         if (++buf == S::NUM_BUF) {
           buf = 0;
           buf_phase ^= 1u;
@@ -601,8 +619,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t buf_phase = 0;
     uint32_t xiter = 0;                      // SwiGLU: chunks exchanged so far on this channel
     bool ok = true;
-    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
+    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), lrank);
+    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), lrank);
     for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
       const Tile t = decode_tile<TN>(tile, p);
       if (t.rows <= 0) continue;
@@ -642,7 +660,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
             mbar_arrive(xempty_bar(xch, sl));
-            const int feat = t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
+            const int feat = (t.mb * NP + (int)pp) * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
             if (feat < p.out_features) {
               const int col = ((feat >> 6) << 7) + (feat & 63);
               __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
@@ -664,7 +682,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
       } else {
         const bool scaled = (p.row_scale != nullptr) && !t.shared;
-        const int feat = t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
+        const int feat = (t.mb * NP + (int)pp) * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
         for (int ci = half; ci < nchunk; ci += 2) {
           const int c0 = ci * 16;
           uint32_t r[16];
@@ -798,7 +816,7 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   return cudaGetLastError();
 }
 
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP>
 static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
   using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
   static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
@@ -818,26 +836,39 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
       m.b_sh[i] = m.b[i];
     }
   }
-  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC>;
+  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC, NP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  int pairs = L.num_sms / 2;
-  const int tiles = L.max_tiles * (p.sched_tn / TN);
-  if (tiles < pairs) pairs = tiles;
-  if (pairs < 1) pairs = 1;
+  // a cluster of NP pairs covers NP feature blocks of the pair kernel
+  p.num_mblocks = (p.num_mblocks + NP - 1) / NP;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = Sh::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = 2 * NP;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // as many clusters as can be resident at once (persistent kernel), at most one per tile
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * NP * (L.num_sms / (2 * NP)));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = L.num_sms / (2 * NP);
+    }
+    max_clusters = n;
+  }
+  int clusters = max_clusters;
+  const int tiles = (L.max_tiles + NP - 1) / NP * (p.sched_tn / TN);
+  if (tiles < clusters) clusters = tiles;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(2 * NP * clusters);
   e = cudaLaunchKernelEx(&cfg, kern, m, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -869,9 +900,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   constexpr int TNP = MOE_TN_PREFILL;
   constexpr int TN2 = MOE_TN_DOWN;
   if (L.pair) {
-    if (L.epi == EPI_SWIGLU && kernel_tn == TNP) return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM>(L, p, s);
+    if (L.epi == EPI_SWIGLU && kernel_tn == TNP)
+      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, MOE_G1_NP>(L, p, s);
     if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == TN2 && L.mblk == 2)
-      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM>(L, p, s);
+      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM, MOE_G2_NP>(L, p, s);
     return cudaErrorInvalidValue;
   }
   if (L.epi == EPI_SWIGLU) {

@@ -44,6 +44,13 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 #ifndef MOE_PAIR_TMEM
 #define MOE_PAIR_TMEM 512
 #endif
+// CTA pairs per cluster of the prefill GEMMs (2: token rows multicast between the pairs).
+#ifndef MOE_G1_NP
+#define MOE_G1_NP 1
+#endif
+#ifndef MOE_G2_NP
+#define MOE_G2_NP 1
+#endif
 
 // Token-tile width (B-operand rows per tile) of the grouped GEMMs for a batch of T tokens.
 inline int token_tile_for(int T) { return T <= 64 ? 64 : MOE_TN_PREFILL; }
