@@ -398,28 +398,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //           [64 r, 64 r + 64) followed by the up rows of the same features, so gate and up of
 //           one feature sit in TMEM lanes i and i + 64 of one CTA (exchanged through smem).
 //   fp32:   the pair covers 256 output features, CTA r the features [128 r, 128 r + 128).
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
+// MB = 2 gives each CTA two 128-row weight slabs against the same token rows (twice the MMA work
+// per byte of B landed; both accumulators fill the 512 TMEM columns, one buffer):
+//   SwiGLU: slab 0 = the gate rows, slab 1 = the up rows of the CTA's 128 features (the pair
+//           covers 256), so gate and up of a feature sit in the same TMEM lane of accumulators
+//           0 and 1 and the epilogue needs no exchange;
+//   fp32:   two adjacent 128-feature blocks (the pair covers 512 output features).
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int MB>
 struct PairShape {
   static constexpr int BLOCK_K = BK;
   static constexpr int ROW_BYTES = BK * 2;
   static constexpr int HALF = TN / 2;
-  static constexpr int A_BYTES = BLOCK_M * BK * 2;
+  static constexpr int A_BYTES = BLOCK_M * BK * 2;                  // one 128-row weight slab
   static constexpr int NUM_B = HILO ? 2 : 1;
   static constexpr int B_BYTES = HALF * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + NUM_B * B_BYTES;
-  static constexpr int XCH = (EPI == EPI_SWIGLU) ? 4 : 0;           // gate/up warp pairs
+  static constexpr int STAGE_BYTES = MB * A_BYTES + NUM_B * B_BYTES;
+  static constexpr bool GU = (EPI == EPI_SWIGLU) && MB == 2;       // gate slab + up slab
+  static constexpr int XCH = (EPI == EPI_SWIGLU && !GU) ? 4 : 0;    // gate/up warp pairs
   static constexpr int XBUF_BYTES = XCH * 2 * 16 * 32 * 4;          // 2 slots of 16 x 32 fp32
-  static constexpr int ACC_COLS = TN;
+  static constexpr int ACC_COLS = MB * TN;                          // MB accumulators of TN columns
   static constexpr int NUM_BUF = (TMEM_ALLOC / ACC_COLS) >= 2 ? 2 : 1;
-  static constexpr int NUM_BARS = 2 * 0 + 4 + 4 * XCH;              // + 2*STAGES at runtime layout
   static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 512 - XBUF_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + XBUF_BYTES + 1024 + 512;
-  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : 2 * BLOCK_M;
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? (GU ? 2 * BLOCK_M : BLOCK_M) : 2 * BLOCK_M * MB;
+  static constexpr int A_BOX = (EPI == EPI_SWIGLU) ? (GU ? BLOCK_M : BLOCK_M / 2) : BLOCK_M;
+  // barriers (full, empty per stage; acc full/empty x2; exchange full/empty x2 per channel),
+  // then the TMEM address slot and the abort flag, in the last 512 bytes
+  static_assert((2 * STAGES + 4 + 4 * XCH) * 8 + 8 <= 512, "barrier area");
   static_assert(TN % 32 == 0 && TN <= 256, "pair token tile");
   static_assert(TMEM_ALLOC >= ACC_COLS && TMEM_ALLOC <= 512, "TMEM allocation");
   static_assert(STAGES >= 2, "pipeline needs two stages");
   static_assert(BK == 64 || BK == 32, "stage K");
+  static_assert(MB == 1 || MB == 2, "weight slabs per CTA");
 };
 
 // NP = CTA pairs per cluster.  With NP = 2 the two pairs of a cluster work on the same token
@@ -427,10 +438,10 @@ struct PairShape {
 // multicasts it to the CTA holding the same half in the other pair, so each SM requests only
 // half of its B half.  The multicast's bytes are counted on each destination pair's even-CTA
 // barrier, and a stage is refilled only after both pairs' MMAs released it.
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP>
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
+  using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB>;
   constexpr int STAGES = S::STAGES;
   constexpr int BLOCK_K = S::BLOCK_K;
   extern __shared__ uint8_t smem_raw[];
@@ -514,12 +525,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
         const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
         const int base = t.shared ? 0 : t.g * p.a_rows_per_group;
-        const int a_row = (EPI == EPI_SWIGLU) ? base + mb * BLOCK_M + (int)rank * (BLOCK_M / 2)
-                                              : base + mb * 2 * BLOCK_M + (int)rank * BLOCK_M;
         const int b_off = (NP == 2) ? (int)pp * qh : 0;  // rows into this CTA's half
         const int b_row = t.b_row + (int)rank * half + b_off;
         const uint32_t b_land = S::NUM_B * half * BLOCK_K * 2;  // B bytes landing in one CTA
-        const uint32_t expect = 2u * (S::A_BYTES + b_land);  // both CTAs' A and B, on the even CTA
+        const uint32_t expect = 2u * (MB * S::A_BYTES + b_land);  // both CTAs' A and B, on the even CTA
         const uint16_t mc_mask = (uint16_t)((1u << rank) | (1u << (2 + rank)));
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
@@ -530,15 +539,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t fbc = mapa_shared(full_bar(stage), lrank);  // the pair's even CTA's full barrier
           if (leader) mbar_arrive_expect_tx(full_bar(stage), expect);
           const int k0 = kb * BLOCK_K;
-          if (EPI == EPI_SWIGLU) {
-            // this CTA's gate and up slabs (64 features each) in one 3-D box
-            tma_load_3d_pair(sa, ta, fbc, k0, mb * BLOCK_M + (int)rank * (BLOCK_M / 2), t.shared ? 0 : 2 * t.g);
+          if (S::GU) {
+            // gate rows, then up rows, of this CTA's 128 features: one 3-D box, two slabs
+            tma_load_3d_pair(sa, ta, fbc, k0, mb * 2 * BLOCK_M + (int)rank * BLOCK_M, t.shared ? 0 : 2 * t.g);
           } else {
-            tma_load_2d_pair(sa, ta, fbc, k0, a_row);
+#pragma unroll
+            for (int ms = 0; ms < MB; ++ms) {
+              const int fb = mb * MB + ms;  // 128-row weight slab of the pair
+              if (EPI == EPI_SWIGLU) {
+                // this CTA's gate and up slabs (64 features each) in one 3-D box
+                tma_load_3d_pair(sa + ms * S::A_BYTES, ta, fbc, k0, fb * BLOCK_M + (int)rank * (BLOCK_M / 2),
+                                 t.shared ? 0 : 2 * t.g);
+              } else {
+                tma_load_2d_pair(sa + ms * S::A_BYTES, ta, fbc, k0,
+                                 base + fb * 2 * BLOCK_M + (int)rank * BLOCK_M);
+              }
+            }
           }
 #pragma unroll
           for (int bp = 0; bp < S::NUM_B; ++bp) {
-            const uint32_t sb = sa + S::A_BYTES + bp * S::B_BYTES + b_off * S::ROW_BYTES;
+            const uint32_t sb = sa + MB * S::A_BYTES + bp * S::B_BYTES + b_off * S::ROW_BYTES;
             const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
             int off = 0;
 #pragma unroll
@@ -585,13 +605,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
-          const uint64_t da = smem_desc_sw(sa, S::ROW_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
 #pragma unroll
-            for (int bp = 0; bp < S::NUM_B; ++bp) {
-              const uint64_t db = smem_desc_sw(sa + S::A_BYTES + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
-              tc_mma_pair(d, da + 2 * kk, db, idesc, (kb | kk | bp) ? 1u : 0u);
+            for (int ms = 0; ms < MB; ++ms) {
+              const uint64_t da = smem_desc_sw(sa + ms * S::A_BYTES, S::ROW_BYTES) + 2 * kk;
+#pragma unroll
+              for (int bp = 0; bp < S::NUM_B; ++bp) {
+                const uint64_t db = smem_desc_sw(sa + MB * S::A_BYTES + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
+                tc_mma_pair(d + ms * TN, da, db, idesc, (kb | kk | bp) ? 1u : 0u);
+              }
             }
           }
           tc_commit_pair_mc(empty_bar(stage), (uint16_t)((1u << (2 * NP)) - 1u));  // every CTA
@@ -626,50 +649,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (t.rows <= 0) continue;
       if (!mbar_wait_cluster(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
       tc_fence_after();
-      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
       const int nchunk = (t.rows + 15) >> 4;
-      if (EPI == EPI_SWIGLU) {
-        float* xb = xbuf + xch * (2 * 16 * 32);
-        for (int ci = half; ci < nchunk; ci += 2, ++xiter) {
-          const int sl = xiter & 1;
-          const uint32_t par = (xiter >> 1) & 1u;
-          const int c0 = ci * 16;
-          if (quad >= 2) {
-            // up lanes: hand the 16 up values of this chunk to the gate warp of the channel
-            uint32_t ru[16];
-            tmem_ld16(tq + c0, ru);
-            tmem_ld_wait();
-            reg_fence16(ru);
-            if (!mbar_wait(xempty_bar(xch, sl), par ^ 1u, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xb[(sl * 16 + j) * 32 + lane] = __uint_as_float(ru[j]);
-            mbar_arrive(xfull_bar(xch, sl));
-          } else {
-            uint32_t rg[16];
+      for (int ms = 0; ok && ms < (S::GU ? 1 : MB); ++ms) {
+        const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS + ms * TN;
+        const int fb = (t.mb * NP + (int)pp) * MB + ms;  // 128-row weight slab of this accumulator
+        if (S::GU) {
+          // lane = feature; gate in accumulator 0, up in accumulator 1 of the same lane
+          const int feat = (t.mb * NP + (int)pp) * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
+          const int col = ((feat >> 6) << 7) + (feat & 63);
+          const bool fvalid = feat < p.out_features;
+          for (int ci = half; ci < nchunk; ci += 2) {
+            const int c0 = ci * 16;
+            uint32_t rg[16], ru[16];
             tmem_ld16(tq + c0, rg);
+            tmem_ld16(tq + TN + c0, ru);
             tmem_ld_wait();
             reg_fence16(rg);
-            if (!mbar_wait(xfull_bar(xch, sl), par, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            float u[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
-            mbar_arrive(xempty_bar(xch, sl));
-            const int feat = (t.mb * NP + (int)pp) * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
-            if (feat < p.out_features) {
-              const int col = ((feat >> 6) << 7) + (feat & 63);
+            reg_fence16(ru);
+            if (fvalid) {
               __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
               const int nr = min(16, t.rows - c0);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 if (j < nr) {
                   const float g = __uint_as_float(rg[j]);
-                  const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
+                  const float h = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(ru[j]);
                   const __nv_bfloat16 hi = __float2bfloat16_rn(h);
                   const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
                   out[(size_t)j * p.out_ld] = hi;
@@ -678,30 +682,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
             }
           }
-        }
-        if (!ok) break;
-      } else {
-        const bool scaled = (p.row_scale != nullptr) && !t.shared;
-        const int feat = (t.mb * NP + (int)pp) * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
-        for (int ci = half; ci < nchunk; ci += 2) {
-          const int c0 = ci * 16;
-          uint32_t r[16];
-          tmem_ld16(tq + c0, r);
-          tmem_ld_wait();
-          reg_fence16(r);
-          if (feat < p.out_features) {
-            float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
-            const int nr = min(16, t.rows - c0);
+        } else if (EPI == EPI_SWIGLU) {
+          float* xb = xbuf + xch * (2 * 16 * 32);
+          for (int ci = half; ci < nchunk; ci += 2, ++xiter) {
+            const int sl = xiter & 1;
+            const uint32_t par = (xiter >> 1) & 1u;
+            const int c0 = ci * 16;
+            if (quad >= 2) {
+              // up lanes: hand the 16 up values of this chunk to the gate warp of the channel
+              uint32_t ru[16];
+              tmem_ld16(tq + c0, ru);
+              tmem_ld_wait();
+              reg_fence16(ru);
+              if (!mbar_wait(xempty_bar(xch, sl), par ^ 1u, abort_flag, p.err)) {
+                ok = false;
+                break;
+              }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (j < nr) {
-                const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
-                out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
+              for (int j = 0; j < 16; ++j) xb[(sl * 16 + j) * 32 + lane] = __uint_as_float(ru[j]);
+              mbar_arrive(xfull_bar(xch, sl));
+            } else {
+              uint32_t rg[16];
+              tmem_ld16(tq + c0, rg);
+              tmem_ld_wait();
+              reg_fence16(rg);
+              if (!mbar_wait(xfull_bar(xch, sl), par, abort_flag, p.err)) {
+                ok = false;
+                break;
+              }
+              float u[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
+              mbar_arrive(xempty_bar(xch, sl));
+              const int feat = fb * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
+              if (feat < p.out_features) {
+                const int col = ((feat >> 6) << 7) + (feat & 63);
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
+                const int nr = min(16, t.rows - c0);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (j < nr) {
+                    const float g = __uint_as_float(rg[j]);
+                    const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+                    out[(size_t)j * p.out_ld] = hi;
+                    out[(size_t)j * p.out_ld + 64] = lo;
+                  }
+                }
+              }
+            }
+          }
+          if (!ok) break;
+        } else {
+          const bool scaled = (p.row_scale != nullptr) && !t.shared;
+          const int feat = fb * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
+          for (int ci = half; ci < nchunk; ci += 2) {
+            const int c0 = ci * 16;
+            uint32_t r[16];
+            tmem_ld16(tq + c0, r);
+            tmem_ld_wait();
+            reg_fence16(r);
+            if (feat < p.out_features) {
+              float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+              const int nr = min(16, t.rows - c0);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (j < nr) {
+                  const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
+                  out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
+                }
               }
             }
           }
         }
       }
+      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf == 0 ? acce_leader0 : acce_leader1);
@@ -816,16 +872,15 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   return cudaGetLastError();
 }
 
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP>
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB>
 static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
-  using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
+  using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB>;
   static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
   if (p.sched_tn % TN != 0 || L.K % BK != 0) return cudaErrorInvalidValue;
   GemmMaps m;
   memset(&m, 0, sizeof(m));
   const int kb_cols = HILO ? 2 * L.K : L.K;
-  const int a_box = (EPI == EPI_SWIGLU) ? BLOCK_M / 2 : BLOCK_M;
-  if (!make_a_maps(m, L, EPI == EPI_SWIGLU, a_box, BK)) return cudaErrorInvalidValue;
+  if (!make_a_maps(m, L, EPI == EPI_SWIGLU, Sh::A_BOX, BK)) return cudaErrorInvalidValue;
   for (int i = 0; i < NUM_BOX_H; ++i) {
     const int h = B_BOX << i;
     if (h > Sh::HALF) break;
@@ -836,11 +891,12 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
       m.b_sh[i] = m.b[i];
     }
   }
-  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC, NP>;
+  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC, NP, MB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  // a cluster of NP pairs covers NP feature blocks of the pair kernel
-  p.num_mblocks = (p.num_mblocks + NP - 1) / NP;
+  // the schedule counts pair feature blocks of one slab; a CTA of MB slabs, in a cluster of NP
+  // pairs, covers MB * NP of them
+  p.num_mblocks = (p.num_mblocks + NP * MB - 1) / (NP * MB);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.blockDim = dim3(NUM_THREADS);
@@ -865,7 +921,8 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
     max_clusters = n;
   }
   int clusters = max_clusters;
-  const int tiles = (L.max_tiles + NP - 1) / NP * (p.sched_tn / TN);
+  if (MOE_PAIR_MAX_CLUSTERS > 0 && clusters > MOE_PAIR_MAX_CLUSTERS) clusters = MOE_PAIR_MAX_CLUSTERS;
+  const int tiles = (L.max_tiles + NP * MB - 1) / (NP * MB) * (p.sched_tn / TN);
   if (tiles < clusters) clusters = tiles;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(2 * NP * clusters);
@@ -900,10 +957,18 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   constexpr int TNP = MOE_TN_PREFILL;
   constexpr int TN2 = MOE_TN_DOWN;
   if (L.pair) {
-    if (L.epi == EPI_SWIGLU && kernel_tn == TNP)
-      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, MOE_G1_NP>(L, p, s);
-    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == TN2 && L.mblk == 2)
-      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM, MOE_G2_NP>(L, p, s);
+    // two weight slabs per CTA where the pair feature blocks divide evenly, else one
+    const bool even = (L.num_mblocks % (2 * (L.epi == EPI_SWIGLU ? MOE_G1_NP : MOE_G2_NP))) == 0;
+    if (L.epi == EPI_SWIGLU && kernel_tn == TNP) {
+      if (MOE_G1_MB == 2 && even)
+        return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, MOE_G1_NP, 2>(L, p, s);
+      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, MOE_G1_NP, 1>(L, p, s);
+    }
+    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == TN2 && L.mblk == 2) {
+      if (MOE_G2_MB == 2 && even)
+        return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM, MOE_G2_NP, 2>(L, p, s);
+      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM, MOE_G2_NP, 1>(L, p, s);
+    }
     return cudaErrorInvalidValue;
   }
   if (L.epi == EPI_SWIGLU) {

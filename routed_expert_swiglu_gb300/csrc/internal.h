@@ -44,6 +44,18 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 #ifndef MOE_PAIR_TMEM
 #define MOE_PAIR_TMEM 512
 #endif
+// 128-row weight slabs per CTA of the pair GEMMs (1 or 2; 2 fills all 512 TMEM columns with one
+// accumulator buffer)
+#ifndef MOE_G1_MB
+#define MOE_G1_MB 1
+#endif
+#ifndef MOE_G2_MB
+#define MOE_G2_MB 1
+#endif
+// Upper bound on the resident clusters a pair GEMM launches (0: as many as fit).
+#ifndef MOE_PAIR_MAX_CLUSTERS
+#define MOE_PAIR_MAX_CLUSTERS 0
+#endif
 // CTA pairs per cluster of the prefill GEMMs (2: token rows multicast between the pairs).
 #ifndef MOE_G1_NP
 #define MOE_G1_NP 1

@@ -9,7 +9,8 @@
 //   2. scan     per-expert prefix over chunks, exclusive scan over experts (offsets), and the
 //               grouped-GEMM schedule: row tiles per group and the row-tile -> group map
 //   3. scatter  rank inside the chunk from warp match masks + per-warp prefix, so row =
-//               chunk base + warp prefix + rank among equal ids in the warp
+//               offset of the expert + its rows in earlier chunks + warp prefix + rank among
+//               equal ids in the warp
 //   4. gather   X_dispatch[row] = x[token(row)], 16-byte vectors, one warp per row
 #include "common.cuh"
 #include "internal.h"
@@ -71,10 +72,16 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ blockh
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
-    for (int b = 0; b < nblk; ++b) {
-      const int c = blockhist[(size_t)b * E + e];
-      blockhist[(size_t)b * E + e] = cnt;  // rows of expert e in earlier chunks
-      cnt += c;
+    // blockhist[b][e] <- rows of expert e in chunks before b (eight loads in flight per step)
+    for (int b0 = 0; b0 < nblk; b0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = (b0 + u < nblk) ? blockhist[(size_t)(b0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (b0 + u < nblk) blockhist[(size_t)(b0 + u) * E + e] = cnt;
+        cnt += c[u];
+      }
     }
   }
   int total_rows;
@@ -82,7 +89,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ blockh
   if (e < E) {
     counts[e] = cnt;
     offsets[e] = off;
-    for (int b = 0; b < nblk; ++b) blockhist[(size_t)b * E + e] += off;  // chunk base row per expert
   }
   if (e == 0) offsets[E] = total_rows;
   // grouped-GEMM schedule: groups 0..E-1 routed, group E shared (rows N .. N+T-1)
@@ -108,6 +114,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ blockh
 __global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* __restrict__ ids,
                                                                 const float* __restrict__ w, int N, int k, int E,
                                                                 const int32_t* __restrict__ blockbase,
+                                                                const int32_t* __restrict__ offsets,
                                                                 int32_t* __restrict__ perm_tok,
                                                                 int32_t* __restrict__ inv, float* __restrict__ row_w,
                                                                 int* err) {
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* _
   }
   __syncthreads();
   if (valid) {
-    const int row = blockbase[(size_t)blockIdx.x * E + e] + wcnt[warp * E + e] + rank;
+    const int row = __ldg(offsets + e) + blockbase[(size_t)blockIdx.x * E + e] + wcnt[warp * E + e] + rank;
     if (perm_tok) perm_tok[row] = i / k;
     if (inv) inv[i] = row;
     if (row_w) row_w[row] = __ldg(w + i);
@@ -142,13 +149,26 @@ __global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* _
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int4* __restrict__ x, int4* __restrict__ xd,
                                                           const int32_t* __restrict__ perm_tok, int N,
                                                           int vec_per_row) {
+  constexpr int U = 8;  // 16-byte vectors in flight per lane
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += nwarps) {
     const int t = __ldg(perm_tok + r);
     const int4* src = x + (size_t)t * vec_per_row;
     int4* dst = xd + (size_t)r * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * U) {
+      int4 buf[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) buf[u] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) dst[v] = buf[u];
+      }
+    }
   }
 }
 
@@ -167,8 +187,8 @@ cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s) {
     e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  scatter_kernel<<<L.nblk, PERMUTE_CHUNK, smem, s>>>(L.topk_ids, L.topk_w, N, L.k, L.E, L.blockhist, L.perm_tok,
-                                                      L.inv, L.row_w, L.err);
+  scatter_kernel<<<L.nblk, PERMUTE_CHUNK, smem, s>>>(L.topk_ids, L.topk_w, N, L.k, L.E, L.blockhist, L.offsets,
+                                                      L.perm_tok, L.inv, L.row_w, L.err);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.xd != nullptr) {
     const int vec = L.d / 8;

@@ -9,7 +9,8 @@
 //   hash     ids = tid2eid[token_id]               (SGLang analysis page, sec. 二, HashTopK)
 //   top-k then softmax over the selected logits  (router page, sec. "Router 的选择过程")
 //
-// One warp per token; expert e lives in lane e % 32, register slot e / 32.  Top-k is k rounds
+// One warp per token; expert e lives in lane e % 32, register slot e / 32 (the kernel is compiled
+// for PL = 1, 2, 4, 8 or 16 slots per lane, the smallest that holds E).  Top-k is k rounds
 // of a warp arg-max (larger key wins, equal keys -> lower expert id), so ids come out in
 // descending key order.  All reductions use a fixed shuffle tree: results are deterministic.
 #include <float.h>
@@ -21,7 +22,6 @@
 namespace moe {
 
 constexpr int TOPK_WARPS = 8;
-constexpr int MAX_PER_LANE = MAX_EXPERTS / 32;
 constexpr int MAX_GROUP_TOPK = 8;
 
 __device__ __forceinline__ float score_fn(float l, int mode) {
@@ -45,16 +45,19 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Value of register slot `i` without dynamic register indexing.
-__device__ __forceinline__ float pick(const float (&a)[MAX_PER_LANE], int i) {
+template <int PL>
+__device__ __forceinline__ float pick(const float (&a)[PL], int i) {
   float v = 0.0f;
 #pragma unroll
-  for (int s = 0; s < MAX_PER_LANE; ++s)
+  for (int s = 0; s < PL; ++s)
     if (s == i) v = a[s];
   return v;
 }
 
+template <int PL>
 __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
-  __shared__ float s_keys[TOPK_WARPS][MAX_EXPERTS];
+  constexpr int MAX_PER_LANE = PL;
+  __shared__ float s_keys[TOPK_WARPS][PL * 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * TOPK_WARPS + warp;
   if (t >= a.T) return;  // whole warp leaves together
@@ -250,8 +253,18 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
 }
 
 cudaError_t launch_topk(const TopkLaunch& L, cudaStream_t s) {
+  static_assert(MAX_EXPERTS <= 16 * 32, "slots per lane");
   const int blocks = (L.T + TOPK_WARPS - 1) / TOPK_WARPS;
-  topk_kernel<<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
+  if (L.E <= 32)
+    topk_kernel<1><<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
+  else if (L.E <= 64)
+    topk_kernel<2><<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
+  else if (L.E <= 128)
+    topk_kernel<4><<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
+  else if (L.E <= 256)
+    topk_kernel<8><<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
+  else
+    topk_kernel<16><<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
   return cudaGetLastError();
 }
 
