@@ -53,6 +53,11 @@ struct GemmParams {
   long long split_stride;
   int dense_rows;
   int* err;
+  // gathered B (pair gate/up): routed row r of a group is row b_idx[r] of b_x ([*, b_ld] bf16),
+  // a shared-expert row r is row r + shared_b_shift of b_x
+  const __nv_bfloat16* b_x;
+  const int32_t* b_idx;
+  int b_ld;
 };
 
 // Tensor maps of one launch.  The B operand has one map per box height 16 << i (i < 5), so a
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //           covers 256), so gate and up of a feature sit in the same TMEM lane of accumulators
 //           0 and 1 and the epilogue needs no exchange;
 //   fp32:   two adjacent 128-feature blocks (the pair covers 512 output features).
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int MB>
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int MB, bool BG>
 struct PairShape {
   static constexpr int BLOCK_K = BK;
   static constexpr int ROW_BYTES = BK * 2;
@@ -423,9 +428,20 @@ struct PairShape {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + XBUF_BYTES + 1024 + 512;
   static constexpr int FEATS = (EPI == EPI_SWIGLU) ? (GU ? 2 * BLOCK_M : BLOCK_M) : 2 * BLOCK_M * MB;
   static constexpr int A_BOX = (EPI == EPI_SWIGLU) ? (GU ? BLOCK_M : BLOCK_M / 2) : BLOCK_M;
-  // barriers (full, empty per stage; acc full/empty x2; exchange full/empty x2 per channel),
-  // then the TMEM address slot and the abort flag, in the last 512 bytes
-  static_assert((2 * STAGES + 4 + 4 * XCH) * 8 + 8 <= 512, "barrier area");
+  // BG: the token rows are gathered by NBW loader warps with 16-byte cp.async copies, and one
+  // relay warp reports their completed stages to the pair's even CTA
+  static constexpr int NBW = BG ? 4 : 0;
+  static constexpr int THREADS = (2 + NUM_EPI_WARPS + NBW + (BG ? 1 : 0)) * 32;
+  static constexpr int CHUNKS = ROW_BYTES / 16;                     // 16-byte chunks per token row
+  static constexpr int ROWS_PER_PASS = BG ? NBW * 32 / CHUNKS : 1;
+  static constexpr int ROWS_PER_THREAD = BG ? HALF / ROWS_PER_PASS : 0;
+  static_assert(!BG || (EPI == EPI_SWIGLU && !HILO && BK == 64 && HALF % ROWS_PER_PASS == 0),
+                "gathered token rows: gate/up, 128-byte rows");
+  // barriers (full, empty per stage; acc full/empty x2; exchange full/empty x2 per channel;
+  // BG: gathered-rows landed per stage), then the TMEM address slot and the abort flag, in the
+  // last 512 bytes
+  static constexpr int NUM_LBAR = BG ? STAGES : 0;
+  static_assert((2 * STAGES + 4 + 4 * XCH + NUM_LBAR) * 8 + 8 <= 512, "barrier area");
   static_assert(TN % 32 == 0 && TN <= 256, "pair token tile");
   static_assert(TMEM_ALLOC >= ACC_COLS && TMEM_ALLOC <= 512, "TMEM allocation");
   static_assert(STAGES >= 2, "pipeline needs two stages");
@@ -438,18 +454,20 @@ struct PairShape {
 // multicasts it to the CTA holding the same half in the other pair, so each SM requests only
 // half of its B half.  The multicast's bytes are counted on each destination pair's even-CTA
 // barrier, and a stage is refilled only after both pairs' MMAs released it.
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB, bool BG>
+__global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, BG>::THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB>;
+  using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, BG>;
+  static_assert(!BG || NP == 1, "gathered token rows with one pair per cluster");
   constexpr int STAGES = S::STAGES;
   constexpr int BLOCK_K = S::BLOCK_K;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES + S::XBUF_BYTES);
-  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], xfull[XCH][2], xempty[XCH][2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4 + 4 * S::XCH);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], xfull[XCH][2], xempty[XCH][2],
+  // landed[NUM_LBAR]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4 + 4 * S::XCH + S::NUM_LBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -458,6 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   auto xfull_bar = [&](int x, int sl) { return bar0 + 8u * (2 * STAGES + 4 + 2 * x + sl); };
   auto xempty_bar = [&](int x, int sl) { return bar0 + 8u * (2 * STAGES + 4 + 2 * S::XCH + 2 * x + sl); };
+  auto landed_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 4 + 4 * S::XCH + s); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -469,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);      // the even CTA's expect-tx arrival
+      mbar_init(full_bar(s), BG ? 3 : 1);  // the even CTA's expect-tx arrival (+ both relays)
       mbar_init(empty_bar(s), NP);  // one commit per pair of the cluster
     }
     for (int a = 0; a < 2; ++a) {
@@ -481,6 +500,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(xfull_bar(x, sl), 32);
         mbar_init(xempty_bar(x, sl), 32);
       }
+    for (int s = 0; s < S::NUM_LBAR; ++s) mbar_init(landed_bar(s), S::NBW * 32);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -527,7 +547,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int base = t.shared ? 0 : t.g * p.a_rows_per_group;
         const int b_off = (NP == 2) ? (int)pp * qh : 0;  // rows into this CTA's half
         const int b_row = t.b_row + (int)rank * half + b_off;
-        const uint32_t b_land = S::NUM_B * half * BLOCK_K * 2;  // B bytes landing in one CTA
+        const uint32_t b_land = BG ? 0u : S::NUM_B * half * BLOCK_K * 2;  // TMA B bytes landing in one CTA
         const uint32_t expect = 2u * (MB * S::A_BYTES + b_land);  // both CTAs' A and B, on the even CTA
         const uint16_t mc_mask = (uint16_t)((1u << rank) | (1u << (2 + rank)));
         for (int kb = 0; kb < KB; ++kb) {
@@ -557,7 +577,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
 #pragma unroll
-          for (int bp = 0; bp < S::NUM_B; ++bp) {
+          for (int bp = 0; bp < (BG ? 0 : S::NUM_B); ++bp) {
             const uint32_t sb = sa + MB * S::A_BYTES + bp * S::B_BYTES + b_off * S::ROW_BYTES;
             const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
             int off = 0;
@@ -632,7 +652,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + NUM_EPI_WARPS) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int ew = warp - 2;
     const int quad = warp & 3;
@@ -766,6 +786,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         buf_phase ^= 1u;
       }
     }
+  } else if constexpr (BG) {
+    // ------------------------------------------------------------------ token-row loaders (both CTAs)
+    // Loader thread b copies 16-byte chunk (b % CHUNKS) of rows b / CHUNKS + j * ROWS_PER_PASS
+    // of this CTA's half of the tile's token rows, straight from x by the permuted token ids,
+    // into the 128-byte-swizzled layout TMA would have written (chunk c of row r at
+    // c ^ (r & 7)), and arrives on the stage's landed barrier when its copies complete.  The
+    // relay lane, which issues no copies, waits for each stage to land, fences the writes to the
+    // async proxy and reports the stage to the even CTA's full barrier.
+    const bool relay = (warp == 2 + NUM_EPI_WARPS + S::NBW);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    if (relay) {
+      if (lane == 0) {
+        for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+          const Tile t = decode_tile<TN>(tile, p);
+          if (t.rows <= 0) continue;
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait(landed_bar(stage), phase, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive_cluster(mapa_shared(full_bar(stage), lrank));
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      __syncwarp();
+    } else {
+      constexpr int RPT = S::ROWS_PER_THREAD;
+      const int b = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
+      const int chunk = b % S::CHUNKS;
+      const int r0 = b / S::CHUNKS;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const int n_mma = max(32, (t.rows + 31) / 32 * 32);
+        const int half = n_mma >> 1;
+        const __nv_bfloat16* src[RPT];
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+          const int r = r0 + j * S::ROWS_PER_PASS;  // row within this CTA's half
+          const int g = (int)rank * half + r;        // row within the tile
+          src[j] = nullptr;
+          if (r < half && g < t.rows) {
+            const int tok = t.shared ? t.out_row + g + p.shared_b_shift : __ldg(p.b_idx + t.out_row + g);
+            src[j] = p.b_x + (size_t)tok * p.b_ld + chunk * 8;
+          }
+        }
+        for (int kb = 0; kb < KB; ++kb) {
+          bool got = true;
+          if (lane == 0) got = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err);
+          if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = smem_u32(smem + stage * S::STAGE_BYTES + MB * S::A_BYTES);
+#pragma unroll
+          for (int j = 0; j < RPT; ++j) {
+            const int r = r0 + j * S::ROWS_PER_PASS;
+            if (src[j] != nullptr) cp_async16(sb + r * S::ROW_BYTES + ((chunk ^ (r & 7)) << 4), src[j] + kb * BLOCK_K);
+          }
+          cp_async_arrive_noinc(landed_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      cp_async_commit();  // copies never committed so far form the last group
+      cp_async_wait<0>();
+    }
   }
 
   tc_fence_before();
@@ -872,16 +968,22 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   return cudaGetLastError();
 }
 
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB>
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB, bool BG = false>
 static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
-  using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB>;
+  using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, BG>;
   static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
   if (p.sched_tn % TN != 0 || L.K % BK != 0) return cudaErrorInvalidValue;
   GemmMaps m;
   memset(&m, 0, sizeof(m));
   const int kb_cols = HILO ? 2 * L.K : L.K;
   if (!make_a_maps(m, L, EPI == EPI_SWIGLU, Sh::A_BOX, BK)) return cudaErrorInvalidValue;
-  for (int i = 0; i < NUM_BOX_H; ++i) {
+  if (BG) {
+    if (L.b_gather_x == nullptr || L.b_gather_idx == nullptr) return cudaErrorInvalidValue;
+    p.b_x = static_cast<const __nv_bfloat16*>(L.b_gather_x);
+    p.b_idx = L.b_gather_idx;
+    p.b_ld = L.K;
+  }
+  for (int i = 0; i < (BG ? 0 : NUM_BOX_H); ++i) {
     const int h = B_BOX << i;
     if (h > Sh::HALF) break;
     if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h, BK)) return cudaErrorInvalidValue;
@@ -891,7 +993,7 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
       m.b_sh[i] = m.b[i];
     }
   }
-  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC, NP, MB>;
+  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC, NP, MB, BG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   // the schedule counts pair feature blocks of one slab; a CTA of MB slabs, in a cluster of NP
@@ -899,7 +1001,7 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
   p.num_mblocks = (p.num_mblocks + NP * MB - 1) / (NP * MB);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(Sh::THREADS);
   cfg.dynamicSmemBytes = Sh::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -954,11 +1056,19 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.split_stride = L.split_stride;
   p.dense_rows = L.dense_rows;
   p.err = L.err;
+  p.b_x = nullptr;
+  p.b_idx = nullptr;
+  p.b_ld = 0;
   constexpr int TNP = MOE_TN_PREFILL;
   constexpr int TN2 = MOE_TN_DOWN;
   if (L.pair) {
     // two weight slabs per CTA where the pair feature blocks divide evenly, else one
     const bool even = (L.num_mblocks % (2 * (L.epi == EPI_SWIGLU ? MOE_G1_NP : MOE_G2_NP))) == 0;
+    if (L.epi == EPI_SWIGLU && kernel_tn == TNP && L.b_gather_x != nullptr) {
+      if (MOE_G1_MB == 2 && even)
+        return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, 1, 2, true>(L, p, s);
+      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, 1, 1, true>(L, p, s);
+    }
     if (L.epi == EPI_SWIGLU && kernel_tn == TNP) {
       if (MOE_G1_MB == 2 && even)
         return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, MOE_G1_NP, 2>(L, p, s);

@@ -64,8 +64,20 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 #define MOE_G2_NP 1
 #endif
 
+// 1: the prefill gate/up GEMM gathers its token rows from x itself (cp.async by the permuted
+// token ids) instead of reading the dispatched copy by TMA.  Off: on GB300 the cp.async row
+// copies land ~11 GB/s per SM, and the gate/up GEMM of the V4-Flash T=8192 layer takes 4.3 ms
+// instead of 1.64 ms, far more than the 0.09 ms gather launch it saves.
+#ifndef MOE_G1_GATHER
+#define MOE_G1_GATHER 0
+#endif
+
 // Token-tile width (B-operand rows per tile) of the grouped GEMMs for a batch of T tokens.
 inline int token_tile_for(int T) { return T <= 64 ? 64 : MOE_TN_PREFILL; }
+
+// True when a batch of T tokens runs the gate/up GEMM with fused row gathering (no
+// dispatched-row buffer, no gather launch).
+inline bool gate_up_gathers(int T) { return token_tile_for(T) != 64 && MOE_G1_PAIR && MOE_G1_GATHER; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -96,6 +108,9 @@ struct GemmLaunch {
   const void* a_sh_ptr; int64_t a_sh_rows;
   const void* b_ptr; int64_t b_rows;
   const void* b_sh_ptr; int64_t b_sh_rows;
+  // gathered B (pair gate/up only): routed row r of a group reads row b_gather_idx[r] of
+  // b_gather_x ([*, K] bf16); b_ptr is then unused
+  const void* b_gather_x; const int32_t* b_gather_idx;
   int K;
   int hilo;                // activation operand is the (hi, lo) pair: B rows hold 2*K values
   int pair;                // run on CTA pairs (2-SM MMA, 256 weight rows per tile)
