@@ -1,0 +1,95 @@
+"""Library limits and degenerate layers on the GPU, through the C ABI, against the oracle:
+the largest expert count, top-k and group count the library accepts; hidden and intermediate
+sizes that are not multiples of 128 (partial weight slabs in both projections); the first
+batch size that takes the prefill kernels; a one-expert (dense SwiGLU) layer; a layer in which
+every token takes every expert; and exact routing ties, whose outcome the tie rule fixes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routed_expert_swiglu_gb300 import binding, inputs, workloads as W
+
+from parity_util import ExpertFetcher, check_output, check_routing, oracle_route, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routed_expert_swiglu_gb300 import build
+    build.build()
+    binding.load()
+
+
+# E = 512 experts (the library's maximum), k = 8 (maximum), 32 groups of 16 (maximum group
+# count), group score from the 4 largest keys, 8 groups kept; sigmoid affinity with bias.
+LIMITS = W.Workload("limits_T300", T=300, d=256, d_ff=128, E=512, k=8, n_shared=1, score=W.SCORE_SIGMOID,
+                    use_bias=True, n_groups=32, topk_groups=8, group_topk=4)
+# d = 320 and d_ff = 192: the last 128-row weight slab of both projections is partial.
+RAGGED = W.Workload("ragged_T517", T=517, d=320, d_ff=192, E=24, k=3, n_shared=1, score=W.SCORE_SOFTMAX)
+# One expert, top-1: the layer is a dense SwiGLU FFN with gate weight exactly 1.
+DENSE = W.Workload("dense_T200", T=200, d=256, d_ff=256, E=1, k=1, n_shared=0, score=W.SCORE_SOFTMAX_TOPK)
+# Every token takes every expert.
+ALL = W.Workload("all_T130", T=130, d=256, d_ff=128, E=8, k=8, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS)
+
+CASES = [LIMITS, LIMITS.with_T(50), RAGGED, RAGGED.with_T(65), RAGGED.with_T(37), DENSE, DENSE.with_T(64), ALL,
+         ALL.with_T(64)]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_layer_at_the_limits(w):
+    inp = inputs.make_layer_inputs(w, seed=7, device=DEV)
+    layer = binding.MoELayer(w, inp)
+    y = layer.forward(inp.x, inp.token_ids)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    gids = v["topk_ids"].cpu().numpy()
+    gw = v["topk_w"].cpu().numpy()
+    _, rids, rw, margin, omargin = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, gids, gw, rids, rw, margin, omargin)
+    if w.E == w.k:
+        # every expert selected: the set is forced whatever the keys
+        assert same.all()
+    if w.E == 1:
+        assert (gids == 0).all() and (gw == 1.0).all()
+    fetch = ExpertFetcher(inp)
+    tok = np.nonzero(same)[0]
+    assert tok.size >= 0.8 * w.T
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
+    print(f"{w.name}: max elementwise {e:.2e}, normwise {n:.2e}")
+    layer.close()
+
+
+TIE_CASES = [
+    W.Workload("tie_softmax_topk_T70", T=70, d=128, d_ff=64, E=8, k=2, n_shared=0, score=W.SCORE_SOFTMAX_TOPK),
+    W.Workload("tie_softmax_T70", T=70, d=128, d_ff=64, E=16, k=4, n_shared=0, score=W.SCORE_SOFTMAX),
+    W.Workload("tie_sigmoid_groups_T300", T=300, d=256, d_ff=128, E=64, k=6, n_shared=1, score=W.SCORE_SIGMOID,
+               n_groups=8, topk_groups=2, group_topk=2),
+    W.Workload("tie_sqrt_softplus_T40", T=40, d=256, d_ff=128, E=384, k=6, n_shared=1,
+               score=W.SCORE_SQRT_SOFTPLUS),
+]
+
+
+@pytest.mark.parametrize("w", TIE_CASES, ids=lambda w: w.name)
+def test_exact_ties_follow_the_tie_rule(w):
+    """Zero router weights make every key equal.  Equal keys go to the lower expert id (and
+    equal groups to the lower group id), so every token must select experts 0..k-1 in that
+    order with weight 1/k, on the oracle and on the GPU alike."""
+    inp = inputs.make_layer_inputs(w, seed=8, device=DEV)
+    inp.w_r.zero_()
+    layer = binding.MoELayer(w, inp)
+    ids, wts = layer.route(inp.x)
+    torch.cuda.synchronize()
+    assert layer.check_status() == 0
+    expect = np.tile(np.arange(w.k, dtype=np.int32), (w.T, 1))
+    _, rids, rw, _ = oracle_route(w, inp)
+    assert (rids == expect).all()
+    np.testing.assert_allclose(rw, 1.0 / w.k, rtol=0, atol=1e-12)
+    assert (ids.cpu().numpy() == expect).all()
+    np.testing.assert_allclose(wts.cpu().numpy(), 1.0 / w.k, rtol=0, atol=1e-6)
+    layer.close()
