@@ -105,7 +105,9 @@ typedef struct {
  * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a bad config. */
 moe_status moe_plan_create(const moe_config* cfg, moe_plan** out_plan);
 
-/* Free a plan (host memory only).  NULL is accepted. */
+/* Free a plan and, if moe_forward_host was called with it, the side stream and events that
+ * call created (on the device it was created on; call after that work has finished).  NULL is
+ * accepted. */
 moe_status moe_plan_destroy(moe_plan* plan);
 
 /* Bytes of workspace a call with T tokens needs (0 if plan is NULL or T is out of range).
@@ -170,9 +172,16 @@ moe_status moe_forward_routed(moe_plan* plan, int32_t T, const moe_bf16* x,
                               moe_stream_t stream);
 
 /* moe_forward with HOST activations: x_host [T,d] bf16 and token_ids_host [T] (hash only)
- * are copied to the workspace, the layer runs, and out_host [T,d] receives the result, all
- * enqueued on `stream` (pinned host memory makes the copies asynchronous; the caller
- * synchronises `stream` before reading out_host).  Weights stay device pointers. */
+ * are copied to the workspace, the layer runs, and out_host [T,d] receives the result
+ * (pinned host memory makes the copies asynchronous).  Weights stay device pointers.
+ * The input copy runs on a side stream the plan creates on first use (on the current device):
+ * it lands in one of two staging slots that alternate between calls, waits only for the layer
+ * that last read that slot, and `stream` waits for it before the layer runs.  So consecutive
+ * calls overlap one call's input copy with the previous call's layer, while synchronising
+ * `stream` still covers the whole call; the caller must not change x_host / token_ids_host
+ * until then.  When out_host is page-locked memory the device can address (cudaHostAlloc /
+ * cudaMallocHost), the combine writes the result into it directly; otherwise the result is
+ * staged in the workspace and copied.  A plan serves one host thread at a time. */
 moe_status moe_forward_host(moe_plan* plan, int32_t T, const moe_bf16* x_host,
                             const int32_t* token_ids_host, const moe_bf16* w_r,
                             const float* bias, const moe_bf16* w13, const moe_bf16* w2,

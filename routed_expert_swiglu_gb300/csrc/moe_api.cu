@@ -10,11 +10,31 @@
 #include "common.cuh"
 #include "internal.h"
 
+// Side stream of moe_forward_host: input copies run on it so that the copy of one call's input
+// overlaps the previous call's layer (created on first use, on the device current then).
+struct HostPipe {
+  int dev;
+  cudaStream_t copy;
+  cudaEvent_t h2d_done;
+  cudaEvent_t slot_free[2];  // the layer that last read input slot s has finished
+  int slot;
+};
+
 struct moe_plan {
   moe_config cfg;
   moe_event_t* events;
   int n_events;
+  HostPipe* pipe;
 };
+
+static void destroy_pipe(HostPipe* q) {
+  if (q == nullptr) return;
+  cudaEventDestroy(q->h2d_done);
+  cudaEventDestroy(q->slot_free[0]);
+  cudaEventDestroy(q->slot_free[1]);
+  cudaStreamDestroy(q->copy);
+  free(q);
+}
 
 namespace moe {
 
@@ -36,6 +56,11 @@ WsLayout ws_layout(const moe_config& c, int T) {
     return at;
   };
   L.err = take(256);
+  // Input staging of moe_forward_host: two slots (alternate calls) of max_tokens rows, at the
+  // same offsets for every T, so that a side-stream copy into one never overlaps a buffer of
+  // another call on the same workspace.
+  L.x_stage = take((size_t)2 * c.max_tokens * d * 2);
+  L.tok_stage = take((size_t)2 * c.max_tokens * 4);
   L.topk_ids = take((size_t)T * k * 4);
   L.topk_w = take((size_t)T * k * 4);
   L.logits = take((size_t)router_ksplit(c, T) * T * E * 4);  // partial logits of the K slices
@@ -50,9 +75,7 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.xd = take(gate_up_gathers(T) ? 0 : (size_t)L.N * d * 2);
   L.h = take(rows_h * 2 * f * 2);  // hi/lo bf16 pair per activation
   L.o = take(rows_h * d * 4);
-  L.x_stage = take((size_t)T * d * 2);
   L.out_stage = take((size_t)T * d * 2);
-  L.tok_stage = take((size_t)T * 4);
   L.total = off;
   return L;
 }
@@ -366,6 +389,7 @@ moe_status moe_plan_create(const moe_config* cfg, moe_plan** out_plan) {
 }
 
 moe_status moe_plan_destroy(moe_plan* plan) {
+  if (plan != nullptr) destroy_pipe(plan->pipe);
   free(plan);
   return MOE_OK;
 }
@@ -482,18 +506,60 @@ moe_status moe_forward_host(moe_plan* plan, int32_t T, const moe_bf16* x_host, c
   MOE_TRY(need16(w_r));
   MOE_TRY(check_forward_ptrs(plan, w13, w2, w13_sh, w2_sh));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const WsLayout L = ws_layout(plan->cfg, T);
-  const size_t xbytes = (size_t)T * plan->cfg.d * 2;
-  moe_bf16* xd = at<moe_bf16>(ws, L.x_stage);
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (plan->pipe == nullptr || plan->pipe->dev != dev) {
+    destroy_pipe(plan->pipe);
+    plan->pipe = nullptr;
+    HostPipe* q = static_cast<HostPipe*>(calloc(1, sizeof(HostPipe)));
+    if (q == nullptr) return MOE_ERR_INVALID_ARG;
+    q->dev = dev;
+    if (cudaStreamCreateWithFlags(&q->copy, cudaStreamNonBlocking) != cudaSuccess) {
+      free(q);
+      return MOE_ERR_CUDA;
+    }
+    cudaError_t e = cudaEventCreateWithFlags(&q->h2d_done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&q->slot_free[0], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&q->slot_free[1], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      destroy_pipe(q);
+      return MOE_ERR_CUDA;
+    }
+    plan->pipe = q;
+  }
+  HostPipe* q = plan->pipe;
+  const int slot = q->slot;
+  const moe_config& c = plan->cfg;
+  const WsLayout L = ws_layout(c, T);
+  const size_t xbytes = (size_t)T * c.d * 2;
+  moe_bf16* xd = at<moe_bf16>(ws, L.x_stage + (size_t)slot * c.max_tokens * c.d * 2);
   moe_bf16* od = at<moe_bf16>(ws, L.out_stage);
   int32_t* td = nullptr;
-  MOE_CUDA(cudaMemcpyAsync(xd, x_host, xbytes, cudaMemcpyHostToDevice, s));
-  if (plan->cfg.tid2eid != nullptr) {
-    td = at<int32_t>(ws, L.tok_stage);
-    MOE_CUDA(cudaMemcpyAsync(td, token_ids_host, (size_t)T * 4, cudaMemcpyHostToDevice, s));
+  // input copy on the side stream, once the layer that last read this slot (two calls back)
+  // is done; the caller's stream waits for it, so every step still carries its own copies
+  MOE_CUDA(cudaStreamWaitEvent(q->copy, q->slot_free[slot], 0));
+  MOE_CUDA(cudaMemcpyAsync(xd, x_host, xbytes, cudaMemcpyHostToDevice, q->copy));
+  if (c.tid2eid != nullptr) {
+    td = at<int32_t>(ws, L.tok_stage + (size_t)slot * c.max_tokens * 4);
+    MOE_CUDA(cudaMemcpyAsync(td, token_ids_host, (size_t)T * 4, cudaMemcpyHostToDevice, q->copy));
   }
-  MOE_TRY(moe_forward(plan, T, xd, td, w_r, bias, w13, w2, w13_sh, w2_sh, od, ws, ws_bytes, stream));
-  MOE_CUDA(cudaMemcpyAsync(out_host, od, xbytes, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaEventRecord(q->h2d_done, q->copy));
+  MOE_CUDA(cudaStreamWaitEvent(s, q->h2d_done, 0));
+  // Page-locked, device-mapped host output: the combine writes the result straight into it
+  // (one pass over the host link during the combine); any other host buffer gets a copy.
+  cudaPointerAttributes pa;
+  moe_bf16* out_dev = nullptr;
+  if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+      pa.devicePointer != nullptr && aligned(pa.devicePointer, 16)) {
+    out_dev = static_cast<moe_bf16*>(pa.devicePointer);
+  } else {
+    cudaGetLastError();  // a pageable pointer is not an error
+  }
+  MOE_TRY(moe_forward(plan, T, xd, td, w_r, bias, w13, w2, w13_sh, w2_sh, out_dev != nullptr ? out_dev : od, ws,
+                      ws_bytes, stream));
+  MOE_CUDA(cudaEventRecord(q->slot_free[slot], s));
+  q->slot = slot ^ 1;
+  if (out_dev == nullptr) MOE_CUDA(cudaMemcpyAsync(out_host, od, xbytes, cudaMemcpyDeviceToHost, s));
   return MOE_OK;
 }
 
