@@ -11,11 +11,18 @@
 //   3. scatter  rank inside the chunk from warp match masks + per-warp prefix, so row =
 //               offset of the expert + its rows in earlier chunks + warp prefix + rank among
 //               equal ids in the warp
-//   4. gather   X_dispatch[row] = x[token(row)], 16-byte vectors, one warp per row
+//   4. rows     X_dispatch rows, 16-byte vectors: token-major X_dispatch[inv[t*k + j]] = x[t]
+//               (each x row read once) for large batches, row-major by perm_tok for small ones
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
+
+// Batches of at least this many tokens copy the dispatched rows token-major (one warp per token
+// keeps every SM busy from here on).
+constexpr int DISPATCH_TOKEN_MAJOR_MIN_T = 1024;
 
 __device__ __forceinline__ int clamp_expert(int e, int E, int* err) {
   if (e < 0 || e >= E) {
@@ -146,15 +153,16 @@ __global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* _
   }
 }
 
+// X_dispatch[row] = x[perm_tok[row]]: row-major, one warp per row, 8 x 16 bytes per lane in
+// flight.  Used for small batches, where one warp per token would leave most SMs idle.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int4* __restrict__ x, int4* __restrict__ xd,
                                                           const int32_t* __restrict__ perm_tok, int N,
                                                           int vec_per_row) {
-  constexpr int U = 8;  // 16-byte vectors in flight per lane
+  constexpr int U = 8;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += nwarps) {
-    const int t = __ldg(perm_tok + r);
-    const int4* src = x + (size_t)t * vec_per_row;
+    const int4* src = x + (size_t)__ldg(perm_tok + r) * vec_per_row;
     int4* dst = xd + (size_t)r * vec_per_row;
     for (int v0 = 0; v0 < vec_per_row; v0 += 32 * U) {
       int4 buf[U];
@@ -166,7 +174,42 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int4* __restrict
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = v0 + u * 32 + lane;
-        if (v < vec_per_row) dst[v] = buf[u];
+        if (v < vec_per_row) __stcs(dst + v, buf[u]);
+      }
+    }
+  }
+}
+
+// X_dispatch[inv[t*k + j]] = x[t] for every slot j of token t: token-major, so each row of x is
+// read once (it would be re-read k times by a row-major gather, from DRAM once x outgrows L2)
+// and written to its k rows with evict-first stores.  One warp per token, 8 x 16 bytes per lane
+// in flight.
+__global__ void __launch_bounds__(256) dispatch_rows_kernel(const int4* __restrict__ x, int4* __restrict__ xd,
+                                                            const int32_t* __restrict__ inv, int T, int k,
+                                                            int vec_per_row) {
+  constexpr int U = 8;
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    const int my_row = lane < k ? __ldg(inv + (size_t)t * k + lane) : 0;
+    const int4* src = x + (size_t)t * vec_per_row;
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * U) {
+      int4 buf[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * 32 + lane;
+        if (v < vec_per_row) buf[u] = __ldcs(src + v);
+      }
+#pragma unroll
+      for (int j = 0; j < MAX_TOPK; ++j) {
+        if (j < k) {
+          int4* dst = xd + (size_t)__shfl_sync(0xffffffffu, my_row, j) * vec_per_row;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * 32 + lane;
+            if (v < vec_per_row) __stcs(dst + v, buf[u]);
+          }
+        }
       }
     }
   }
@@ -192,11 +235,17 @@ cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.xd != nullptr) {
     const int vec = L.d / 8;
-    int blocks = (N + 7) / 8;
     const int cap = L.num_sms * 8;
-    if (blocks > cap) blocks = cap;
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const int4*>(L.x), static_cast<int4*>(L.xd), L.perm_tok,
-                                              N, vec);
+    if (L.T >= DISPATCH_TOKEN_MAJOR_MIN_T) {
+      if (L.inv == nullptr) return cudaErrorInvalidValue;  // the token-major copy goes by the inverse map
+      const int blocks = std::min((L.T + 7) / 8, cap);
+      dispatch_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const int4*>(L.x), static_cast<int4*>(L.xd), L.inv,
+                                                  L.T, L.k, vec);
+    } else {
+      const int blocks = std::min((N + 7) / 8, cap);
+      gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const int4*>(L.x), static_cast<int4*>(L.xd),
+                                                L.perm_tok, N, vec);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
