@@ -72,12 +72,19 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 #define MOE_G1_GATHER 0
 #endif
 
-// Token-tile width (B-operand rows per tile) of the grouped GEMMs for a batch of T tokens.
-inline int token_tile_for(int T) { return T <= 64 ? 64 : MOE_TN_PREFILL; }
+// Batches of at most 64 tokens run the single-CTA (decode) kernels with 64-row token tiles
+// (16- and 32-row tiles, which leave more of each stage to the weight slab, measured slower).
+inline bool is_decode(int T) { return T <= 64; }
+
+// Token-tile width (B-operand rows per tile) of the expert GEMMs and their schedule.
+inline int token_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
+
+// Token-tile width of the router GEMM.
+inline int router_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
 
 // True when a batch of T tokens runs the gate/up GEMM with fused row gathering (no
 // dispatched-row buffer, no gather launch).
-inline bool gate_up_gathers(int T) { return token_tile_for(T) != 64 && MOE_G1_PAIR && MOE_G1_GATHER; }
+inline bool gate_up_gathers(int T) { return !is_decode(T) && MOE_G1_PAIR && MOE_G1_GATHER; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }

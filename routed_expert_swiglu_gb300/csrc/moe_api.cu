@@ -85,7 +85,7 @@ const moe_config* plan_config(const moe_plan* p) { return &p->cfg; }
 int router_ksplit(const moe_config& c, int T) {
   if (T <= 0) return 1;
   const int mblk = c.n_experts > 128 ? 2 : 1;
-  const int base_tiles = ceil_div(T, token_tile_for(T)) * ceil_div(c.n_experts, gemm_features_per_tile(1, mblk));
+  const int base_tiles = ceil_div(T, router_tile_for(T)) * ceil_div(c.n_experts, gemm_features_per_tile(1, mblk));
   if (base_tiles >= 64) return 1;
   int want = 128 / base_tiles;
   if (want > 16) want = 16;
@@ -188,7 +188,7 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   GemmLaunch g;
   memset(&g, 0, sizeof(g));
   g.epi = 1;
-  g.TN = L.TN;
+  g.TN = router_tile_for(T);
   g.a_ptr = w_r;
   g.a_rows = c.n_experts;
   g.b_ptr = x;
@@ -204,7 +204,7 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   g.ksplit = router_ksplit(c, T);
   g.split_stride = (long long)T * c.n_experts;
   if (g.ksplit > 1) g.out = at<float>(ws, L.logits);  // partial slabs; top-k sums them
-  g.max_tiles = ceil_div(T, L.TN) * g.num_mblocks;
+  g.max_tiles = ceil_div(T, g.TN) * g.num_mblocks;
   g.err = err;
   g.num_sms = sms;
   MOE_CUDA(launch_grouped_gemm(g, s));
@@ -287,7 +287,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.b_sh_rows = T;
   g1.K = d;
   g1.mblk = 1;
-  g1.pair = (L.TN != 64) && MOE_G1_PAIR;
+  g1.pair = !is_decode(T) && MOE_G1_PAIR;
   g1.num_mblocks = ceil_div(f, gemm_features_per_tile(0, 1));
   g1.a_rows_per_group = 2 * f;
   g1.a_up_offset = f;
@@ -316,9 +316,9 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.b_rows = rows_h;
   g2.K = f;
   g2.hilo = 1;         // B rows hold the (hi, lo) pair: 2*f values, each pair against one W2 block
-  g2.mblk = L.TN == 64 ? 2 : MOE_G2_MBLK;
-  g2.kernel_tn = L.TN == 64 ? 64 : MOE_TN_DOWN;
-  g2.pair = (L.TN != 64) && MOE_G2_PAIR;
+  g2.mblk = is_decode(T) ? 2 : MOE_G2_MBLK;
+  g2.kernel_tn = is_decode(T) ? L.TN : MOE_TN_DOWN;
+  g2.pair = !is_decode(T) && MOE_G2_PAIR;
   if (g2.pair) g2.mblk = 2;  // a pair tile covers 256 output features
   g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
   g2.a_rows_per_group = d;
