@@ -380,7 +380,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     w = workloads.BY_NAME[args.workload]
-    ntok = args.cpu_tokens
+    ntok = args.ref_tokens
     dev = "cuda:0" if torch.cuda.is_available() else "cpu"
     inp = inputs.make_layer_inputs(w, seed=0, device=dev, T=ntok)   # input synthesis only
     h = HostLayer(inp, ntok)
@@ -418,7 +418,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v4flash_T8192", choices=sorted(workloads.BY_NAME))
     ap.add_argument("--decode-workload", default="v4flash_T64", help="second (decode) workload, or none")
-    ap.add_argument("--cpu-tokens", type=int, default=48)
+    ap.add_argument("--cpu-tokens", type=int, default=1536,
+                    help="tokens of the workload the CPU-baseline oracle runs (about 10 s on 16 Grace cores)")
+    ap.add_argument("--ref-tokens", type=int, default=240,
+                    help="tokens per step of the reference arm (the oracle; about 3 s per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

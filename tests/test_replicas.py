@@ -35,7 +35,7 @@ def _worker(rank, world, port, q):
     bench.barrier(w)
     m = bench.max_over_ranks(10.0 + 5.0 * rank, w)
     args = A()
-    args.workload, args.cpu_tokens, args.warmup, args.steps = "toy_T64", 2, 1, 1
+    args.workload, args.ref_tokens, args.warmup, args.steps = "toy_T64", 2, 1, 1
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         bench.run_reference(args, w, r)
