@@ -6,3 +6,4 @@ baseline leg are its only users.  It shares no code with the CUDA path.
 from .moe_oracle import (DENOM_MIN, SCORES, affinity, bias_update, forward, permute, round_to_bf16,
                          route, router_logits, sigmoid, silu, softmax, softplus,
                          sqrt_softplus, swiglu_expert)
+from . import fp8_weights  # noqa: E402,F401
