@@ -145,6 +145,31 @@ moe_status moe_permute(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32
 moe_status moe_permute_noalloc(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32_t* counts,
                                int32_t* offsets, int32_t* perm_tok, int32_t* inv, moe_stream_t stream);
 
+/* FP8 (E4M3) weights with one power-of-two scale per 128 x 128 tile ("DeepSeek-V4 MoE",
+ * section "FP4 QAT 怎么做到反量化无损": FP8 E4M3 weights, one scale per 128 x 128 tile).
+ *   w [n_mats, rows, K] bf16 (device, 2-byte aligned) -> codes [n_mats, rows, K] uint8 E4M3 bit
+ *   patterns and exps [n_mats, ceil(rows/128), ceil(K/128)] int8, tiles counted from each
+ *   matrix's first row and column.  e = the smallest integer with max|w| <= 448 * 2^e over the
+ *   tile (0 for an all-zero tile, at least -126); code = round-to-nearest-even of w * 2^-e,
+ *   negative zero stored as 0x00.  q * 2^e is exact and is a bf16 value.  Run once per weight
+ *   set (w13 as n_mats = E, rows = 2*d_ff, K = d; w2 as E, d, d_ff; shared with n_mats = 1)
+ *   for moe_forward_fp8.  Enqueued on `stream`; no plan needed; outputs caller-owned. */
+moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int32_t K, uint8_t* codes,
+                            int8_t* exps, moe_stream_t stream);
+
+/* moe_forward with FP8 expert weights (the router stays bf16): q13 [E, 2*d_ff, d] and q2
+ * [E, d, d_ff] hold E4M3 codes, e13 [E, ceil(2*d_ff/128), ceil(d/128)] and e2 [E, ceil(d/128),
+ * ceil(d_ff/128)] their tile exponents, as moe_quantize_fp8 writes them (shared expert: the
+ * same with E = 1; NULL without one).  The layer equals moe_forward on the dequantised weights
+ * q * 2^e: the GEMM kernels stream the codes (half the weight bytes) and widen them to bf16 in
+ * shared memory before the tensor-core MMA.  Code pointers 16-byte aligned; same workspace and
+ * outputs as moe_forward. */
+moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
+                           const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,
+                           const uint8_t* q2, const int8_t* e2, const uint8_t* q13_sh, const int8_t* e13_sh,
+                           const uint8_t* q2_sh, const int8_t* e2_sh, moe_bf16* out, void* ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
 /* Aux-loss-free selection-bias step ("MoE compute and communication", sec. 七.3; "DeepSeek-V4
  * MoE", aux-loss-free balancing, update speed 0.001): for each expert e with load counts[e]
  * (tokens_per_expert of a T-token step, e.g. from moe_permute or moe_workspace_views),

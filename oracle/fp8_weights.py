@@ -13,7 +13,7 @@ the weight bytes a decode step reads.  What they leave open, and the reading tak
     (at most 4 significant bits) is exactly a bf16 value, so the quantised layer is exactly
     the bf16 layer evaluated on the dequantised weights;
   * tiles are counted per weight matrix from its first row and column (the last ones may be
-    partial); an all-zero tile has e = 0.
+    partial); an all-zero tile has e = 0; e is at least -126 (2^-e stays a normal fp32 value).
 """
 from __future__ import annotations
 
@@ -67,11 +67,13 @@ def e4m3_value(code):
 
 
 def tile_exponent(amax):
-    """Smallest integer e with amax <= 448 * 2^e (0 for amax == 0).  With amax = m * 2^x,
-    m in [0.5, 1): 448 = 0.875 * 2^9, so e = x - 9 when m <= 0.875, else x - 8."""
+    """Smallest integer e with amax <= 448 * 2^e (0 for amax == 0), but at least -126 so that
+    2^-e stays a normal fp32 number (only tiles with amax below 448 * 2^-127 are affected; they
+    still fit).  With amax = m * 2^x, m in [0.5, 1): 448 = 0.875 * 2^9, so e = x - 9 when
+    m <= 0.875, else x - 8."""
     amax = np.asarray(amax, dtype=np.float64)
     m, x = np.frexp(np.where(amax > 0, amax, 1.0))
-    e = np.where(m <= 0.875, x - 9, x - 8)
+    e = np.maximum(np.where(m <= 0.875, x - 9, x - 8), -126)
     return np.where(amax > 0, e, 0).astype(np.int64)
 
 

@@ -28,7 +28,7 @@ EXPORTED = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_r
             "moe_forward", "moe_forward_routed", "moe_forward_host", "moe_check_status",
             "moe_workspace_views", "moe_forward_stage_count", "moe_plan_set_events",
             "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc",
-            "moe_update_bias")
+            "moe_update_bias", "moe_quantize_fp8", "moe_forward_fp8")
 
 
 class MoEError(RuntimeError):
@@ -78,6 +78,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_status_string": ([I], ctypes.c_char_p),
         "moe_permute_noalloc": ([P, I, V, V, V, V, V, V], I),
         "moe_update_bias": ([P, I, V, V, ctypes.c_float, V], I),
+        "moe_quantize_fp8": ([V, I, I, I, V, V, V], I),
+        "moe_forward_fp8": ([P, I, V, V, V, V, V, V, V, V, V, V, V, V, V, V, S, V], I),
     }
     for name, (argt, rest) in sig.items():
         fn = getattr(lib, name)
@@ -158,6 +160,31 @@ def moe_forward(plan, T, x, token_ids, w_r, bias, w13, w2, w13_sh, w2_sh, out, w
     _check(load().moe_forward(plan, T, _ptr(x), _ptr(token_ids), _ptr(w_r), _ptr(bias), _ptr(w13), _ptr(w2),
                               _ptr(w13_sh), _ptr(w2_sh), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
                               _stream(stream)), "moe_forward")
+
+
+def moe_quantize_fp8(w, codes, exps, stream=None):
+    """E4M3 codes [n, rows, K] (uint8) and 128 x 128 tile exponents [n, ceil(rows/128),
+    ceil(K/128)] (int8) of bf16 weight matrices w [n, rows, K] (or [rows, K])."""
+    n, rows, K = (1,) + tuple(w.shape) if w.dim() == 2 else tuple(w.shape)
+    _check(load().moe_quantize_fp8(_ptr(w), n, rows, K, _ptr(codes), _ptr(exps), _stream(stream)),
+           "moe_quantize_fp8")
+
+
+def quantize_fp8(w, stream=None):
+    """Allocate and fill the FP8 codes and tile exponents of bf16 weights w [.., rows, K]."""
+    rows, K = w.shape[-2:]
+    codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    exps = torch.empty(tuple(w.shape[:-2]) + (-(-rows // 128), -(-K // 128)), dtype=torch.int8, device=w.device)
+    moe_quantize_fp8(w, codes, exps, stream)
+    return codes, exps
+
+
+def moe_forward_fp8(plan, T, x, token_ids, w_r, bias, q13, e13, q2, e2, q13_sh, e13_sh, q2_sh, e2_sh, out, ws,
+                    stream=None):
+    _check(load().moe_forward_fp8(plan, T, _ptr(x), _ptr(token_ids), _ptr(w_r), _ptr(bias), _ptr(q13), _ptr(e13),
+                                  _ptr(q2), _ptr(e2), _ptr(q13_sh), _ptr(e13_sh), _ptr(q2_sh), _ptr(e2_sh),
+                                  _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_forward_fp8")
 
 
 def moe_forward_routed(plan, T, x, topk_ids, topk_w, w13, w2, w13_sh, w2_sh, out, ws, stream=None):
@@ -244,6 +271,28 @@ class MoELayer:
             out = torch.empty((T, self.w.d), dtype=torch.bfloat16, device=self.device)
         moe_forward(self.plan, T, x, token_ids, inp.w_r, inp.bias, inp.w13, inp.w2, inp.w13_sh, inp.w2_sh, out,
                     self.ws, stream)
+        return out
+
+    def quantize_fp8(self, stream=None):
+        """FP8 codes and tile exponents of this layer's expert weights (routed and shared)."""
+        inp = self.inputs
+        q = {"w13": quantize_fp8(inp.w13, stream), "w2": quantize_fp8(inp.w2, stream)}
+        if inp.w13_sh is not None:
+            q["w13_sh"] = quantize_fp8(inp.w13_sh, stream)
+            q["w2_sh"] = quantize_fp8(inp.w2_sh, stream)
+        return q
+
+    def forward_fp8(self, x, q, token_ids=None, out=None, stream=None):
+        """The layer with FP8 expert weights q (from quantize_fp8)."""
+        T = x.shape[0]
+        inp = self.inputs
+        if out is None:
+            out = torch.empty((T, self.w.d), dtype=torch.bfloat16, device=self.device)
+        sh = q.get("w13_sh"), q.get("w2_sh")
+        moe_forward_fp8(self.plan, T, x, token_ids, inp.w_r, inp.bias, q["w13"][0], q["w13"][1], q["w2"][0],
+                        q["w2"][1], None if sh[0] is None else sh[0][0], None if sh[0] is None else sh[0][1],
+                        None if sh[1] is None else sh[1][0], None if sh[1] is None else sh[1][1], out, self.ws,
+                        stream)
         return out
 
     def forward_routed(self, x, topk_ids, topk_w, out=None, stream=None):

@@ -19,6 +19,8 @@
 // Tiles: for group g with R_g = ceil(rows_g / TN) row tiles, tile ids run m-block-major
 // (all row tiles of one weight slab are adjacent, so a slab re-read hits L2).
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -58,6 +60,11 @@ struct GemmParams {
   const __nv_bfloat16* b_x;
   const int32_t* b_idx;
   int b_ld;
+  // FP8 weights: int8 tile exponents [mats, exp_nr, exp_nk] of the routed (a_exp) and shared
+  // (a_sh_exp) weight codes, one per 128 x 128 tile of each matrix
+  const int8_t* a_exp;
+  const int8_t* a_sh_exp;
+  int exp_nr, exp_nk;
 };
 
 // Tensor maps of one launch.  The B operand has one map per box height 16 << i (i < 5), so a
@@ -136,6 +143,71 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmParams& p) {
   t.shared = (p.grp != nullptr) && (t.g == p.n_routed);
   t.b_row = t.out_row + (t.shared ? p.shared_b_shift : 0);
   return t;
+}
+
+// Epilogue of one tile of the single-CTA kernels, run by each of the 8 epilogue warps on its TMEM
+// lane quadrant (`quad`) and its half of the 16-column chunks (`half`): SwiGLU -> the bf16
+// (hi, lo) activation pair, fp32 -> O rows (x optional row scale).  tq = the quadrant's address
+// in the tile's accumulator buffer.
+template <int EPI, int TN, int NACC, int FEATS>
+__device__ __forceinline__ void epilogue_tile(const Tile& t, const GemmParams& p, uint32_t tq, int quad, int half,
+                                              int lane, long long out_shift) {
+  const int nchunk = (t.rows + 15) >> 4;
+  if (EPI == EPI_SWIGLU) {
+    const int feat = t.mb * BLOCK_M + quad * 32 + lane;
+    // h is stored as an unevaluated pair hi + lo of bf16 values: hi = bf16(h),
+    // lo = bf16(h - hi), so the down projection sees h to ~16 significant bits.  Within
+    // each 64-feature block, hi occupies columns [128*b, 128*b + 64) and lo the next 64.
+    const int col = ((feat >> 6) << 7) + (feat & 63);
+    const bool fvalid = feat < p.out_features;
+    for (int ci = half; ci < nchunk; ci += 2) {
+      const int c0 = ci * 16;
+      uint32_t rg[16], ru[16];
+      tmem_ld16(tq + c0, rg);
+      tmem_ld16(tq + TN + c0, ru);
+      tmem_ld_wait();
+      reg_fence16(rg);
+      reg_fence16(ru);
+      if (fvalid) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
+        const int nr = min(16, t.rows - c0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (j < nr) {
+            const float g = __uint_as_float(rg[j]);
+            const float u = __uint_as_float(ru[j]);
+            const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+            out[(size_t)j * p.out_ld] = hi;
+            out[(size_t)j * p.out_ld + 64] = lo;
+          }
+        }
+      }
+    }
+  } else {
+    const bool scaled = (p.row_scale != nullptr) && !t.shared;
+    for (int w = half; w < NACC * nchunk; w += 2) {
+      const int a = w / nchunk;
+      const int c0 = (w - a * nchunk) * 16;
+      const int feat = t.mb * FEATS + a * BLOCK_M + quad * 32 + lane;
+      uint32_t r[16];
+      tmem_ld16(tq + a * TN + c0, r);
+      tmem_ld_wait();
+      reg_fence16(r);
+      if (feat < p.out_features) {
+        float* out = static_cast<float*>(p.out) + out_shift + (size_t)(t.out_row + c0) * p.out_ld + feat;
+        const int nr = min(16, t.rows - c0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (j < nr) {
+            const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
+            out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
+          }
+        }
+      }
+    }
+  }
 }
 
 template <int EPI, int TN, int MBLK, bool HILO, int BK>
@@ -319,68 +391,321 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
-      const int nchunk = (t.rows + 15) >> 4;
-      if (EPI == EPI_SWIGLU) {
-        const int feat = t.mb * BLOCK_M + quad * 32 + lane;
-        // h is stored as an unevaluated pair hi + lo of bf16 values: hi = bf16(h),
-        // lo = bf16(h - hi), so the down projection sees h to ~16 significant bits.  Within
-        // each 64-feature block, hi occupies columns [128*b, 128*b + 64) and lo the next 64.
-        const int col = ((feat >> 6) << 7) + (feat & 63);
-        const bool fvalid = feat < p.out_features;
-        for (int ci = half; ci < nchunk; ci += 2) {
-          const int c0 = ci * 16;
-          uint32_t rg[16], ru[16];
-          tmem_ld16(tq + c0, rg);
-          tmem_ld16(tq + TN + c0, ru);
-          tmem_ld_wait();
-          reg_fence16(rg);
-          reg_fence16(ru);
-          if (fvalid) {
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
-            const int nr = min(16, t.rows - c0);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (j < nr) {
-                const float g = __uint_as_float(rg[j]);
-                const float u = __uint_as_float(ru[j]);
-                const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(h);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
-                out[(size_t)j * p.out_ld] = hi;
-                out[(size_t)j * p.out_ld + 64] = lo;
-              }
-            }
-          }
-        }
-      } else {
-        const bool scaled = (p.row_scale != nullptr) && !t.shared;
-        for (int w = half; w < S::NACC * nchunk; w += 2) {
-          const int a = w / nchunk;
-          const int c0 = (w - a * nchunk) * 16;
-          const int feat = t.mb * S::FEATS + a * BLOCK_M + quad * 32 + lane;
-          uint32_t r[16];
-          tmem_ld16(tq + a * TN + c0, r);
-          tmem_ld_wait();
-          reg_fence16(r);
-          if (feat < p.out_features) {
-            float* out = static_cast<float*>(p.out) + out_shift + (size_t)(t.out_row + c0) * p.out_ld + feat;
-            const int nr = min(16, t.rows - c0);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (j < nr) {
-                const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
-                out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
-              }
-            }
-          }
-        }
-      }
+      epilogue_tile<EPI, TN, S::NACC, S::FEATS>(t, p, tq, quad, half, lane, out_shift);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));
       if (++buf == S::NUM_BUF) {
         buf = 0;
         buf_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// ============================================================================ FP8-weight variant
+// The single-CTA kernel on FP8 (E4M3) weight codes with one power-of-two scale per 128 x 128
+// tile ("DeepSeek-V4 MoE", section "FP4 QAT 怎么做到反量化无损").  TMA brings each stage's codes
+// (64-byte rows, no swizzle) and token rows into a raw ring; four converter warps expand the
+// codes to bf16 (q * 2^e, exact) into a two-slot ring in the 128-byte-swizzled layout the MMA
+// reads, fence those stores to the async proxy and arrive on the slot's barrier; the MMA takes A
+// from the converted slot and B from the raw stage, then releases both.  The weight bytes a
+// stage streams are half those of the bf16 kernel.
+template <int EPI, int TN, int MBLK, bool HILO>
+struct Fp8Shape {
+  static constexpr int BLOCK_K = 64;
+  static constexpr int ROW_BYTES = 128;                  // bf16 rows of the converted A and of B
+  static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
+  static constexpr int RAW_SLAB = BLOCK_M * BLOCK_K;     // 128 rows x 64 E4M3 codes
+  static constexpr int RAW_A = NUM_A * RAW_SLAB;
+  static constexpr int NUM_B = HILO ? 2 : 1;
+  static constexpr int B_BYTES = TN * ROW_BYTES;
+  static constexpr int RAW_STAGE = RAW_A + NUM_B * B_BYTES;
+  static constexpr int CONV_SLAB = BLOCK_M * ROW_BYTES;
+  static constexpr int CONV_STAGE = NUM_A * CONV_SLAB;
+  static constexpr int CSTAGES = 2;
+  static constexpr int NUM_CVT_WARPS = 4;
+  static constexpr int THREADS = (2 + NUM_EPI_WARPS + NUM_CVT_WARPS) * 32;
+  static constexpr int NACC = NUM_A;
+  static constexpr int ACC_COLS = NACC * TN;
+  static constexpr int NUM_BUF = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int USED_COLS = NUM_BUF * ACC_COLS;
+  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
+                                   : USED_COLS <= 256 ? 256 : 512;
+  static constexpr int RSTAGES_FIT = (SMEM_LIMIT - CSTAGES * CONV_STAGE - 1024 - 512) / RAW_STAGE;
+  static constexpr int RSTAGES = RSTAGES_FIT > 8 ? 8 : RSTAGES_FIT;
+  static constexpr int SMEM_BYTES = CSTAGES * CONV_STAGE + RSTAGES * RAW_STAGE + 1024 + 512;
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : BLOCK_M * MBLK;
+  static constexpr int CHUNKS = NUM_A * RAW_SLAB / 16;   // 16-code chunks per stage
+  static_assert(USED_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(TN % B_BOX == 0 && TN <= 256, "token tile");
+  static_assert(RSTAGES >= 2, "pipeline needs two raw stages");
+  static_assert(RAW_A % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled B must start on 1024 bytes");
+  static_assert(CHUNKS % (NUM_CVT_WARPS * 32) == 0, "chunks per converter thread");
+  static_assert((2 * RSTAGES + 2 * CSTAGES + 4) * 8 + 8 <= 512, "barrier area");
+  static_assert(EPI == EPI_F32 || (MBLK == 1 && !HILO), "SwiGLU variant");
+};
+
+template <int EPI, int TN, int MBLK, bool HILO>
+__global__ void __launch_bounds__(Fp8Shape<EPI, TN, MBLK, HILO>::THREADS, 1)
+    fp8w_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using S = Fp8Shape<EPI, TN, MBLK, HILO>;
+  constexpr int BLOCK_K = S::BLOCK_K;
+  constexpr int RST = S::RSTAGES;
+  constexpr int CST = S::CSTAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* conv = smem;                                   // CST converted A slots
+  uint8_t* raw = smem + CST * S::CONV_STAGE;              // RST raw stages (codes + token rows)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + RST * S::RAW_STAGE);
+  // bars: full[RST], empty[RST], cfull[CST], cempty[CST], acc_full[2], acc_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RST + 2 * CST + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (RST + s); };
+  auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * RST + c); };
+  auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * RST + CST + c); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * RST + 2 * CST + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * RST + 2 * CST + 2 + a); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RST; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int c = 0; c < CST; ++c) {
+      mbar_init(cfull_bar(c), S::NUM_CVT_WARPS * 32);
+      mbar_init(cempty_bar(c), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), NUM_EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a_sh);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int total_tiles;
+  if (p.grp != nullptr) {
+    total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks * (p.sched_tn / TN);
+  } else {
+    total_tiles = ((p.dense_rows + p.sched_tn - 1) / p.sched_tn) * p.num_mblocks * (p.sched_tn / TN);
+  }
+  const int KB = p.K / BLOCK_K;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
+        const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
+        const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * S::FEATS;
+        const uint32_t bytes = S::RAW_A + S::NUM_B * t.n_mma * S::ROW_BYTES;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, bytes);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_3d(sr, ta, fb, kb * BLOCK_K, t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);  // gate, up codes
+          } else {
+            tma_load_2d(sr, ta, fb, kb * BLOCK_K, a_row);                                   // MBLK slabs
+          }
+#pragma unroll
+          for (int bp = 0; bp < S::NUM_B; ++bp) {
+            const uint32_t sb = sr + S::RAW_A + bp * S::B_BYTES;
+            const int k0 = kb * BLOCK_K;
+            const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
+            int off = 0;
+#pragma unroll
+            for (int i = NUM_BOX_H - 1; i >= 0; --i) {
+              const int h = B_BOX << i;
+              if (h <= TN && (t.n_mma - off) >= h) {
+                tma_load_2d(sb + off * S::ROW_BYTES, tb + i, fb, kc, t.b_row + off);
+                off += h;
+              }
+            }
+          }
+          if (++stage == RST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, cs = 0;
+      uint32_t phase = 0, cphase = 0;
+      int buf = 0;
+      uint32_t buf_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        if (!mbar_wait(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(t.n_mma);
+        const uint32_t d0 = tmem_base + buf * S::ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+              !mbar_wait(cfull_bar(cs), cphase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const uint32_t sc = smem_u32(conv + cs * S::CONV_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+#pragma unroll
+            for (int a = 0; a < S::NUM_A; ++a) {
+              const uint64_t da = smem_desc_sw(sc + a * S::CONV_SLAB, S::ROW_BYTES) + 2 * kk;
+#pragma unroll
+              for (int bp = 0; bp < S::NUM_B; ++bp) {
+                const uint64_t db = smem_desc_sw(sr + S::RAW_A + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
+                tc_mma(d0 + a * TN, da, db, idesc, (kb | kk | bp) ? 1u : 0u);
+              }
+            }
+          }
+          tc_commit(empty_bar(stage));
+          tc_commit(cempty_bar(cs));
+          if (++stage == RST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++cs == CST) {
+            cs = 0;
+            cphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(buf));
+        if (++buf == S::NUM_BUF) {
+          buf = 0;
+          buf_phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + NUM_EPI_WARPS) {
+    // ------------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    int buf = 0;
+    uint32_t buf_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      if (!mbar_wait(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
+      epilogue_tile<EPI, TN, S::NACC, S::FEATS>(t, p, tq, quad, half, lane, 0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+      if (++buf == S::NUM_BUF) {
+        buf = 0;
+        buf_phase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ code -> bf16 converters
+    // Thread ct converts 16-code chunks ct, ct + 128, ...: chunk i of slab a holds codes
+    // [16 (i % 4), 16 (i % 4) + 16) of row i / 4 (64-byte rows, as TMA wrote them); the 16 bf16
+    // results are 16-byte chunks 2 (i % 4) and 2 (i % 4) + 1 of that row in the 128-byte-
+    // swizzled slot (chunk j of row r at position j ^ (r & 7)).  The row's scale 2^e comes from
+    // its 128 x 128 tile (tile-row index clamped for rows past the matrix: their results are
+    // never stored by the epilogue).
+    constexpr int PER_THREAD = S::CHUNKS / (S::NUM_CVT_WARPS * 32);
+    const int ct = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
+    int stage = 0, cs = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+            !mbar_wait(cempty_bar(cs), cphase ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* src = raw + stage * S::RAW_STAGE;
+        const uint32_t dst = smem_u32(conv + cs * S::CONV_STAGE);
+        const int kt = (kb * BLOCK_K) >> 7;  // 128-wide K tile of this stage
+#pragma unroll
+        for (int j = 0; j < PER_THREAD; ++j) {
+          const int i = ct + j * S::NUM_CVT_WARPS * 32;
+          const int a = i / (S::RAW_SLAB / 16);
+          const int ci = i % (S::RAW_SLAB / 16);
+          const int r = ci >> 2, kc = ci & 3;
+          // row of this slab within its expert's weight matrix
+          const int mrow = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M + r
+                                               : t.mb * S::FEATS + a * BLOCK_M + r;
+          const int tr = min(mrow >> 7, p.exp_nr - 1);
+          const int e = __ldg(ex + tr * p.exp_nk + kt);
+          const float scale = __int_as_float((e + 127) << 23);
+          const uint4 q = *reinterpret_cast<const uint4*>(src + a * S::RAW_SLAB + ci * 16);
+          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((qw[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+            o[h] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          const uint32_t row_addr = dst + a * S::CONV_SLAB + r * S::ROW_BYTES;
+          st_shared_v4(row_addr + ((((2 * kc) ^ (r & 7))) << 4), o[0], o[1], o[2], o[3]);
+          st_shared_v4(row_addr + ((((2 * kc + 1) ^ (r & 7))) << 4), o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(cfull_bar(cs));
+        if (++stage == RST) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++cs == CST) {
+          cs = 0;
+          cphase ^= 1u;
+        }
       }
     }
   }
@@ -921,6 +1246,33 @@ static bool make_tmap_gateup(CUtensorMap* m, const void* ptr, int64_t groups, in
   return r == CUDA_SUCCESS;
 }
 
+// E4M3 weight codes: 2-D uint8 [rows, cols] with boxes of 64 codes x box_rows rows, and the
+// gate/up 3-D view (cols, d_ff, 2*groups) with boxes (64, 128, 2); no swizzle (the converter
+// warps read 64-byte rows).
+static bool make_tmap_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_tmap_u8_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t cols) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
+  cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(d_ff * cols)};
+  cuuint32_t box[3] = {64, (cuuint32_t)BLOCK_M, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A-operand maps of a launch: 2-D row slabs, or the gate/up 3-D view for SwiGLU.
 static bool make_a_maps(GemmMaps& m, const GemmLaunch& L, bool swiglu, int box_rows, int bk) {
   if (swiglu) {
@@ -965,6 +1317,50 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   if (tiles < grid) grid = tiles;
   if (grid < 1) grid = 1;
   kern<<<grid, NUM_THREADS, Sh::SMEM_BYTES, s>>>(m, p);
+  return cudaGetLastError();
+}
+
+template <int EPI, int TN, int MBLK, bool HILO>
+static cudaError_t launch_fp8_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
+  using Sh = Fp8Shape<EPI, TN, MBLK, HILO>;
+  static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
+  if (p.sched_tn % TN != 0 || L.K % 64 != 0 || p.ksplit != 1 || L.a_exp == nullptr) return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr && L.a_sh_exp == nullptr) return cudaErrorInvalidValue;
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  if (EPI == EPI_SWIGLU) {
+    const int64_t f = L.a_up_offset;
+    if (!make_tmap_u8_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, L.K)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8_gateup(&m.a_sh, L.a_sh_ptr, 1, f, L.K)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_u8(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M * MBLK)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M * MBLK))
+      return cudaErrorInvalidValue;
+  }
+  if (L.a_sh_ptr == nullptr) m.a_sh = m.a;
+  const int kb_cols = HILO ? 2 * L.K : L.K;
+  for (int i = 0; i < NUM_BOX_H; ++i) {
+    const int h = B_BOX << i;
+    if (h > TN) break;
+    if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h, 64)) return cudaErrorInvalidValue;
+    if (L.b_sh_ptr != nullptr) {
+      if (!make_tmap(&m.b_sh[i], L.b_sh_ptr, L.b_sh_rows, kb_cols, h, 64)) return cudaErrorInvalidValue;
+    } else {
+      m.b_sh[i] = m.b[i];
+    }
+  }
+  p.a_exp = L.a_exp;
+  p.a_sh_exp = L.a_sh_exp != nullptr ? L.a_sh_exp : L.a_exp;
+  p.exp_nr = (L.a_rows_per_group + 127) / 128;
+  p.exp_nk = (L.K + 127) / 128;
+  auto kern = fp8w_gemm_kernel<EPI, TN, MBLK, HILO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int grid = L.num_sms;
+  const int tiles = L.max_tiles * (p.sched_tn / TN);
+  if (tiles < grid) grid = tiles;
+  if (grid < 1) grid = 1;
+  kern<<<grid, Sh::THREADS, Sh::SMEM_BYTES, s>>>(m, p);
   return cudaGetLastError();
 }
 
@@ -1059,6 +1455,16 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.b_x = nullptr;
   p.b_idx = nullptr;
   p.b_ld = 0;
+  p.a_exp = nullptr;
+  p.a_sh_exp = nullptr;
+  p.exp_nr = p.exp_nk = 0;
+  if (L.q8) {
+    // FP8 weight codes: single-CTA kernels with 64-row token sub-tiles
+    if (L.epi == EPI_SWIGLU && kernel_tn == 64) return launch_fp8_variant<EPI_SWIGLU, 64, 1, false>(L, p, s);
+    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == 64 && L.mblk == 2)
+      return launch_fp8_variant<EPI_F32, 64, 2, true>(L, p, s);
+    return cudaErrorInvalidValue;
+  }
   constexpr int TNP = MOE_TN_PREFILL;
   constexpr int TN2 = MOE_TN_DOWN;
   if (L.pair) {

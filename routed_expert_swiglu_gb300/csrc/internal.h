@@ -118,6 +118,9 @@ struct GemmLaunch {
   // gathered B (pair gate/up only): routed row r of a group reads row b_gather_idx[r] of
   // b_gather_x ([*, K] bf16); b_ptr is then unused
   const void* b_gather_x; const int32_t* b_gather_idx;
+  // FP8 weights (q8 = 1): a_ptr / a_sh_ptr hold E4M3 codes and a_exp / a_sh_exp the int8
+  // exponents of their 128 x 128 tiles ([mats, ceil(rows/128), ceil(K/128)])
+  int q8; const int8_t* a_exp; const int8_t* a_sh_exp;
   int K;
   int hilo;                // activation operand is the (hi, lo) pair: B rows hold 2*K values
   int pair;                // run on CTA pairs (2-SM MMA, 256 weight rows per tile)

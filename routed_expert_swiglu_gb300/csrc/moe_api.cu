@@ -235,9 +235,15 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
 }
 
 // Dispatch + grouped GEMMs + combine, from routing in the workspace or the caller's buffers.
+// FP8 (E4M3) expert weights: codes and 128 x 128 tile exponents (see moe_quantize_fp8).
+struct Fp8Weights {
+  const uint8_t* q13; const int8_t* e13; const uint8_t* q2; const int8_t* e2;
+  const uint8_t* q13_sh; const int8_t* e13_sh; const uint8_t* q2_sh; const int8_t* e2_sh;
+};
+
 moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_t* ids, const float* w,
                        const moe_bf16* w13, const moe_bf16* w2, const moe_bf16* w13_sh, const moe_bf16* w2_sh,
-                       moe_bf16* out, void* ws, int sms, cudaStream_t s) {
+                       moe_bf16* out, void* ws, int sms, cudaStream_t s, const Fp8Weights* q8 = nullptr) {
   const moe_config& c = p->cfg;
   const WsLayout L = ws_layout(c, T);
   int* err = at<int>(ws, L.err);
@@ -261,6 +267,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   pm.row_w = at<float>(ws, L.row_w);
   pm.err = err;
   const bool fused_gather = gate_up_gathers(T);
+  if (fused_gather && q8 != nullptr) return MOE_ERR_UNSUPPORTED;  // the FP8 kernels read dispatched rows
   pm.x = x;
   pm.xd = fused_gather ? nullptr : at<void>(ws, L.xd);
   pm.d = d;
@@ -299,6 +306,15 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.grp = pm.grp;
   g1.rt2g = pm.rt2g;
   g1.max_tiles = L.max_rt * g1.num_mblocks;
+  if (q8 != nullptr) {
+    g1.q8 = 1;
+    g1.a_ptr = q8->q13;
+    g1.a_exp = q8->e13;
+    g1.a_sh_ptr = sh ? q8->q13_sh : nullptr;
+    g1.a_sh_exp = sh ? q8->e13_sh : nullptr;
+    g1.pair = 0;
+    g1.kernel_tn = 64;
+  }
   g1.err = err;
   g1.num_sms = sms;
   MOE_CUDA(launch_grouped_gemm(g1, s));
@@ -331,6 +347,18 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.grp = pm.grp;
   g2.rt2g = pm.rt2g;
   g2.max_tiles = L.max_rt * g2.num_mblocks;
+  if (q8 != nullptr) {
+    g2.q8 = 1;
+    g2.a_ptr = q8->q2;
+    g2.a_exp = q8->e2;
+    g2.a_sh_ptr = sh ? q8->q2_sh : nullptr;
+    g2.a_sh_exp = sh ? q8->e2_sh : nullptr;
+    g2.pair = 0;
+    g2.kernel_tn = 64;
+    g2.mblk = 2;
+    g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, 2));
+    g2.max_tiles = L.max_rt * g2.num_mblocks;
+  }
   g2.err = err;
   g2.num_sms = sms;
   MOE_CUDA(launch_grouped_gemm(g2, s));
@@ -472,6 +500,36 @@ moe_status moe_forward(moe_plan* plan, int32_t T, const moe_bf16* x, const int32
   float* w = at<float>(ws, L.topk_w);
   MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
   return run_experts(plan, T, x, ids, w, w13, w2, w13_sh, w2_sh, out, ws, sms, s);
+}
+
+moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
+                           const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,
+                           const uint8_t* q2, const int8_t* e2, const uint8_t* q13_sh, const int8_t* e13_sh,
+                           const uint8_t* q2_sh, const int8_t* e2_sh, moe_bf16* out, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+  MOE_TRY(check_common(plan, T, ws, ws_bytes));
+  if (T == 0) return MOE_OK;
+  MOE_TRY(check_route_ptrs(plan, x, token_ids, w_r, bias));
+  MOE_TRY(need16(q13));
+  MOE_TRY(need16(q2));
+  if (e13 == nullptr || e2 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (plan->cfg.n_shared) {
+    MOE_TRY(need16(q13_sh));
+    MOE_TRY(need16(q2_sh));
+    if (e13_sh == nullptr || e2_sh == nullptr) return MOE_ERR_INVALID_ARG;
+  }
+  MOE_TRY(need16(out));
+  int sms = 0;
+  MOE_TRY(num_sms(&sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(plan->cfg, T);
+  record(plan, ST_START, s);
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  int32_t* ids = at<int32_t>(ws, L.topk_ids);
+  float* w = at<float>(ws, L.topk_w);
+  MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
+  const Fp8Weights qw = {q13, e13, q2, e2, q13_sh, e13_sh, q2_sh, e2_sh};
+  return run_experts(plan, T, x, ids, w, nullptr, nullptr, nullptr, nullptr, out, ws, sms, s, &qw);
 }
 
 moe_status moe_forward_routed(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* topk_ids,

@@ -1,0 +1,97 @@
+"""FP8 (E4M3) expert weights on the GPU, through the C ABI, against the oracle: the quantiser's
+codes and tile exponents bit for bit (partial tiles, an all-zero tile, magnitudes over many
+binades), and the layer with FP8 weights against the oracle's layer on its own dequantised
+weights (the oracle quantises the bf16 weights itself), at decode and prefill batch sizes."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8_weights as F
+from routed_expert_swiglu_gb300 import binding, inputs, workloads as W
+
+from parity_util import check_output, check_routing, oracle_route, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routed_expert_swiglu_gb300 import build
+    build.build()
+    binding.load()
+
+
+@pytest.mark.parametrize("shape", [(3, 256, 384), (2, 200, 192), (1, 64, 4096), (5, 128, 64)])
+def test_quantiser_bit_exact(shape):
+    g = torch.Generator().manual_seed(sum(shape))
+    w = torch.randn(shape, generator=g) * torch.exp(torch.randn(shape[:-1] + (1,), generator=g) * 3)
+    w = w.to(torch.bfloat16)
+    if shape[1] > 128 and shape[2] > 128:
+        w[0, 128:, :128] = 0                                    # an all-zero tile
+    codes, exps = binding.quantize_fp8(w.to(DEV))
+    torch.cuda.synchronize()
+    rc, re = F.quantize_fp8_tiles(w.double().numpy())
+    assert np.array_equal(exps.cpu().numpy().astype(np.int64), re)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+class OracleFp8Fetcher:
+    """Expert weights as the oracle's own FP8 round trip of the bf16 weights (per expert, lazily)."""
+
+    def __init__(self, inp):
+        self.inp = inp
+        self.cache = {}
+
+    @staticmethod
+    def _rt(w):
+        codes, exps = F.quantize_fp8_tiles(to64(w))
+        return F.dequantize_fp8_tiles(codes, exps)
+
+    def __call__(self, e):
+        if e not in self.cache:
+            self.cache[e] = (self._rt(self.inp.w13[e]), self._rt(self.inp.w2[e]))
+        return self.cache[e]
+
+    def shared(self):
+        if self.inp.w13_sh is None:
+            return None
+        return self._rt(self.inp.w13_sh), self._rt(self.inp.w2_sh)
+
+
+def small(w, T, **kw):
+    return dataclasses.replace(w, T=T, name=f"{w.name.rsplit('_T', 1)[0]}_T{T}", **kw)
+
+
+CASES = [
+    W.TOY,                                                                  # decode kernels
+    small(W.TOY, 333),                                                      # prefill batch, 64-row sub-tiles
+    W.Workload("mid_T64", T=64, d=512, d_ff=256, E=16, k=4, n_shared=1, score=W.SCORE_SIGMOID, use_bias=True),
+    W.Workload("ragged_T150", T=150, d=320, d_ff=192, E=12, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
+    small(W.V3_T4096, 96, E=32, n_groups=8, topk_groups=4, group_topk=2, d=1024, d_ff=256),
+    small(W.V4FLASH_T64, 64, E=16),                                         # V4-Flash dims, 16 experts
+    small(W.V4PRO_HASH_T16384, 40, E=24, d=1024, d_ff=384),
+]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_fp8_layer_vs_oracle(w):
+    inp = inputs.make_layer_inputs(w, seed=21, device=DEV)
+    layer = binding.MoELayer(w, inp)
+    q = layer.quantize_fp8()
+    y = layer.forward_fp8(inp.x, q, inp.token_ids)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    fetch = OracleFp8Fetcher(inp)
+    tok = np.nonzero(same)[0]
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
+    print(f"{w.name} (fp8 weights): max elementwise {e:.2e}, normwise {n:.2e}")
+    layer.close()
