@@ -139,11 +139,14 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
-def time_layer(layer, x, token_ids, steps, warmup, stream, with_stages=True):
-    """Device time of `steps` forwards (after `warmup`), with per-stage event times."""
+def time_layer(layer, x, token_ids, steps, warmup, stream, with_stages=True, fwd=None):
+    """Device time of `steps` forwards (after `warmup`), with per-stage event times.  `fwd`
+    replaces layer.forward (same arguments), e.g. the FP8-weight forward."""
     nstage = len(STAGES)
+    if fwd is None:
+        fwd = layer.forward
     for _ in range(warmup):
-        layer.forward(x, token_ids, out=layer._out)
+        fwd(x, token_ids, out=layer._out)
     torch.cuda.synchronize()
     evsets = []
     if with_stages:
@@ -158,7 +161,7 @@ def time_layer(layer, x, token_ids, steps, warmup, stream, with_stages=True):
     for i in range(steps):
         if with_stages:
             layer.set_events(evsets[i])
-        layer.forward(x, token_ids, out=layer._out)
+        fwd(x, token_ids, out=layer._out)
     end.record(stream)
     torch.cuda.synchronize()
     layer.set_events(None)
@@ -187,6 +190,32 @@ def measure_workload(w, steps, warmup, device, seed, world, rank):
     active = int((counts > 0).sum())
     launches = binding.moe_forward_launch_count(layer.plan, w.T)
     return layer, inp, total_ms, stage_ms, active, launches
+
+
+def measure_fp8(layer, inp, w, steps, warmup, active, bf16_ms, hbm_peak, world):
+    """The same layer with FP8 (E4M3) expert weights, one power-of-two scale per 128 x 128
+    tile: quantised once before timing (static weights), then moe_forward_fp8 timed like the
+    bf16 forward.  Bytes = the bf16 layer's with one byte per expert weight plus the tile
+    exponents."""
+    from routed_expert_swiglu_gb300 import binding
+    q = layer.quantize_fp8()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    fwd = lambda x, tok, out: layer.forward_fp8(x, q, tok, out=out)  # noqa: E731
+    ms, stage = time_layer(layer, inp.x, inp.token_ids, steps, warmup, stream, fwd=fwd)
+    st = layer.check_status()
+    if st != 0:
+        raise RuntimeError(f"device status {binding.STATUS_NAMES.get(st, st)} on {w.name} (fp8 weights)")
+    ms = max_over_ranks(ms, world) / steps
+    n_mat = active + w.n_shared
+    exps = n_mat * (-(-2 * w.d_ff // 128) * -(-w.d // 128) + -(-w.d // 128) * -(-w.d_ff // 128))
+    nbytes = cost.layer_bytes(w, active) - n_mat * 3 * w.d * w.d_ff + exps
+    return {"weights": "fp8 e4m3, one power-of-two scale per 128x128 tile", "ms_per_step": round(ms, 4),
+            "tokens_per_s": round(world * w.T / (ms / 1e3), 1), "layer_bytes": int(nbytes),
+            "hbm_gbs_layer": round(nbytes / (ms / 1e3) / 1e9, 1),
+            "hbm_frac_layer": round(nbytes / (ms / 1e3) / 1e9 / hbm_peak, 4),
+            "speedup_vs_bf16": round(bf16_ms / ms, 3),
+            "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, stage)}}
 
 
 def measure_e2e(layer, inp, w, steps, warmup, world):
@@ -294,6 +323,9 @@ def run_ours(args, world, rank, local):
                   "layer_bytes": int(dbytes), "hbm_gbs_layer": round(dbytes / (dms / 1e3) / 1e9, 1),
                   "hbm_frac_layer": round(dbytes / (dms / 1e3) / 1e9 / hbm_peak, 4),
                   "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, dstage)}}
+        if not args.no_fp8:
+            decode["fp8_weights"] = measure_fp8(dl, dinp, wd, max(args.steps, 10), args.warmup, dactive, dms,
+                                                hbm_peak, world)
         dl.close()
         del dl, dinp
         torch.cuda.empty_cache()
@@ -423,6 +455,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=240,
                     help="tokens per step of the reference arm (the oracle; about 3 s per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight decode measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -413,42 +413,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ============================================================================ FP8-weight variant
 // The single-CTA kernel on FP8 (E4M3) weight codes with one power-of-two scale per 128 x 128
 // tile ("DeepSeek-V4 MoE", section "FP4 QAT 怎么做到反量化无损").  TMA brings each stage's codes
-// (64-byte rows, no swizzle) and token rows into a raw ring; four converter warps expand the
-// codes to bf16 (q * 2^e, exact) into a two-slot ring in the 128-byte-swizzled layout the MMA
-// reads, fence those stores to the async proxy and arrive on the slot's barrier; the MMA takes A
-// from the converted slot and B from the raw stage, then releases both.  The weight bytes a
-// stage streams are half those of the bf16 kernel.
+// (64-byte rows, 64-byte swizzle) and token rows into a raw ring in shared memory; four
+// converter warps, one per TMEM lane quadrant, each widen whole weight rows to bf16 (q * 2^e,
+// exact) and store them into a ring of A tiles in Tensor Memory (lane = weight row, two bf16 per
+// column); the MMA reads A from Tensor Memory and B from the raw stage, then releases both.  The
+// weight bytes a stage streams are half those of the bf16 kernel, and the widened tiles never
+// pass through shared memory.
+// Two E4M3 codes -> two bf16 values q * 2^e in one word (low half = the first code), exact,
+// through the f16 conversion instruction: the path for zero and subnormal codes and very small
+// scales.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_exact(uint32_t two_codes, float scale) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Four normal E4M3 codes (one word) -> four bf16 values q * 2^e (two words, low half first),
+// exact.  A normal code (exponent field E in 1..15, mantissa M) is (1 + M/8) 2^(E-7), so its
+// bf16 bits are the sign, the exponent field E + 120 + e and M as the top three mantissa bits:
+// the bytes are spread into 16-bit lanes, shifted, biased (bias2 = (120 + e) in both lanes'
+// exponent fields) and signed with integer operations.
+__device__ __forceinline__ uint2 e4m3x4_normal_to_bf16x4(uint32_t w, uint32_t bias2) {
+  const uint32_t l0 = __byte_perm(w, 0u, 0x4140);  // codes 0, 1 in 16-bit lanes
+  const uint32_t l1 = __byte_perm(w, 0u, 0x4342);  // codes 2, 3
+  uint2 r;
+  r.x = (((l0 & 0x007F007Fu) << 4) + bias2) | ((l0 & 0x00800080u) << 8);
+  r.y = (((l1 & 0x007F007Fu) << 4) + bias2) | ((l1 & 0x00800080u) << 8);
+  return r;
+}
+
+// True when some code of the word has exponent field 0 (zero or subnormal).
+__device__ __forceinline__ bool e4m3x4_has_small(uint32_t w) {
+  const uint32_t t = w & 0x78787878u;                  // exponent fields, each byte < 0x80
+  return ((t - 0x01010101u) & ~t & 0x80808080u) != 0;  // some byte of t is zero
+}
+
 template <int EPI, int TN, int MBLK, bool HILO>
 struct Fp8Shape {
   static constexpr int BLOCK_K = 64;
-  static constexpr int ROW_BYTES = 128;                  // bf16 rows of the converted A and of B
+  static constexpr int ROW_BYTES = 128;                  // bf16 rows of B
   static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
   static constexpr int RAW_SLAB = BLOCK_M * BLOCK_K;     // 128 rows x 64 E4M3 codes
   static constexpr int RAW_A = NUM_A * RAW_SLAB;
   static constexpr int NUM_B = HILO ? 2 : 1;
   static constexpr int B_BYTES = TN * ROW_BYTES;
   static constexpr int RAW_STAGE = RAW_A + NUM_B * B_BYTES;
-  static constexpr int CONV_SLAB = BLOCK_M * ROW_BYTES;
-  static constexpr int CONV_STAGE = NUM_A * CONV_SLAB;
-  static constexpr int CSTAGES = 2;
-  static constexpr int NUM_CVT_WARPS = 4;
+  static constexpr int A_COLS = BLOCK_K / 2;             // TMEM columns of one widened 128 x 64 slab
+  static constexpr int CSTAGES = 4;                      // widened-A stages in Tensor Memory
+  static constexpr int CVT_GROUPS = CSTAGES;             // group g widens every CSTAGES-th stage into slot g
+  static constexpr int NUM_CVT_WARPS = 4 * CVT_GROUPS;   // one warp per TMEM lane quadrant per group
   static constexpr int THREADS = (2 + NUM_EPI_WARPS + NUM_CVT_WARPS) * 32;
   static constexpr int NACC = NUM_A;
   static constexpr int ACC_COLS = NACC * TN;
-  static constexpr int NUM_BUF = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int NUM_BUF = (2 * ACC_COLS + CSTAGES * NUM_A * A_COLS <= 512) ? 2 : 1;
   static constexpr int USED_COLS = NUM_BUF * ACC_COLS;
-  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
-                                   : USED_COLS <= 256 ? 256 : 512;
-  static constexpr int RSTAGES_FIT = (SMEM_LIMIT - CSTAGES * CONV_STAGE - 1024 - 512) / RAW_STAGE;
+  static constexpr int A_COL0 = USED_COLS;               // first column of the A ring
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int RSTAGES_FIT = (SMEM_LIMIT - 1024 - 512) / RAW_STAGE;
   static constexpr int RSTAGES = RSTAGES_FIT > 8 ? 8 : RSTAGES_FIT;
-  static constexpr int SMEM_BYTES = CSTAGES * CONV_STAGE + RSTAGES * RAW_STAGE + 1024 + 512;
+  static constexpr int SMEM_BYTES = RSTAGES * RAW_STAGE + 1024 + 512;
   static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : BLOCK_M * MBLK;
-  static constexpr int CHUNKS = NUM_A * RAW_SLAB / 16;   // 16-code chunks per stage
-  static_assert(USED_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(USED_COLS + CSTAGES * NUM_A * A_COLS <= TMEM_COLS, "TMEM: accumulators + A ring");
   static_assert(TN % B_BOX == 0 && TN <= 256, "token tile");
   static_assert(RSTAGES >= 2, "pipeline needs two raw stages");
-  static_assert(RAW_A % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled B must start on 1024 bytes");
-  static_assert(CHUNKS % (NUM_CVT_WARPS * 32) == 0, "chunks per converter thread");
+  static_assert(RAW_A % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled tiles start on 1024 bytes");
   static_assert((2 * RSTAGES + 2 * CSTAGES + 4) * 8 + 8 <= 512, "barrier area");
   static_assert(EPI == EPI_F32 || (MBLK == 1 && !HILO), "SwiGLU variant");
 };
@@ -462,8 +491,7 @@ __global__ void __launch_bounds__(Fp8Shape<EPI, TN, MBLK, HILO>::THREADS, 1)
   constexpr int CST = S::CSTAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* conv = smem;                                   // CST converted A slots
-  uint8_t* raw = smem + CST * S::CONV_STAGE;              // RST raw stages (codes + token rows)
+  uint8_t* raw = smem;                                    // RST raw stages (codes + token rows)
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw + RST * S::RAW_STAGE);
   // bars: full[RST], empty[RST], cfull[CST], cempty[CST], acc_full[2], acc_empty[2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RST + 2 * CST + 4);
@@ -485,7 +513,7 @@ __global__ void __launch_bounds__(Fp8Shape<EPI, TN, MBLK, HILO>::THREADS, 1)
       mbar_init(empty_bar(s), 1);
     }
     for (int c = 0; c < CST; ++c) {
-      mbar_init(cfull_bar(c), S::NUM_CVT_WARPS * 32);
+      mbar_init(cfull_bar(c), 4 * 32);  // the four warps of the slot's converter group
       mbar_init(cempty_bar(c), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -588,16 +616,15 @@ __global__ void __launch_bounds__(Fp8Shape<EPI, TN, MBLK, HILO>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
-          const uint32_t sc = smem_u32(conv + cs * S::CONV_STAGE);
+          const uint32_t ta = tmem_base + S::A_COL0 + cs * (S::NUM_A * S::A_COLS);
 #pragma unroll
           for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
 #pragma unroll
             for (int a = 0; a < S::NUM_A; ++a) {
-              const uint64_t da = smem_desc_sw(sc + a * S::CONV_SLAB, S::ROW_BYTES) + 2 * kk;
 #pragma unroll
               for (int bp = 0; bp < S::NUM_B; ++bp) {
                 const uint64_t db = smem_desc_sw(sr + S::RAW_A + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
-                tc_mma(d0 + a * TN, da, db, idesc, (kb | kk | bp) ? 1u : 0u);
+                tc_mma_ta(d0 + a * TN, ta + a * S::A_COLS + kk * 8, db, idesc, (kb | kk | bp) ? 1u : 0u);
               }
             }
           }
@@ -645,67 +672,104 @@ __global__ void __launch_bounds__(Fp8Shape<EPI, TN, MBLK, HILO>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------------ code -> bf16 converters
-    // Thread ct converts 16-code chunks ct, ct + 128, ...: chunk i of slab a holds codes
-    // [16 (i % 4), 16 (i % 4) + 16) of row i / 4 (64-byte rows, as TMA wrote them); the 16 bf16
-    // results are 16-byte chunks 2 (i % 4) and 2 (i % 4) + 1 of that row in the 128-byte-
-    // swizzled slot (chunk j of row r at position j ^ (r & 7)).  The row's scale 2^e comes from
-    // its 128 x 128 tile (tile-row index clamped for rows past the matrix: their results are
-    // never stored by the epilogue).
-    constexpr int PER_THREAD = S::CHUNKS / (S::NUM_CVT_WARPS * 32);
-    const int ct = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
-    int stage = 0, cs = 0;
-    uint32_t phase = 0, cphase = 0;
+    // CVT_GROUPS groups of four warps; group g widens the stages n with n % CVT_GROUPS == g into
+    // A slot g, so that several stages are widened at once (each warp must wait for its Tensor
+    // Memory stores before reporting a stage).  Within a group, warp w owns TMEM lane quadrant
+    // w % 4, i.e. weight rows r = 32 (w % 4) + lane of every slab: the thread reads that row's 64
+    // codes (four 16-byte chunks; chunk c of row r at c ^ ((r >> 1) & 3), the 64-byte swizzle
+    // TMA wrote), widens them with the row's scale 2^e and stores the 32 columns of bf16 pairs
+    // into the slot's A tile.  A slab spans at most two 128-row tiles: the thread keeps the two
+    // exponents of the current 128-wide K tile and loads those of the next one ahead, so no
+    // global load sits in a stage's critical path and no converter waits on another.
+    const int quad = warp & 3;
+    const int group = (warp - 2 - NUM_EPI_WARPS) >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t ta = tmem_base + (uint32_t(quad * 32) << 16) + S::A_COL0 + group * (S::NUM_A * S::A_COLS);
+    const int nk = p.exp_nk;
+    uint32_t n = 0;   // stage counter over all tiles of this CTA
+    uint32_t mine = 0; // stages this group has widened
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<TN>(tile, p);
       if (t.rows <= 0) continue;
       const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
-      for (int kb = 0; kb < KB; ++kb) {
+      int trow[S::NUM_A];  // this row's tile row in each slab (clamped to the matrix)
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        const int base = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M : t.mb * S::FEATS + a * BLOCK_M;
+        trow[a] = min((base + r) >> 7, p.exp_nr - 1);
+      }
+      int e_cur[S::NUM_A], e_nxt[S::NUM_A];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        e_cur[a] = __ldg(ex + trow[a] * nk);
+        e_nxt[a] = nk > 1 ? __ldg(ex + trow[a] * nk + 1) : 0;
+      }
+      for (int kb = 0; kb < KB; ++kb, ++n) {
+        if (kb > 0 && ((kb * BLOCK_K) & 127) == 0) {  // a new 128-wide K tile: rotate, fetch the next
+          const int kn = ((kb * BLOCK_K) >> 7) + 1;
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) {
+            e_cur[a] = e_nxt[a];
+            e_nxt[a] = kn < nk ? __ldg(ex + trow[a] * nk + kn) : 0;
+          }
+        }
+        if ((int)(n % S::CVT_GROUPS) != group) continue;
+        const int stage = (int)(n % RST);
+        const uint32_t phase = (n / RST) & 1u;
         if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
-            !mbar_wait(cempty_bar(cs), cphase ^ 1u, abort_flag, p.err)) {
+            !mbar_wait(cempty_bar(group), (mine & 1u) ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
+        ++mine;
+        tc_fence_after();
         const uint8_t* src = raw + stage * S::RAW_STAGE;
-        const uint32_t dst = smem_u32(conv + cs * S::CONV_STAGE);
-        const int kt = (kb * BLOCK_K) >> 7;  // 128-wide K tile of this stage
 #pragma unroll
-        for (int j = 0; j < PER_THREAD; ++j) {
-          const int i = ct + j * S::NUM_CVT_WARPS * 32;
-          const int a = i / (S::RAW_SLAB / 16);
-          const int ci = i % (S::RAW_SLAB / 16);
-          const int r = ci >> 2, kc = ci & 3;
-          // row of this slab within its expert's weight matrix
-          const int mrow = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M + r
-                                               : t.mb * S::FEATS + a * BLOCK_M + r;
-          const int tr = min(mrow >> 7, p.exp_nr - 1);
-          const int e = __ldg(ex + tr * p.exp_nk + kt);
+        for (int a = 0; a < S::NUM_A; ++a) {
+          const int e = e_cur[a];
+          const uint32_t bias2 = (uint32_t)(120 + e) * 0x00800080u;
           const float scale = __int_as_float((e + 127) << 23);
-          const uint4 q = *reinterpret_cast<const uint4*>(src + a * S::RAW_SLAB + ci * 16);
-          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-          uint32_t o[8];
+          const bool tiny = e < -120;
+          const uint8_t* row = src + a * S::RAW_SLAB + r * 64;
 #pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((qw[h >> 1] >> (16 * (h & 1))) & 0xFFFFu);
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-            const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-            o[h] = *reinterpret_cast<const uint32_t*>(&b);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[16];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = 2 * h + cc;  // K codes [16 c, 16 c + 16)
+              const uint4 q = *reinterpret_cast<const uint4*>(row + ((c ^ ((r >> 1) & 3)) << 4));
+              uint2 v0, v1, v2, v3;
+              // normal codes and an ordinary scale (the common case): integer path; otherwise (a
+              // zero or subnormal code, or a scale below 2^-120, where E + 120 + e could leave the
+              // normal bf16 range) the chunk goes through the conversion instruction
+              if (!tiny && !(e4m3x4_has_small(q.x) | e4m3x4_has_small(q.y) | e4m3x4_has_small(q.z) |
+                             e4m3x4_has_small(q.w))) {
+                v0 = e4m3x4_normal_to_bf16x4(q.x, bias2);
+                v1 = e4m3x4_normal_to_bf16x4(q.y, bias2);
+                v2 = e4m3x4_normal_to_bf16x4(q.z, bias2);
+                v3 = e4m3x4_normal_to_bf16x4(q.w, bias2);
+              } else {
+                v0 = make_uint2(e4m3x2_to_bf16x2_exact(q.x, scale), e4m3x2_to_bf16x2_exact(q.x >> 16, scale));
+                v1 = make_uint2(e4m3x2_to_bf16x2_exact(q.y, scale), e4m3x2_to_bf16x2_exact(q.y >> 16, scale));
+                v2 = make_uint2(e4m3x2_to_bf16x2_exact(q.z, scale), e4m3x2_to_bf16x2_exact(q.z >> 16, scale));
+                v3 = make_uint2(e4m3x2_to_bf16x2_exact(q.w, scale), e4m3x2_to_bf16x2_exact(q.w >> 16, scale));
+              }
+              o[8 * cc + 0] = v0.x;
+              o[8 * cc + 1] = v0.y;
+              o[8 * cc + 2] = v1.x;
+              o[8 * cc + 3] = v1.y;
+              o[8 * cc + 4] = v2.x;
+              o[8 * cc + 5] = v2.y;
+              o[8 * cc + 6] = v3.x;
+              o[8 * cc + 7] = v3.y;
+            }
+            tmem_st16(ta + a * S::A_COLS + h * 16, o);
           }
-          const uint32_t row_addr = dst + a * S::CONV_SLAB + r * S::ROW_BYTES;
-          st_shared_v4(row_addr + ((((2 * kc) ^ (r & 7))) << 4), o[0], o[1], o[2], o[3]);
-          st_shared_v4(row_addr + ((((2 * kc + 1) ^ (r & 7))) << 4), o[4], o[5], o[6], o[7]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(cfull_bar(cs));
-        if (++stage == RST) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (++cs == CST) {
-          cs = 0;
-          cphase ^= 1u;
-        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(cfull_bar(group));
       }
     }
   }
@@ -1247,8 +1311,8 @@ static bool make_tmap_gateup(CUtensorMap* m, const void* ptr, int64_t groups, in
 }
 
 // E4M3 weight codes: 2-D uint8 [rows, cols] with boxes of 64 codes x box_rows rows, and the
-// gate/up 3-D view (cols, d_ff, 2*groups) with boxes (64, 128, 2); no swizzle (the converter
-// warps read 64-byte rows).
+// gate/up 3-D view (cols, d_ff, 2*groups) with boxes (64, 128, 2); 64-byte swizzle, so that the
+// converter warps' row-wise 16-byte reads spread over all banks.
 static bool make_tmap_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
@@ -1257,7 +1321,7 @@ static bool make_tmap_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t 
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1269,7 +1333,7 @@ static bool make_tmap_u8_gateup(CUtensorMap* m, const void* ptr, int64_t groups,
   cuuint32_t box[3] = {64, (cuuint32_t)BLOCK_M, 2};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

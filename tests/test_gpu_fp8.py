@@ -95,3 +95,32 @@ def test_fp8_layer_vs_oracle(w):
     e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
     print(f"{w.name} (fp8 weights): max elementwise {e:.2e}, normwise {n:.2e}")
     layer.close()
+
+
+def test_fp8_layer_with_zero_subnormal_and_tiny_scale_codes():
+    """Weights with exact zeros, values that quantise to subnormal codes, and one expert scaled
+    down to a tile exponent below -120: every code class of the converter, against the oracle."""
+    w = W.Workload("edges_T80", T=80, d=256, d_ff=128, E=8, k=3, n_shared=1, score=W.SCORE_SOFTMAX)
+    inp = inputs.make_layer_inputs(w, seed=23, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    for t in (inp.w13, inp.w2, inp.w13_sh, inp.w2_sh):
+        u = torch.rand(t.shape, generator=g, device=DEV)
+        t[u < 0.05] = 0
+        tiny = (u >= 0.05) & (u < 0.10)
+        t[tiny] = (t[tiny].float() * 2.0 ** -14).to(torch.bfloat16)
+    inp.w2[2] = (inp.w2[2].float() * 1e-36).to(torch.bfloat16)
+    inp.w13[5] = (inp.w13[5].float() * 1e-36).to(torch.bfloat16)
+    layer = binding.MoELayer(w, inp)
+    q = layer.quantize_fp8()
+    e2 = q["w2"][1].cpu().numpy()
+    assert e2[2].max() < -120 and (q["w13"][0].cpu().numpy() & 0x78 == 0).any()
+    y = layer.forward_fp8(inp.x, q, None)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    fetch = OracleFp8Fetcher(inp)
+    tok = np.nonzero(same)[0]
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
+    layer.close()
