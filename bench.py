@@ -306,7 +306,7 @@ def run_ours(args, world, rank, local):
     e2e_ms, h2d, d2h = measure_e2e(layer, inp, w, args.steps, args.warmup, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, inp, args.cpu_tokens)
+        cpu = cpu_baseline(w, inp, min(args.cpu_tokens, w.T))
     layer.close()
     del layer, inp
     torch.cuda.empty_cache()
@@ -450,8 +450,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v4flash_T8192", choices=sorted(workloads.BY_NAME))
     ap.add_argument("--decode-workload", default="v4flash_T64", help="second (decode) workload, or none")
-    ap.add_argument("--cpu-tokens", type=int, default=1536,
-                    help="tokens of the workload the CPU-baseline oracle runs (about 10 s on 16 Grace cores)")
+    ap.add_argument("--cpu-tokens", type=int, default=8192,
+                    help="tokens of the workload the CPU-baseline oracle runs, at most T (the whole "
+                         "V4-Flash T=8192 batch: about 10 s on 16 Grace cores)")
     ap.add_argument("--ref-tokens", type=int, default=240,
                     help="tokens per step of the reference arm (the oracle; about 3 s per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
