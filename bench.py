@@ -398,14 +398,29 @@ def _oracle_sample(w, h: HostLayer):
     return oracle.forward(x64, ids, wts, lambda e: (f64(h.w13[e]), f64(h.w2[e])), shared)
 
 
+def _oracle_routing(w, h: HostLayer):
+    """Oracle routing alone (router logits + scoring + top-k) on the host copy."""
+    import oracle
+    f64 = lambda t: None if t is None else t.to(torch.float64).numpy()  # noqa: E731
+    logits = oracle.router_logits(f64(h.x), f64(h.w_r))
+    return oracle.route(logits, w.k, w.score, bias=f64(h.bias), n_groups=w.n_groups,
+                        topk_groups=w.topk_groups, group_topk=w.group_topk,
+                        token_ids=None if h.token_ids is None else h.token_ids.numpy(),
+                        tid2eid=None if h.tid2eid is None else h.tid2eid.numpy())
+
+
 def cpu_baseline(w, inp, ntok):
     h = HostLayer(inp, ntok)
     t0 = time.perf_counter()
     _oracle_sample(w, h)
     dt = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    _oracle_routing(w, h)
+    dr = time.perf_counter() - t0
     return {"value": round(ntok / dt, 3), "unit": "tokens/s", "cores": _NCORES, "kind": "oracle",
             "sample": f"{ntok} tokens of {w.name} (routing + every selected expert + shared + combine), "
-                      f"fp64 numpy on host copies of the bf16 inputs", "seconds": round(dt, 2)}
+                      f"fp64 numpy on host copies of the bf16 inputs", "seconds": round(dt, 2),
+            "routing_tokens_per_s": round(ntok / dr, 1)}
 
 
 def run_reference(args, world, rank):
