@@ -161,9 +161,9 @@ moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int
  * [E, d, d_ff] hold E4M3 codes, e13 [E, ceil(2*d_ff/128), ceil(d/128)] and e2 [E, ceil(d/128),
  * ceil(d_ff/128)] their tile exponents, as moe_quantize_fp8 writes them (shared expert: the
  * same with E = 1; NULL without one).  The layer equals moe_forward on the dequantised weights
- * q * 2^e: the GEMM kernels stream the codes (half the weight bytes) and widen them to bf16 in
- * shared memory before the tensor-core MMA.  Code pointers 16-byte aligned; same workspace and
- * outputs as moe_forward. */
+ * q * 2^e: the GEMM kernels stream the codes (half the weight bytes), widen them to bf16 into
+ * Tensor Memory and run the bf16 tensor-core MMA from there.  Code pointers 16-byte aligned;
+ * same workspace and outputs as moe_forward. */
 moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                            const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,
                            const uint8_t* q2, const int8_t* e2, const uint8_t* q13_sh, const int8_t* e13_sh,
