@@ -3,6 +3,8 @@ the largest expert count, top-k and group count the library accepts; hidden and 
 sizes that are not multiples of 128 (partial weight slabs in both projections); the first
 batch size that takes the prefill kernels; a one-expert (dense SwiGLU) layer; a layer in which
 every token takes every expert; and exact routing ties, whose outcome the tie rule fixes."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -92,4 +94,34 @@ def test_exact_ties_follow_the_tie_rule(w):
     np.testing.assert_allclose(rw, 1.0 / w.k, rtol=0, atol=1e-12)
     assert (ids.cpu().numpy() == expect).all()
     np.testing.assert_allclose(wts.cpu().numpy(), 1.0 / w.k, rtol=0, atol=1e-6)
+    layer.close()
+
+
+def test_large_batch():
+    """131072 tokens through the toy layer (262144 assignments: 256 dispatch chunks, the
+    token-major row copy, thousands of row tiles): dispatch invariants on the whole batch, the
+    output against the oracle on a sample of tokens."""
+    w = dataclasses.replace(W.TOY, T=131072, name="toy_T131072")
+    inp = inputs.make_layer_inputs(w, seed=9, device=DEV)
+    layer = binding.MoELayer(w, inp)
+    y = layer.forward(inp.x, inp.token_ids)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    ids = v["topk_ids"].cpu().numpy()
+    counts = v["counts"].cpu().numpy()
+    offsets = v["offsets"].cpu().numpy()
+    perm = v["perm_tok"].cpu().numpy()
+    inv = v["inv"].cpu().numpy()
+    assert (counts == np.bincount(ids.ravel(), minlength=w.E)).all()
+    assert offsets[0] == 0 and (np.diff(offsets) == counts).all() and offsets[-1] == w.T * w.k
+    assert (perm[inv] == np.arange(w.T * w.k) // w.k).all()                # inverse map
+    assert (np.sort(inv) == np.arange(w.T * w.k)).all()                    # every row used once
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(w.T, 512, replace=False))
+    _, rids, rw, margin = oracle_route(w, inp)
+    safe = tok[margin[tok] > 1e-3]
+    assert (ids[safe] == rids[safe]).all()
+    fetch = ExpertFetcher(inp)
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=safe)
+    check_output(y.double().cpu().numpy()[safe], ref, label=w.name)
     layer.close()
