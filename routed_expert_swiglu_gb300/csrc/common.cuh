@@ -220,6 +220,25 @@ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t n) {
          | ((128u >> 4) << 24);  // M >> 4, bits [24,29)
 }
 
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B (format code 0 in both
+// operand fields), fp32 accumulator, both operands K-major, M = 128, N = n (multiple of 16).
+__device__ __forceinline__ uint32_t idesc_e4m3_f32(uint32_t n) {
+  return (1u << 4)               // accumulator format f32, bits [4,6)
+         | ((n >> 3) << 17)      // N >> 3, bits [17,23)
+         | ((128u >> 4) << 24);  // M >> 4, bits [24,29)
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T on 8-bit operands (K = 32 per instruction), one thread.
+__device__ __forceinline__ void tc_mma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {

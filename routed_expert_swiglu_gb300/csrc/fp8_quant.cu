@@ -6,6 +6,8 @@
 // x - 8; 0 for an all-zero tile; at least -126), code = E4M3 round-to-nearest-even of w * 2^-e
 // (exact fp32 scaling), negative zero stored as 0x00.  Dequantisation q * 2^e is exact and
 // every such value is a bf16 value.  One CTA per tile; deterministic.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -66,6 +68,123 @@ cudaError_t launch_quantize_fp8(const void* w, int n_mats, int rows, int K, uint
                                 cudaStream_t s) {
   const dim3 grid((K + QTILE - 1) / QTILE, (rows + QTILE - 1) / QTILE, n_mats);
   quantize_fp8_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w), rows, K, codes, exps);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Activation rows as sums of E4M3 pieces, the B operand of the FP8-weight MMA kernels.
+//
+// Row r becomes P pieces of K codes (piece p at dst + (r * P + p) * K) and one exponent
+// exps[r] = e: the scale 2^-e brings the row's largest magnitude into (224, 448] (e as for the
+// weight tiles: the smallest integer with amax <= 448 * 2^e, 0 for a zero row, at least -126);
+// with v = value * 2^-e (exact), piece 0 is the E4M3 rounding (nearest, ties to even) of v and
+// piece p the rounding of what pieces 0..p-1 leave, so that sum_p piece_p * 2^e reproduces the
+// row.  Each piece removes all but 2^-4 of the remainder while it is a normal E4M3 value: two
+// pieces reproduce a bf16 value (8 significant bits) exactly when |v| >= 2^-2, four pieces
+// leave at most 2^-16 of |v|; below that, the subnormal step (2^-9) bounds the error by 2^-10,
+// i.e. by less than 2^-17 of the row's largest magnitude.
+//
+// One CTA per row; the row is staged in shared memory as fp32 before any piece is written, so
+// the fp32 source may be the destination itself (P = 4: a row's pieces fill exactly its fp32
+// bytes).  Bf16 sources may be gathered: row r < n_gather reads row gather[r] of src, later
+// rows read row r - n_gather.
+constexpr int SPLIT_THREADS = 256;
+
+template <bool BF16_SRC, int P>
+__global__ void __launch_bounds__(SPLIT_THREADS) split_rows_e4m3_kernel(const void* src, const int32_t* __restrict__ gather,
+                                                                        int n_gather, int K, uint8_t* dst,
+                                                                        int32_t* __restrict__ exps) {
+  extern __shared__ float srow[];
+  __shared__ float s_max[SPLIT_THREADS / 32];
+  __shared__ int s_e;
+  const int r = blockIdx.x;
+  float m = 0.0f;
+  if (BF16_SRC) {
+    const int sr = gather == nullptr ? r : (r < n_gather ? __ldg(gather + r) : r - n_gather);
+    const uint4* s = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + (size_t)sr * K);
+    for (int i = threadIdx.x; i < K / 8; i += SPLIT_THREADS) {
+      const uint4 v = __ldg(s + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+        srow[8 * i + 2 * j] = lo;
+        srow[8 * i + 2 * j + 1] = hi;
+        m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+      }
+    }
+  } else {
+    // plain loads: with an in-place split this CTA later overwrites the row
+    const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(src) + (size_t)r * K);
+    for (int i = threadIdx.x; i < K / 4; i += SPLIT_THREADS) {
+      const float4 v = s[i];
+      srow[4 * i] = v.x;
+      srow[4 * i + 1] = v.y;
+      srow[4 * i + 2] = v.z;
+      srow[4 * i + 3] = v.w;
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float amax = 0.0f;
+    for (int i = 0; i < SPLIT_THREADS / 32; ++i) amax = fmaxf(amax, s_max[i]);
+    int e = 0;
+    if (amax > 0.0f) {
+      int x;
+      const float mant = frexpf(amax, &x);
+      e = max((mant <= 0.875f) ? x - 9 : x - 8, -126);
+    }
+    s_e = e;
+    exps[r] = e;
+  }
+  __syncthreads();
+  const float sc = __int_as_float((127 - s_e) << 23);  // 2^-e (e in [-126, 120])
+  uint32_t* out = reinterpret_cast<uint32_t*>(dst + (size_t)r * P * K);
+  for (int i = threadIdx.x; i < K / 4; i += SPLIT_THREADS) {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = srow[4 * i + j] * sc;
+#pragma unroll
+    for (int pc = 0; pc < P; ++pc) {
+      const __nv_fp8x2_storage_t c01 = __nv_cvt_float2_to_fp8x2(make_float2(v[0], v[1]), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t c23 = __nv_cvt_float2_to_fp8x2(make_float2(v[2], v[3]), __NV_SATFINITE, __NV_E4M3);
+      out[(size_t)pc * (K / 4) + i] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+      if (pc + 1 < P) {
+        const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(c01, __NV_E4M3);
+        const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(c23, __NV_E4M3);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        v[0] -= f01.x;  // exact: the rounding and its source are within a factor of two
+        v[1] -= f01.y;
+        v[2] -= f23.x;
+        v[3] -= f23.y;
+      }
+    }
+  }
+}
+
+cudaError_t launch_split_rows_e4m3(const void* src, bool bf16_src, const int32_t* gather, int n_gather, int rows,
+                                   int K, int pieces, uint8_t* dst, int32_t* exps, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (K % 8 != 0 || (size_t)K * 4 > SPLIT_SMEM_MAX) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)K * 4;
+  if (bf16_src && pieces == 2) {
+    auto kern = split_rows_e4m3_kernel<true, 2>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    kern<<<rows, SPLIT_THREADS, smem, s>>>(src, gather, n_gather, K, dst, exps);
+  } else if (!bf16_src && pieces == 4) {
+    auto kern = split_rows_e4m3_kernel<false, 4>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM_MAX);
+    if (e != cudaSuccess) return e;
+    kern<<<rows, SPLIT_THREADS, smem, s>>>(src, nullptr, 0, K, dst, exps);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

@@ -72,6 +72,15 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 #define MOE_G1_GATHER 0
 #endif
 
+// 1: FP8 expert weights run the kernels that feed the E4M3 codes straight to the tensor cores
+// (tcgen05 kind::f8f6f4, activations split into E4M3 pieces) where the shapes allow it
+// (d and d_ff multiples of 128); 0: always the kernels that widen the codes to bf16 first.
+#ifndef MOE_FP8_MMA
+#define MOE_FP8_MMA 1
+#endif
+// Largest activation row (bytes, staged as fp32) the E4M3 split kernel takes.
+constexpr size_t SPLIT_SMEM_MAX = 200 * 1024;
+
 // Batches of at most 64 tokens run the single-CTA (decode) kernels with 64-row token tiles
 // (16- and 32-row tiles, which leave more of each stage to the weight slab, measured slower).
 inline bool is_decode(int T) { return T <= 64; }
@@ -81,6 +90,16 @@ inline int token_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
 
 // Token-tile width of the router GEMM.
 inline int router_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
+
+// Row-tile width of the FP8-weight GEMMs' schedule, from the mean rows per routed expert
+// T k / E: 16 up to 8 rows, 32 up to 24, else 64.  Narrow tiles leave more of each pipeline
+// stage to the weight codes; a tile narrower than an expert's rows streams its weights again.
+// The kernels run this schedule without sub-tiles (sub-tiles of a wider schedule alias with the
+// grid stride, leaving the CTAs that only ever draw the mostly empty later sub-tiles idle).
+inline int fp8_token_tile(int T, int k, int E) {
+  const long long rows = (long long)T * k;
+  return rows <= 8LL * E ? 16 : rows <= 24LL * E ? 32 : 64;
+}
 
 // True when a batch of T tokens runs the gate/up GEMM with fused row gathering (no
 // dispatched-row buffer, no gather launch).
@@ -93,7 +112,7 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 struct WsLayout {
   int T, N, G, TN, nblk, max_rt;
   size_t err, topk_ids, topk_w, logits, blockhist, counts, offsets, grp, rt2g, perm_tok, inv,
-      row_w, xd, h, o, x_stage, out_stage, tok_stage, total;
+      row_w, xd, xexp, h, hexp, o, x_stage, out_stage, tok_stage, total;
 };
 
 WsLayout ws_layout(const moe_config& c, int T);
@@ -121,6 +140,10 @@ struct GemmLaunch {
   // FP8 weights (q8 = 1): a_ptr / a_sh_ptr hold E4M3 codes and a_exp / a_sh_exp the int8
   // exponents of their 128 x 128 tiles ([mats, ceil(rows/128), ceil(K/128)])
   int q8; const int8_t* a_exp; const int8_t* a_sh_exp;
+  // q8 = 2: the codes feed the MMA directly; B rows are E4M3 pieces ([rows, pieces, K] codes,
+  // 2 pieces for SwiGLU, 4 for fp32) with one power-of-two exponent per row (b_exp), shared rows
+  // after the routed ones in the same buffers
+  const int32_t* b_exp;
   int K;
   int hilo;                // activation operand is the (hi, lo) pair: B rows hold 2*K values
   int pair;                // run on CTA pairs (2-SM MMA, 256 weight rows per tile)
@@ -160,6 +183,12 @@ struct PermuteLaunch {
 };
 cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s);
 int permute_launch_count(bool gather);
+
+// Activation rows -> E4M3 pieces and one exponent per row (the B operand of the q8 = 2 GEMMs):
+// bf16 rows (2 pieces; row r < n_gather is row gather[r] of src, later rows row r - n_gather)
+// or fp32 rows (4 pieces, in place allowed).  K * 4 <= SPLIT_SMEM_MAX.
+cudaError_t launch_split_rows_e4m3(const void* src, bool bf16_src, const int32_t* gather, int n_gather, int rows,
+                                   int K, int pieces, uint8_t* dst, int32_t* exps, cudaStream_t s);
 
 struct CombineLaunch {
   const float* o; const int32_t* inv; int T, k, d, N, n_shared; void* out;

@@ -47,7 +47,11 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.G = E + sh;
   L.TN = token_tile_for(T);
   L.nblk = ceil_div(L.N > 0 ? L.N : 1, PERMUTE_CHUNK);
-  L.max_rt = E + ceil_div(L.N, L.TN) + sh * ceil_div(T, L.TN) + 1;
+  // row tiles of the narrowest schedule a forward may build (the FP8-weight GEMMs' 16 to 64 rows)
+  const int tn_min = L.TN < 64 ? L.TN : 64;
+  const int tn_f8 = fp8_token_tile(T, k, E);
+  const int tn_sched = tn_f8 < tn_min ? tn_f8 : tn_min;
+  L.max_rt = E + ceil_div(L.N, tn_sched) + sh * ceil_div(T, tn_sched) + 1;
   const size_t rows_h = (size_t)L.N + (size_t)sh * T;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -72,8 +76,11 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.perm_tok = take((size_t)L.N * 4);
   L.inv = take((size_t)L.N * 4);
   L.row_w = take((size_t)L.N * 4);
-  L.xd = take(gate_up_gathers(T) ? 0 : (size_t)L.N * d * 2);
-  L.h = take(rows_h * 2 * f * 2);  // hi/lo bf16 pair per activation
+  // dispatched rows (bf16), or with FP8 weights the routed and shared rows as two E4M3 pieces
+  L.xd = take(gate_up_gathers(T) ? 0 : rows_h * d * 2);
+  L.xexp = take(rows_h * 4);
+  L.h = take(rows_h * 2 * f * 2);  // hi/lo bf16 pair per activation (FP8 weights: fp32, then 4 pieces)
+  L.hexp = take(rows_h * 4);
   L.o = take(rows_h * d * 4);
   L.out_stage = take((size_t)T * d * 2);
   L.total = off;
@@ -234,6 +241,13 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   return MOE_OK;
 }
 
+// Shapes for which FP8 weights feed the MMA directly: every 128-row weight slab and 128-wide K
+// tile lies on one scale tile, and activation rows fit the split kernel.
+bool fp8_mma_shapes(const moe_config& c) {
+  return MOE_FP8_MMA && c.d % 128 == 0 && c.d_ff % 128 == 0 && (size_t)c.d * 4 <= SPLIT_SMEM_MAX &&
+         (size_t)c.d_ff * 4 <= SPLIT_SMEM_MAX;
+}
+
 // Dispatch + grouped GEMMs + combine, from routing in the workspace or the caller's buffers.
 // FP8 (E4M3) expert weights: codes and 128 x 128 tile exponents (see moe_quantize_fp8).
 struct Fp8Weights {
@@ -255,7 +269,10 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   pm.k = c.top_k;
   pm.E = E;
   pm.n_shared = sh;
-  pm.TN = L.TN;
+  // FP8 weights: a schedule of the FP8 kernels' own row tiles (the widening kernels: 64 rows)
+  const bool f8mma = q8 != nullptr && fp8_mma_shapes(c);
+  const int sched_tn = q8 == nullptr ? L.TN : (f8mma ? fp8_token_tile(T, c.top_k, E) : 64);
+  pm.TN = sched_tn;
   pm.nblk = L.nblk;
   pm.blockhist = at<int32_t>(ws, L.blockhist);
   pm.counts = at<int32_t>(ws, L.counts);
@@ -268,14 +285,19 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   pm.err = err;
   const bool fused_gather = gate_up_gathers(T);
   if (fused_gather && q8 != nullptr) return MOE_ERR_UNSUPPORTED;  // the FP8 kernels read dispatched rows
+  // FP8 weights straight into the MMA: the activation rows go in as E4M3 pieces (the gather
+  // from x builds them, so the dispatch copies no rows)
   pm.x = x;
-  pm.xd = fused_gather ? nullptr : at<void>(ws, L.xd);
+  pm.xd = (fused_gather || f8mma) ? nullptr : at<void>(ws, L.xd);
   pm.d = d;
   pm.num_sms = sms;
   MOE_CUDA(launch_permute(pm, s));
+  const int64_t rows_h = (int64_t)L.N + (int64_t)sh * T;
+  if (f8mma)
+    MOE_CUDA(launch_split_rows_e4m3(x, true, pm.perm_tok, L.N, (int)rows_h, d, 2, at<uint8_t>(ws, L.xd),
+                                    at<int32_t>(ws, L.xexp), s));
   record(p, ST_DISPATCH, s);
 
-  const int64_t rows_h = (int64_t)L.N + (int64_t)sh * T;
   GemmLaunch g1;
   memset(&g1, 0, sizeof(g1));
   g1.epi = 0;
@@ -313,11 +335,24 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
     g1.a_sh_ptr = sh ? q8->q13_sh : nullptr;
     g1.a_sh_exp = sh ? q8->e13_sh : nullptr;
     g1.pair = 0;
-    g1.kernel_tn = 64;
+    g1.TN = sched_tn;
+    g1.kernel_tn = sched_tn;
+    if (f8mma) {
+      g1.q8 = 2;
+      g1.b_ptr = at<void>(ws, L.xd);
+      g1.b_rows = rows_h;  // routed rows, then the shared expert's
+      g1.b_sh_ptr = nullptr;
+      g1.shared_b_shift = 0;
+      g1.b_exp = at<int32_t>(ws, L.xexp);
+      g1.out_ld = f;       // fp32 h
+    }
   }
   g1.err = err;
   g1.num_sms = sms;
   MOE_CUDA(launch_grouped_gemm(g1, s));
+  if (f8mma)  // h (fp32) -> four E4M3 pieces per row, in place
+    MOE_CUDA(launch_split_rows_e4m3(at<void>(ws, L.h), false, nullptr, 0, (int)rows_h, f, 4, at<uint8_t>(ws, L.h),
+                                    at<int32_t>(ws, L.hexp), s));
   record(p, ST_GATE_UP, s);
 
   GemmLaunch g2;
@@ -354,10 +389,16 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
     g2.a_sh_ptr = sh ? q8->q2_sh : nullptr;
     g2.a_sh_exp = sh ? q8->e2_sh : nullptr;
     g2.pair = 0;
-    g2.kernel_tn = 64;
-    g2.mblk = 2;
-    g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, 2));
+    g2.TN = sched_tn;
+    g2.kernel_tn = sched_tn;
+    g2.mblk = (f8mma && sched_tn == 64) ? 1 : 2;  // four 64-row pieces already fill N = 256
+    g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
     g2.max_tiles = L.max_rt * g2.num_mblocks;
+    if (f8mma) {
+      g2.q8 = 2;
+      g2.hilo = 0;
+      g2.b_exp = at<int32_t>(ws, L.hexp);
+    }
   }
   g2.err = err;
   g2.num_sms = sms;
