@@ -160,10 +160,14 @@ moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int
 /* moe_forward with FP8 expert weights (the router stays bf16): q13 [E, 2*d_ff, d] and q2
  * [E, d, d_ff] hold E4M3 codes, e13 [E, ceil(2*d_ff/128), ceil(d/128)] and e2 [E, ceil(d/128),
  * ceil(d_ff/128)] their tile exponents, as moe_quantize_fp8 writes them (shared expert: the
- * same with E = 1; NULL without one).  The layer equals moe_forward on the dequantised weights
- * q * 2^e: the GEMM kernels stream the codes (half the weight bytes), widen them to bf16 into
- * Tensor Memory and run the bf16 tensor-core MMA from there.  Code pointers 16-byte aligned;
- * same workspace and outputs as moe_forward. */
+ * same with E = 1; NULL without one).  The layer is moe_forward on the dequantised weights
+ * q * 2^e, with the activations kept at bf16-level precision.  When d and d_ff are multiples of
+ * 128, the GEMMs feed the codes (half the weight bytes) straight to the FP8 tensor-core MMA, with
+ * the activations as sums of E4M3 pieces and one power-of-two scale per row: x in two pieces,
+ * exact for every value above 2^-10.8 of its row's largest magnitude and within 2^-17 of that
+ * magnitude below it; h in four pieces, about 16 significant bits.  Other shapes widen the codes
+ * to bf16 into Tensor Memory and run the bf16 MMA.  Code pointers 16-byte aligned; same
+ * workspace and outputs as moe_forward. */
 moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                            const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,
                            const uint8_t* q2, const int8_t* e2, const uint8_t* q13_sh, const int8_t* e13_sh,

@@ -1,7 +1,9 @@
 """FP8 (E4M3) expert weights on the GPU, through the C ABI, against the oracle: the quantiser's
 codes and tile exponents bit for bit (partial tiles, an all-zero tile, magnitudes over many
 binades), and the layer with FP8 weights against the oracle's layer on its own dequantised
-weights (the oracle quantises the bf16 weights itself), at decode and prefill batch sizes."""
+weights (the oracle quantises the bf16 weights itself), at decode and prefill batch sizes.
+Shapes with d and d_ff multiples of 128 run the codes straight into the tensor cores (16-, 32-
+and 64-row tiles all appear below); the others (toy, ragged) run the widening kernels."""
 import dataclasses
 
 import numpy as np
@@ -76,6 +78,11 @@ CASES = [
     small(W.V3_T4096, 96, E=32, n_groups=8, topk_groups=4, group_topk=2, d=1024, d_ff=256),
     small(W.V4FLASH_T64, 64, E=16),                                         # V4-Flash dims, 16 experts
     small(W.V4PRO_HASH_T16384, 40, E=24, d=1024, d_ff=384),
+    # direct-MMA path at each schedule width: 16-row tiles (2 mean rows per expert; the shared
+    # expert's 64 rows span four tiles) and 64-row tiles with several tiles per expert
+    W.Workload("wide_T64", T=64, d=512, d_ff=256, E=64, k=2, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
+               use_bias=True),
+    W.Workload("tall_T600", T=600, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
 ]
 
 
