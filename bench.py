@@ -247,15 +247,27 @@ def measure_e2e(layer, inp, w, steps, warmup, world):
     return ms, h2d, d2h
 
 
+# The sources the bf16 grouped-GEMM kernels are compiled from (the FP8 kernels live elsewhere).
+GEMM_SOURCES = ("common.cuh", "gemm_common.cuh", "grouped_gemm.cu")
+
+
+def gemm_source_sha():
+    """sha256 prefix of the bf16 grouped-GEMM sources, concatenated in GEMM_SOURCES order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "routed_expert_swiglu_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def measured_traffic(workload_name):
     """DRAM bytes per gate/up launch from the committed ncu capture, or None when there is no
-    capture for this workload or the kernel source changed since it was taken."""
-    import hashlib
+    capture for this workload or the kernel sources changed since it was taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "gate_up_traffic.json")) as fh:
             rec = json.load(fh)
-        with open(os.path.join(ROOT, "routed_expert_swiglu_gb300", "csrc", "grouped_gemm.cu"), "rb") as fh:
-            sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+        sha = gemm_source_sha()
     except (OSError, ValueError):
         return None
     if rec.get("source_sha256_prefix") != sha:

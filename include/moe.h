@@ -163,9 +163,10 @@ moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int
  * same with E = 1; NULL without one).  The layer is moe_forward on the dequantised weights
  * q * 2^e, with the activations kept at bf16-level precision.  When d and d_ff are multiples of
  * 128, the GEMMs feed the codes (half the weight bytes) straight to the FP8 tensor-core MMA, with
- * the activations as sums of E4M3 pieces and one power-of-two scale per row: x in two pieces,
- * exact for every value above 2^-10.8 of its row's largest magnitude and within 2^-17 of that
- * magnitude below it; h in four pieces, about 16 significant bits.  Other shapes widen the codes
+ * the activations as sums of E4M3 pieces (piece p weighted 2^(-4p)) and one power-of-two scale
+ * per row: x in two pieces, exact for every value above 2^-13.8 of its row's largest magnitude
+ * and within 2^-21 of that magnitude below it; h in four pieces, within 2^-16 of each value plus
+ * 2^-29 of the row's largest magnitude.  Other shapes widen the codes
  * to bf16 into Tensor Memory and run the bf16 MMA.  Code pointers 16-byte aligned; same
  * workspace and outputs as moe_forward. */
 moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,

@@ -1,0 +1,838 @@
+// FP8 (E4M3) expert weights in the grouped GEMMs: one power-of-two scale per 128 x 128 tile of
+// codes ("DeepSeek-V4 MoE", section "FP4 QAT 怎么做到反量化无损").  Two kernel families:
+//   * fp8mma_gemm_kernel: the codes are the 8-bit MMA's A operand as stored, the activations
+//     E4M3 pieces (d and d_ff multiples of 128);
+//   * fp8w_gemm_kernel: the codes are widened to bf16 into Tensor Memory and multiplied by the
+//     bf16 activations (any shape).
+#include "gemm_common.cuh"
+
+namespace moe {
+
+// ============================================================================ FP8-weight variant
+// The single-CTA kernel on FP8 (E4M3) weight codes with one power-of-two scale per 128 x 128
+// tile ("DeepSeek-V4 MoE", section "FP4 QAT 怎么做到反量化无损").  TMA brings each stage's codes
+// (64-byte rows, 64-byte swizzle) and token rows into a raw ring in shared memory; four
+// converter warps, one per TMEM lane quadrant, each widen whole weight rows to bf16 (q * 2^e,
+// exact) and store them into a ring of A tiles in Tensor Memory (lane = weight row, two bf16 per
+// column); the MMA reads A from Tensor Memory and B from the raw stage, then releases both.  The
+// weight bytes a stage streams are half those of the bf16 kernel, and the widened tiles never
+// pass through shared memory.
+// Two E4M3 codes -> two bf16 values q * 2^e in one word (low half = the first code), exact,
+// through the f16 conversion instruction: the path for zero and subnormal codes and very small
+// scales.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_exact(uint32_t two_codes, float scale) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Four normal E4M3 codes (one word) -> four bf16 values q * 2^e (two words, low half first),
+// exact.  A normal code (exponent field E in 1..15, mantissa M) is (1 + M/8) 2^(E-7), so its
+// bf16 bits are the sign, the exponent field E + 120 + e and M as the top three mantissa bits:
+// the bytes are spread into 16-bit lanes, shifted, biased (bias2 = (120 + e) in both lanes'
+// exponent fields) and signed with integer operations.
+__device__ __forceinline__ uint2 e4m3x4_normal_to_bf16x4(uint32_t w, uint32_t bias2) {
+  const uint32_t l0 = __byte_perm(w, 0u, 0x4140);  // codes 0, 1 in 16-bit lanes
+  const uint32_t l1 = __byte_perm(w, 0u, 0x4342);  // codes 2, 3
+  uint2 r;
+  r.x = (((l0 & 0x007F007Fu) << 4) + bias2) | ((l0 & 0x00800080u) << 8);
+  r.y = (((l1 & 0x007F007Fu) << 4) + bias2) | ((l1 & 0x00800080u) << 8);
+  return r;
+}
+
+// True when some code of the word has exponent field 0 (zero or subnormal).
+__device__ __forceinline__ bool e4m3x4_has_small(uint32_t w) {
+  const uint32_t t = w & 0x78787878u;                  // exponent fields, each byte < 0x80
+  return ((t - 0x01010101u) & ~t & 0x80808080u) != 0;  // some byte of t is zero
+}
+
+template <int EPI, int TN, int MBLK, bool HILO>
+struct Fp8Shape {
+  static constexpr int BLOCK_K = 64;
+  static constexpr int ROW_BYTES = 128;                  // bf16 rows of B
+  static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
+  static constexpr int RAW_SLAB = BLOCK_M * BLOCK_K;     // 128 rows x 64 E4M3 codes
+  static constexpr int RAW_A = NUM_A * RAW_SLAB;
+  static constexpr int NUM_B = HILO ? 2 : 1;
+  static constexpr int B_BYTES = TN * ROW_BYTES;
+  static constexpr int RAW_STAGE = RAW_A + NUM_B * B_BYTES;
+  static constexpr int A_COLS = BLOCK_K / 2;             // TMEM columns of one widened 128 x 64 slab
+  static constexpr int CSTAGES = 4;                      // widened-A stages in Tensor Memory
+  static constexpr int CVT_GROUPS = CSTAGES;             // group g widens every CSTAGES-th stage into slot g
+  static constexpr int NUM_CVT_WARPS = 4 * CVT_GROUPS;   // one warp per TMEM lane quadrant per group
+  static constexpr int THREADS = (2 + NUM_EPI_WARPS + NUM_CVT_WARPS) * 32;
+  static constexpr int NACC = NUM_A;
+  static constexpr int ACC_COLS = NACC * TN;
+  static constexpr int NUM_BUF = (2 * ACC_COLS + CSTAGES * NUM_A * A_COLS <= 512) ? 2 : 1;
+  static constexpr int USED_COLS = NUM_BUF * ACC_COLS;
+  static constexpr int A_COL0 = USED_COLS;               // first column of the A ring
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int RSTAGES_FIT = (SMEM_LIMIT - 1024 - 512) / RAW_STAGE;
+  static constexpr int RSTAGES = RSTAGES_FIT > 8 ? 8 : RSTAGES_FIT;
+  static constexpr int SMEM_BYTES = RSTAGES * RAW_STAGE + 1024 + 512;
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : BLOCK_M * MBLK;
+  static_assert(USED_COLS + CSTAGES * NUM_A * A_COLS <= TMEM_COLS, "TMEM: accumulators + A ring");
+  static_assert(TN % B_BOX == 0 && TN <= 256, "token tile");
+  static_assert(RSTAGES >= 2, "pipeline needs two raw stages");
+  static_assert(RAW_A % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled tiles start on 1024 bytes");
+  static_assert((2 * RSTAGES + 2 * CSTAGES + 4) * 8 + 8 <= 512, "barrier area");
+  static_assert(EPI == EPI_F32 || (MBLK == 1 && !HILO), "SwiGLU variant");
+};
+
+template <int EPI, int TN, int MBLK, bool HILO>
+__global__ void __launch_bounds__(Fp8Shape<EPI, TN, MBLK, HILO>::THREADS, 1)
+    fp8w_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using S = Fp8Shape<EPI, TN, MBLK, HILO>;
+  constexpr int BLOCK_K = S::BLOCK_K;
+  constexpr int RST = S::RSTAGES;
+  constexpr int CST = S::CSTAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw = smem;                                    // RST raw stages (codes + token rows)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + RST * S::RAW_STAGE);
+  // bars: full[RST], empty[RST], cfull[CST], cempty[CST], acc_full[2], acc_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RST + 2 * CST + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (RST + s); };
+  auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * RST + c); };
+  auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * RST + CST + c); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * RST + 2 * CST + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * RST + 2 * CST + 2 + a); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RST; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int c = 0; c < CST; ++c) {
+      mbar_init(cfull_bar(c), 4 * 32);  // the four warps of the slot's converter group
+      mbar_init(cempty_bar(c), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), NUM_EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a_sh);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int total_tiles;
+  if (p.grp != nullptr) {
+    total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks * (p.sched_tn / TN);
+  } else {
+    total_tiles = ((p.dense_rows + p.sched_tn - 1) / p.sched_tn) * p.num_mblocks * (p.sched_tn / TN);
+  }
+  const int KB = p.K / BLOCK_K;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
+        const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
+        const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * S::FEATS;
+        const uint32_t bytes = S::RAW_A + S::NUM_B * t.n_mma * S::ROW_BYTES;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, bytes);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_3d(sr, ta, fb, kb * BLOCK_K, t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);  // gate, up codes
+          } else {
+            tma_load_2d(sr, ta, fb, kb * BLOCK_K, a_row);                                   // MBLK slabs
+          }
+#pragma unroll
+          for (int bp = 0; bp < S::NUM_B; ++bp) {
+            const uint32_t sb = sr + S::RAW_A + bp * S::B_BYTES;
+            const int k0 = kb * BLOCK_K;
+            const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
+            int off = 0;
+#pragma unroll
+            for (int i = NUM_BOX_H - 1; i >= 0; --i) {
+              const int h = B_BOX << i;
+              if (h <= TN && (t.n_mma - off) >= h) {
+                tma_load_2d(sb + off * S::ROW_BYTES, tb + i, fb, kc, t.b_row + off);
+                off += h;
+              }
+            }
+          }
+          if (++stage == RST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, cs = 0;
+      uint32_t phase = 0, cphase = 0;
+      int buf = 0;
+      uint32_t buf_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        if (!mbar_wait(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(t.n_mma);
+        const uint32_t d0 = tmem_base + buf * S::ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+              !mbar_wait(cfull_bar(cs), cphase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const uint32_t ta = tmem_base + S::A_COL0 + cs * (S::NUM_A * S::A_COLS);
+#pragma unroll
+          for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+#pragma unroll
+            for (int a = 0; a < S::NUM_A; ++a) {
+#pragma unroll
+              for (int bp = 0; bp < S::NUM_B; ++bp) {
+                const uint64_t db = smem_desc_sw(sr + S::RAW_A + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
+                tc_mma_ta(d0 + a * TN, ta + a * S::A_COLS + kk * 8, db, idesc, (kb | kk | bp) ? 1u : 0u);
+              }
+            }
+          }
+          tc_commit(empty_bar(stage));
+          tc_commit(cempty_bar(cs));
+          if (++stage == RST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++cs == CST) {
+            cs = 0;
+            cphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(buf));
+        if (++buf == S::NUM_BUF) {
+          buf = 0;
+          buf_phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + NUM_EPI_WARPS) {
+    // ------------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    int buf = 0;
+    uint32_t buf_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      if (!mbar_wait(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
+      epilogue_tile<EPI, TN, S::NACC, S::FEATS>(t, p, tq, quad, half, lane, 0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+      if (++buf == S::NUM_BUF) {
+        buf = 0;
+        buf_phase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ code -> bf16 converters
+    // CVT_GROUPS groups of four warps; group g widens the stages n with n % CVT_GROUPS == g into
+    // A slot g, so that several stages are widened at once (each warp must wait for its Tensor
+    // Memory stores before reporting a stage).  Within a group, warp w owns TMEM lane quadrant
+    // w % 4, i.e. weight rows r = 32 (w % 4) + lane of every slab: the thread reads that row's 64
+    // codes (four 16-byte chunks; chunk c of row r at c ^ ((r >> 1) & 3), the 64-byte swizzle
+    // TMA wrote), widens them with the row's scale 2^e and stores the 32 columns of bf16 pairs
+    // into the slot's A tile.  A slab spans at most two 128-row tiles: the thread keeps the two
+    // exponents of the current 128-wide K tile and loads those of the next one ahead, so no
+    // global load sits in a stage's critical path and no converter waits on another.
+    const int quad = warp & 3;
+    const int group = (warp - 2 - NUM_EPI_WARPS) >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t ta = tmem_base + (uint32_t(quad * 32) << 16) + S::A_COL0 + group * (S::NUM_A * S::A_COLS);
+    const int nk = p.exp_nk;
+    uint32_t n = 0;   // stage counter over all tiles of this CTA
+    uint32_t mine = 0; // stages this group has widened
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
+      int trow[S::NUM_A];  // this row's tile row in each slab (clamped to the matrix)
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        const int base = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M : t.mb * S::FEATS + a * BLOCK_M;
+        trow[a] = min((base + r) >> 7, p.exp_nr - 1);
+      }
+      int e_cur[S::NUM_A], e_nxt[S::NUM_A];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        e_cur[a] = __ldg(ex + trow[a] * nk);
+        e_nxt[a] = nk > 1 ? __ldg(ex + trow[a] * nk + 1) : 0;
+      }
+      for (int kb = 0; kb < KB; ++kb, ++n) {
+        if (kb > 0 && ((kb * BLOCK_K) & 127) == 0) {  // a new 128-wide K tile: rotate, fetch the next
+          const int kn = ((kb * BLOCK_K) >> 7) + 1;
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) {
+            e_cur[a] = e_nxt[a];
+            e_nxt[a] = kn < nk ? __ldg(ex + trow[a] * nk + kn) : 0;
+          }
+        }
+        if ((int)(n % S::CVT_GROUPS) != group) continue;
+        const int stage = (int)(n % RST);
+        const uint32_t phase = (n / RST) & 1u;
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+            !mbar_wait(cempty_bar(group), (mine & 1u) ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        ++mine;
+        tc_fence_after();
+        const uint8_t* src = raw + stage * S::RAW_STAGE;
+#pragma unroll
+        for (int a = 0; a < S::NUM_A; ++a) {
+          const int e = e_cur[a];
+          const uint32_t bias2 = (uint32_t)(120 + e) * 0x00800080u;
+          const float scale = __int_as_float((e + 127) << 23);
+          const bool tiny = e < -120;
+          const uint8_t* row = src + a * S::RAW_SLAB + r * 64;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[16];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = 2 * h + cc;  // K codes [16 c, 16 c + 16)
+              const uint4 q = *reinterpret_cast<const uint4*>(row + ((c ^ ((r >> 1) & 3)) << 4));
+              uint2 v0, v1, v2, v3;
+              // normal codes and an ordinary scale (the common case): integer path; otherwise (a
+              // zero or subnormal code, or a scale below 2^-120, where E + 120 + e could leave the
+              // normal bf16 range) the chunk goes through the conversion instruction
+              if (!tiny && !(e4m3x4_has_small(q.x) | e4m3x4_has_small(q.y) | e4m3x4_has_small(q.z) |
+                             e4m3x4_has_small(q.w))) {
+                v0 = e4m3x4_normal_to_bf16x4(q.x, bias2);
+                v1 = e4m3x4_normal_to_bf16x4(q.y, bias2);
+                v2 = e4m3x4_normal_to_bf16x4(q.z, bias2);
+                v3 = e4m3x4_normal_to_bf16x4(q.w, bias2);
+              } else {
+                v0 = make_uint2(e4m3x2_to_bf16x2_exact(q.x, scale), e4m3x2_to_bf16x2_exact(q.x >> 16, scale));
+                v1 = make_uint2(e4m3x2_to_bf16x2_exact(q.y, scale), e4m3x2_to_bf16x2_exact(q.y >> 16, scale));
+                v2 = make_uint2(e4m3x2_to_bf16x2_exact(q.z, scale), e4m3x2_to_bf16x2_exact(q.z >> 16, scale));
+                v3 = make_uint2(e4m3x2_to_bf16x2_exact(q.w, scale), e4m3x2_to_bf16x2_exact(q.w >> 16, scale));
+              }
+              o[8 * cc + 0] = v0.x;
+              o[8 * cc + 1] = v0.y;
+              o[8 * cc + 2] = v1.x;
+              o[8 * cc + 3] = v1.y;
+              o[8 * cc + 4] = v2.x;
+              o[8 * cc + 5] = v2.y;
+              o[8 * cc + 6] = v3.x;
+              o[8 * cc + 7] = v3.y;
+            }
+            tmem_st16(ta + a * S::A_COLS + h * 16, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(cfull_bar(group));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// ============================================================================ FP8 MMA variant
+// The single-CTA kernel with the E4M3 weight codes as the MMA's A operand as they are (tcgen05
+// kind::f8f6f4, twice the bf16 rate), one power-of-two scale per 128 x 128 code tile ("DeepSeek-V4
+// MoE", section "FP4 QAT 怎么做到反量化无损").  B holds the token rows as E4M3 pieces with one
+// power-of-two scale per row and piece p weighted 2^(-4p) (x: 2 pieces, h: 4; see the split
+// kernel).  The pieces of a tile's
+// token rows sit one after another in the stage (piece p at rows p * n .. p * n + n - 1), so one
+// MMA per slab and K step multiplies all of them (N = pieces * n) and reads the A tile from
+// shared memory once.  A stage is one 128-wide K tile, so a single weight scale 2^e covers each
+// slab of it: the MMAs of K tile kt write their own slot of a ring in Tensor Memory, and the
+// epilogue warps add (sum of the piece columns x 2^(-4p)) * 2^e(kt) into fp32 registers and release the
+// slot; after the last K tile they apply the row scales and write the tile (SwiGLU: fp32 h;
+// fp32: O rows x gate weight).  The slabs must start on a scale tile (gate/up: d_ff a multiple
+// of 128).
+template <int EPI, int MBLK, int TN_>
+struct F8Shape {
+  static constexpr int TN = TN_;                        // token rows per tile (16, 32 or 64)
+  static constexpr int BLOCK_K = 128;                   // codes per stage = one scale tile of K
+  static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
+  static constexpr int A_SLAB = BLOCK_M * BLOCK_K;      // 128 weight rows x 128 codes
+  static constexpr int PIECES = (EPI == EPI_SWIGLU) ? 2 : 4;
+  static constexpr int B_PIECE = TN * BLOCK_K;          // TN token rows x 128 codes
+  static constexpr int STAGE_BYTES = NUM_A * A_SLAB + PIECES * B_PIECE;
+  static constexpr int SLOT_COLS = NUM_A * PIECES * TN; // partial products of one K tile
+  static constexpr int SLOTS = (512 / SLOT_COLS) > 8 ? 8 : (512 / SLOT_COLS);
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 512) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 512;
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : BLOCK_M * MBLK;
+  static_assert(SLOTS * SLOT_COLS <= 512, "TMEM holds 512 columns");
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(A_SLAB % 1024 == 0 && B_PIECE % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzled tiles on 1024 B");
+  static_assert((2 * STAGES + 2 * SLOTS) * 8 + 8 <= 512, "barrier area");
+  static_assert(EPI == EPI_F32 || MBLK == 1, "SwiGLU variant");
+  static_assert(TN == 16 || TN == 32 || TN == 64, "token tile");
+  static_assert(PIECES * TN <= 256, "MMA N");
+  static_assert(PIECES == 2 || PIECES == 4, "pieces are summed in pairs");
+};
+
+template <int EPI, int MBLK, int TN_>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fp8mma_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using S = F8Shape<EPI, MBLK, TN_>;
+  constexpr int TN = S::TN;
+  constexpr int ST = S::STAGES;
+  constexpr int SL = S::SLOTS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST * S::STAGE_BYTES);
+  // bars: full[ST], empty[ST], slot_full[SL], slot_empty[SL]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * ST + 2 * SL);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (ST + s); };
+  auto sfull_bar = [&](int c) { return bar0 + 8u * (2 * ST + c); };
+  auto sempty_bar = [&](int c) { return bar0 + 8u * (2 * ST + SL + c); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int c = 0; c < SL; ++c) {
+      mbar_init(sfull_bar(c), 1);
+      mbar_init(sempty_bar(c), NUM_EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a_sh);
+    for (int i = 0; (B_BOX << i) <= TN; ++i) tma_prefetch_desc(&maps.b[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int row_tiles = p.grp != nullptr ? __ldg(&p.grp[p.n_groups_total].z)
+                                         : (p.dense_rows + p.sched_tn - 1) / p.sched_tn;
+  const int total_tiles = row_tiles * p.num_mblocks * (p.sched_tn / TN);
+  const int KB = p.K / S::BLOCK_K;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
+        const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * S::FEATS;
+        const uint32_t bytes = S::NUM_A * S::A_SLAB + S::PIECES * t.n_mma * S::BLOCK_K;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, bytes);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_3d(sa, ta, fb, kb * S::BLOCK_K, t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);  // gate, up codes
+          } else {
+            tma_load_2d(sa, ta, fb, kb * S::BLOCK_K, a_row);                                   // MBLK slabs
+          }
+#pragma unroll
+          for (int pc = 0; pc < S::PIECES; ++pc) {
+            const uint32_t sb = sa + S::NUM_A * S::A_SLAB + pc * t.n_mma * S::BLOCK_K;
+            int off = 0;
+#pragma unroll
+            for (int i = 2; i >= 0; --i) {  // boxes of 64, 32, 16 rows
+              const int h = B_BOX << i;
+              if (h <= TN && (t.n_mma - off) >= h) {
+                tma_load_3d(sb + off * S::BLOCK_K, &maps.b[i], fb, kb * S::BLOCK_K, pc, t.b_row + off);
+                off += h;
+              }
+            }
+          }
+          if (++stage == ST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, sphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const uint32_t idesc = idesc_e4m3_f32(S::PIECES * t.n_mma);  // all pieces in one N
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+              !mbar_wait(sempty_bar(slot), sphase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
+          const uint32_t d0 = tmem_base + slot * S::SLOT_COLS;
+#pragma unroll
+          for (int kk = 0; kk < S::BLOCK_K / 32; ++kk) {
+            // advance 32 codes = 32 bytes along K inside the swizzle row: +2 in the >>4 field
+            const uint64_t db = smem_desc_sw(sa + S::NUM_A * S::A_SLAB, 128) + 2 * kk;
+#pragma unroll
+            for (int a = 0; a < S::NUM_A; ++a) {
+              const uint64_t da = smem_desc_sw(sa + a * S::A_SLAB, 128) + 2 * kk;
+              tc_mma_f8(d0 + a * S::PIECES * TN, da, db, idesc, kk ? 1u : 0u);
+            }
+          }
+          tc_commit(empty_bar(stage));
+          tc_commit(sfull_bar(slot));
+          if (++stage == ST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++slot == SL) {
+            slot = 0;
+            sphase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    // Warp (quad, half): TMEM lanes 32 quad .. 32 quad + 31 (weight rows), token columns
+    // 32 half .. 32 half + 31 of every slab's partial products.
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    int slot = 0;
+    uint32_t sphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      const int cols = min(32, t.rows - half * 32);  // valid token columns of this warp (may be <= 0)
+      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
+      int erow[S::NUM_A];  // each slab's row of scale tiles (clamped to the matrix)
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        const int base = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M : t.mb * S::FEATS + a * BLOCK_M;
+        erow[a] = min(base >> 7, p.exp_nr - 1) * p.exp_nk;
+      }
+      float acc[S::NUM_A][32];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[a][j] = 0.0f;
+      int e_cur[S::NUM_A];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) e_cur[a] = __ldg(ex + erow[a]);
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + half * 32;
+      for (int kb = 0; kb < KB; ++kb) {
+        int e_nxt[S::NUM_A];  // the next K tile's scales, loaded ahead of the wait
+#pragma unroll
+        for (int a = 0; a < S::NUM_A; ++a) e_nxt[a] = (kb + 1 < KB) ? __ldg(ex + erow[a] + kb + 1) : 0;
+        if (!mbar_wait(sfull_bar(slot), sphase, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (cols > 0) {
+          const uint32_t ts = tq + slot * S::SLOT_COLS;
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) {
+            const float sc = __int_as_float((e_cur[a] + 127) << 23);  // 2^e, e in [-126, 120]
+#pragma unroll
+            for (int pp = 0; pp < S::PIECES; pp += 2) {  // two pieces' columns per wait
+              const float scp = sc * (pp == 0 ? 1.0f : 0.00390625f);  // 2^e * 2^(-4 pp), exact
+              uint32_t r0[2][16], r1[2][16];
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const uint32_t c = ts + a * S::PIECES * TN + (pp + q) * t.n_mma;
+                tmem_ld16(c, r0[q]);
+                if (cols > 16) tmem_ld16(c + 16, r1[q]);
+              }
+              tmem_ld_wait();
+              reg_fence16(r0[0]);
+              reg_fence16(r0[1]);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                acc[a][j] = fmaf(fmaf(__uint_as_float(r0[1][j]), 0.0625f, __uint_as_float(r0[0][j])), scp, acc[a][j]);
+              if (cols > 16) {
+                reg_fence16(r1[0]);
+                reg_fence16(r1[1]);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  acc[a][16 + j] =
+                      fmaf(fmaf(__uint_as_float(r1[1][j]), 0.0625f, __uint_as_float(r1[0][j])), scp, acc[a][16 + j]);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty_bar(slot));
+#pragma unroll
+        for (int a = 0; a < S::NUM_A; ++a) e_cur[a] = e_nxt[a];
+        if (++slot == SL) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+      }
+      if (!ok || cols <= 0) continue;
+      // row scales 2^e_r (the pieces hold row r times 2^-e_r) and the gate weight: lane l holds
+      // those of token column 32 half + l
+      const int rl = half * 32 + lane;
+      const bool rvalid = rl < t.rows;
+      const int er = rvalid ? __ldg(p.b_exp + t.b_row + rl) : 0;
+      float cs_l = __int_as_float((127 + er) << 23);  // e_r in [-126, 120]
+      if (EPI == EPI_F32 && p.row_scale != nullptr && !t.shared && rvalid) cs_l *= __ldg(p.row_scale + t.out_row + rl);
+      float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + half * 32) * p.out_ld;
+      if (EPI == EPI_SWIGLU) {
+        const int feat = t.mb * BLOCK_M + quad * 32 + lane;
+        const bool fvalid = feat < p.out_features;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float cs = __shfl_sync(0xffffffffu, cs_l, j);
+          if (j < cols && fvalid) {
+            const float g = acc[0][j] * cs, u = acc[1][j] * cs;
+            out[(size_t)j * p.out_ld + feat] = __fdividef(g, 1.0f + __expf(-g)) * u;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float cs = __shfl_sync(0xffffffffu, cs_l, j);
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) {
+            const int feat = t.mb * S::FEATS + a * BLOCK_M + quad * 32 + lane;
+            if (j < cols && feat < p.out_features) out[(size_t)j * p.out_ld + feat] = acc[a][j] * cs;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------- host side
+
+// E4M3 weight codes: 2-D uint8 [rows, cols] with boxes of box_k codes x box_rows rows, and the
+// gate/up 3-D view (cols, d_ff, 2*groups) with boxes (box_k, 128, 2).  box_k = 64: 64-byte
+// swizzle, so that the converter warps' row-wise 16-byte reads spread over all banks; box_k =
+// 128: 128-byte swizzle, the K-major layout the 8-bit MMA reads.
+static bool make_tmap_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows, int box_k = 64) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_tmap_u8_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t cols,
+                                int box_k = 64) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
+  cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(d_ff * cols)};
+  cuuint32_t box[3] = {(cuuint32_t)box_k, (cuuint32_t)BLOCK_M, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// E4M3 activation pieces [rows, pieces, K]: 3-D view (K, pieces, rows) with boxes of
+// (128, 1, box_rows), i.e. box_rows rows of 128 codes of one piece, 128-byte swizzle.
+static bool make_tmap_pieces(CUtensorMap* m, const void* ptr, int64_t rows, int pieces, int64_t K, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)pieces, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)(pieces * K)};
+  cuuint32_t box[3] = {128, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI, int TN, int MBLK, bool HILO>
+static cudaError_t launch_fp8_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
+  using Sh = Fp8Shape<EPI, TN, MBLK, HILO>;
+  static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
+  if (p.sched_tn % TN != 0 || L.K % 64 != 0 || p.ksplit != 1 || L.a_exp == nullptr) return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr && L.a_sh_exp == nullptr) return cudaErrorInvalidValue;
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  if (EPI == EPI_SWIGLU) {
+    const int64_t f = L.a_up_offset;
+    if (!make_tmap_u8_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, L.K)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8_gateup(&m.a_sh, L.a_sh_ptr, 1, f, L.K)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_u8(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M * MBLK)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M * MBLK))
+      return cudaErrorInvalidValue;
+  }
+  if (L.a_sh_ptr == nullptr) m.a_sh = m.a;
+  const int kb_cols = HILO ? 2 * L.K : L.K;
+  for (int i = 0; i < NUM_BOX_H; ++i) {
+    const int h = B_BOX << i;
+    if (h > TN) break;
+    if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h, 64)) return cudaErrorInvalidValue;
+    if (L.b_sh_ptr != nullptr) {
+      if (!make_tmap(&m.b_sh[i], L.b_sh_ptr, L.b_sh_rows, kb_cols, h, 64)) return cudaErrorInvalidValue;
+    } else {
+      m.b_sh[i] = m.b[i];
+    }
+  }
+  p.a_exp = L.a_exp;
+  p.a_sh_exp = L.a_sh_exp != nullptr ? L.a_sh_exp : L.a_exp;
+  p.exp_nr = (L.a_rows_per_group + 127) / 128;
+  p.exp_nk = (L.K + 127) / 128;
+  auto kern = fp8w_gemm_kernel<EPI, TN, MBLK, HILO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int grid = L.num_sms;
+  const int tiles = L.max_tiles * (p.sched_tn / TN);
+  if (tiles < grid) grid = tiles;
+  if (grid < 1) grid = 1;
+  kern<<<grid, Sh::THREADS, Sh::SMEM_BYTES, s>>>(m, p);
+  return cudaGetLastError();
+}
+
+template <int EPI, int MBLK, int TN>
+static cudaError_t launch_fp8mma_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
+  using Sh = F8Shape<EPI, MBLK, TN>;
+  static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
+  if (p.sched_tn % Sh::TN != 0 || L.K % Sh::BLOCK_K != 0 || p.ksplit != 1) return cudaErrorInvalidValue;
+  if (L.a_exp == nullptr || L.b_exp == nullptr || (L.a_sh_ptr != nullptr && L.a_sh_exp == nullptr))
+    return cudaErrorInvalidValue;
+  if (EPI == EPI_SWIGLU && L.a_up_offset % 128 != 0) return cudaErrorInvalidValue;  // slabs on scale tiles
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  if (EPI == EPI_SWIGLU) {
+    const int64_t f = L.a_up_offset;
+    if (!make_tmap_u8_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, L.K, 128)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8_gateup(&m.a_sh, L.a_sh_ptr, 1, f, L.K, 128))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_u8(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M * MBLK, 128)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M * MBLK, 128))
+      return cudaErrorInvalidValue;
+  }
+  if (L.a_sh_ptr == nullptr) m.a_sh = m.a;
+  for (int i = 0; (B_BOX << i) <= Sh::TN; ++i)
+    if (!make_tmap_pieces(&m.b[i], L.b_ptr, L.b_rows, Sh::PIECES, L.K, B_BOX << i)) return cudaErrorInvalidValue;
+  p.a_exp = L.a_exp;
+  p.a_sh_exp = L.a_sh_exp != nullptr ? L.a_sh_exp : L.a_exp;
+  p.exp_nr = (L.a_rows_per_group + 127) / 128;
+  p.exp_nk = (L.K + 127) / 128;
+  p.b_exp = L.b_exp;
+  auto kern = fp8mma_gemm_kernel<EPI, MBLK, TN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int grid = L.num_sms;
+  const int tiles = L.max_tiles * (p.sched_tn / Sh::TN);
+  if (tiles < grid) grid = tiles;
+  if (grid < 1) grid = 1;
+  kern<<<grid, NUM_THREADS, Sh::SMEM_BYTES, s>>>(m, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_gemm(const GemmLaunch& L, GemmParams p, int kernel_tn, cudaStream_t s) {
+  if (L.q8 == 2) {
+    // FP8 weight codes straight into the MMA, E4M3-piece activations, 16-, 32- or 64-row token
+    // tiles (the down projection's 64-row tiles on one 128-feature slab: its four pieces then
+    // fill N = 256)
+    if (L.epi == EPI_SWIGLU && kernel_tn == 16) return launch_fp8mma_variant<EPI_SWIGLU, 1, 16>(L, p, s);
+    if (L.epi == EPI_SWIGLU && kernel_tn == 32) return launch_fp8mma_variant<EPI_SWIGLU, 1, 32>(L, p, s);
+    if (L.epi == EPI_SWIGLU && kernel_tn == 64) return launch_fp8mma_variant<EPI_SWIGLU, 1, 64>(L, p, s);
+    if (L.epi != EPI_SWIGLU && kernel_tn == 16 && L.mblk == 2) return launch_fp8mma_variant<EPI_F32, 2, 16>(L, p, s);
+    if (L.epi != EPI_SWIGLU && kernel_tn == 32 && L.mblk == 2) return launch_fp8mma_variant<EPI_F32, 2, 32>(L, p, s);
+    if (L.epi != EPI_SWIGLU && kernel_tn == 64 && L.mblk == 1) return launch_fp8mma_variant<EPI_F32, 1, 64>(L, p, s);
+    return cudaErrorInvalidValue;
+  }
+  if (L.q8 == 1) {
+    // codes widened to bf16: single-CTA kernels with 64-row token tiles
+    if (L.epi == EPI_SWIGLU && kernel_tn == 64) return launch_fp8_variant<EPI_SWIGLU, 64, 1, false>(L, p, s);
+    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == 64 && L.mblk == 2)
+      return launch_fp8_variant<EPI_F32, 64, 2, true>(L, p, s);
+    return cudaErrorInvalidValue;
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -75,14 +75,16 @@ cudaError_t launch_quantize_fp8(const void* w, int n_mats, int rows, int K, uint
 // Activation rows as sums of E4M3 pieces, the B operand of the FP8-weight MMA kernels.
 //
 // Row r becomes P pieces of K codes (piece p at dst + (r * P + p) * K) and one exponent
-// exps[r] = e: the scale 2^-e brings the row's largest magnitude into (224, 448] (e as for the
-// weight tiles: the smallest integer with amax <= 448 * 2^e, 0 for a zero row, at least -126);
-// with v = value * 2^-e (exact), piece 0 is the E4M3 rounding (nearest, ties to even) of v and
-// piece p the rounding of what pieces 0..p-1 leave, so that sum_p piece_p * 2^e reproduces the
-// row.  Each piece removes all but 2^-4 of the remainder while it is a normal E4M3 value: two
-// pieces reproduce a bf16 value (8 significant bits) exactly when |v| >= 2^-2, four pieces
-// leave at most 2^-16 of |v|; below that, the subnormal step (2^-9) bounds the error by 2^-10,
-// i.e. by less than 2^-17 of the row's largest magnitude.
+// exps[r] = e such that row = 2^e * sum_p piece_p * 2^(-4p).  The scale 2^-e brings the row's
+// largest magnitude into (224, 448] (e as for the weight tiles: the smallest integer with
+// amax <= 448 * 2^e, 0 for a zero row, at least -126).  With v = value * 2^-e (exact), piece 0
+// is the E4M3 rounding (nearest, ties to even) of v, and piece p the rounding of 16 times what
+// the pieces before it leave: a normal E4M3 rounding leaves at most 2^-4 of its input, so each
+// piece stays within the E4M3 range while the subnormal step (2^-9) of piece p sits at
+// 2^(-9-4p) of v's scale.  Two pieces reproduce a bf16 value (8 significant bits) exactly when
+// |v| >= 2^-6, i.e. above 2^-13.8 of the row's largest magnitude, and within 2^-14 of the scale
+// (2^-21.8 of the largest magnitude) below that; four pieces keep 2^-16 of every value above the
+// floor of 2^-22 of the scale (2^-29.8 of the largest magnitude).
 //
 // One CTA per row; the row is staged in shared memory as fp32 before any piece is written, so
 // the fp32 source may be the destination itself (P = 4: a row's pieces fill exactly its fp32
@@ -158,10 +160,12 @@ __global__ void __launch_bounds__(SPLIT_THREADS) split_rows_e4m3_kernel(const vo
         const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(c23, __NV_E4M3);
         const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
         const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-        v[0] -= f01.x;  // exact: the rounding and its source are within a factor of two
-        v[1] -= f01.y;
-        v[2] -= f23.x;
-        v[3] -= f23.y;
+        // what the piece leaves, times 16 (exact: a rounding and its source lie within a factor
+        // of two of each other, and the remainder is at most 2^-4 of the source or below 2^-10)
+        v[0] = (v[0] - f01.x) * 16.0f;
+        v[1] = (v[1] - f01.y) * 16.0f;
+        v[2] = (v[2] - f23.x) * 16.0f;
+        v[3] = (v[3] - f23.y) * 16.0f;
       }
     }
   }

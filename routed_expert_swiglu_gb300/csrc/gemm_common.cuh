@@ -1,0 +1,190 @@
+// Definitions shared by the grouped-GEMM translation units (the bf16 kernels in
+// grouped_gemm.cu, the FP8-weight kernels in fp8_gemm.cu): tile constants, the kernel parameter
+// block, the tensor-map set, the device-side tile schedule, the single-CTA epilogue and the bf16
+// tensor-map helper.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int BLOCK_M = 128;
+constexpr int B_BOX = 16;            // rows per TMA box of the B operand
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = (2 + NUM_EPI_WARPS) * 32;
+constexpr int SMEM_LIMIT = 232448;   // dynamic shared memory per block on sm_103a
+enum { EPI_SWIGLU = 0, EPI_F32 = 1 };
+
+struct GemmParams {
+  int K;                // reduction length of the weight (A) operand, multiple of 64
+  int num_mblocks;      // output-feature blocks per group (128 features, or 128*MBLK for fp32)
+  int a_rows_per_group;
+  int a_up_offset;      // SwiGLU: row offset of the up rows (W3) after the gate rows (W1)
+  int out_features;
+  int out_ld;
+  void* out;
+  const float* row_scale;
+  int n_routed;
+  int shared_b_shift;
+  const int4* grp;      // {row_base, rows, first row tile, 0}; grp[G].z = total row tiles
+  const int* rt2g;
+  int n_groups_total;   // G (index of the total entry)
+  int sched_tn;         // rows per row tile of the schedule (a multiple of the kernel's TN)
+  int ksplit;           // dense (router) schedule only: K split into ksplit slices, slice s
+                        // writing its partial result at out + s * split_stride
+  long long split_stride;
+  int dense_rows;
+  int* err;
+  // gathered B (pair gate/up): routed row r of a group is row b_idx[r] of b_x ([*, b_ld] bf16),
+  // a shared-expert row r is row r + shared_b_shift of b_x
+  const __nv_bfloat16* b_x;
+  const int32_t* b_idx;
+  int b_ld;
+  // FP8 weights: int8 tile exponents [mats, exp_nr, exp_nk] of the routed (a_exp) and shared
+  // (a_sh_exp) weight codes, one per 128 x 128 tile of each matrix
+  const int8_t* a_exp;
+  const int8_t* a_sh_exp;
+  int exp_nr, exp_nk;
+  // E4M3-piece activations: one power-of-two exponent per B row
+  const int32_t* b_exp;
+};
+
+// Tensor maps of one launch.  The B operand has one map per box height 16 << i (i < 5), so a
+// tile of n rows is loaded with at most five boxes (binary decomposition of n / 16).
+constexpr int NUM_BOX_H = 5;
+struct GemmMaps {
+  CUtensorMap a, a_sh;
+  CUtensorMap b[NUM_BOX_H], b_sh[NUM_BOX_H];
+};
+
+struct Tile {
+  int g, mb, b_row, out_row, rows, n_mma;
+  bool shared;
+};
+
+// Tile id -> (group, m-block, row sub-tile).  The schedule counts row tiles of sched_tn rows;
+// a kernel with a smaller TN splits each into sched_tn / TN sub-tiles, some of which may be
+// empty (rows <= 0): every role skips those identically.
+template <int TN>
+__device__ __forceinline__ Tile decode_tile(int tile, const GemmParams& p) {
+  Tile t;
+  const int split = p.sched_tn / TN;
+  const int per_rt = p.num_mblocks * split;
+  const int rt_glob = tile / per_rt;
+  int row_base, rows_g, rt_start;
+  if (p.grp != nullptr) {
+    t.g = __ldg(p.rt2g + rt_glob);
+    const int4 gi = __ldg(p.grp + t.g);
+    row_base = gi.x;
+    rows_g = gi.y;
+    rt_start = gi.z;
+  } else {
+    t.g = 0;
+    row_base = 0;
+    rows_g = p.dense_rows;
+    rt_start = 0;
+  }
+  const int R = ((rows_g + p.sched_tn - 1) / p.sched_tn) * split;
+  const int local = tile - rt_start * per_rt;
+  t.mb = local / R;
+  const int rt = local - t.mb * R;
+  t.rows = min(TN, rows_g - rt * TN);
+  t.n_mma = max(16, (t.rows + 15) & ~15);
+  t.out_row = row_base + rt * TN;
+  t.shared = (p.grp != nullptr) && (t.g == p.n_routed);
+  t.b_row = t.out_row + (t.shared ? p.shared_b_shift : 0);
+  return t;
+}
+
+// Epilogue of one tile of the single-CTA kernels, run by each of the 8 epilogue warps on its TMEM
+// lane quadrant (`quad`) and its half of the 16-column chunks (`half`): SwiGLU -> the bf16
+// (hi, lo) activation pair, fp32 -> O rows (x optional row scale).  tq = the quadrant's address
+// in the tile's accumulator buffer.
+template <int EPI, int TN, int NACC, int FEATS>
+__device__ __forceinline__ void epilogue_tile(const Tile& t, const GemmParams& p, uint32_t tq, int quad, int half,
+                                              int lane, long long out_shift) {
+  const int nchunk = (t.rows + 15) >> 4;
+  if (EPI == EPI_SWIGLU) {
+    const int feat = t.mb * BLOCK_M + quad * 32 + lane;
+    // h is stored as an unevaluated pair hi + lo of bf16 values: hi = bf16(h),
+    // lo = bf16(h - hi), so the down projection sees h to ~16 significant bits.  Within
+    // each 64-feature block, hi occupies columns [128*b, 128*b + 64) and lo the next 64.
+    const int col = ((feat >> 6) << 7) + (feat & 63);
+    const bool fvalid = feat < p.out_features;
+    for (int ci = half; ci < nchunk; ci += 2) {
+      const int c0 = ci * 16;
+      uint32_t rg[16], ru[16];
+      tmem_ld16(tq + c0, rg);
+      tmem_ld16(tq + TN + c0, ru);
+      tmem_ld_wait();
+      reg_fence16(rg);
+      reg_fence16(ru);
+      if (fvalid) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
+        const int nr = min(16, t.rows - c0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (j < nr) {
+            const float g = __uint_as_float(rg[j]);
+            const float u = __uint_as_float(ru[j]);
+            const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+            out[(size_t)j * p.out_ld] = hi;
+            out[(size_t)j * p.out_ld + 64] = lo;
+          }
+        }
+      }
+    }
+  } else {
+    const bool scaled = (p.row_scale != nullptr) && !t.shared;
+    for (int w = half; w < NACC * nchunk; w += 2) {
+      const int a = w / nchunk;
+      const int c0 = (w - a * nchunk) * 16;
+      const int feat = t.mb * FEATS + a * BLOCK_M + quad * 32 + lane;
+      uint32_t r[16];
+      tmem_ld16(tq + a * TN + c0, r);
+      tmem_ld_wait();
+      reg_fence16(r);
+      if (feat < p.out_features) {
+        float* out = static_cast<float*>(p.out) + out_shift + (size_t)(t.out_row + c0) * p.out_ld + feat;
+        const int nr = min(16, t.rows - c0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (j < nr) {
+            const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
+            out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
+          }
+        }
+      }
+    }
+  }
+}
+
+// 2-D bf16 tensor [rows, cols] (cols innermost, contiguous), box bk x box_rows, swizzle of
+// 2*bk bytes (bk = 64: 128-byte, bk = 32: 64-byte).
+inline bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows, int bk) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, bk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The FP8-weight grouped GEMMs (fp8_gemm.cu) for a launch with L.q8 set: 1 = codes widened to
+// bf16 in Tensor Memory, 2 = codes straight into the 8-bit MMA with E4M3-piece activations.
+cudaError_t launch_fp8_gemm(const GemmLaunch& L, GemmParams p, int kernel_tn, cudaStream_t s);
+
+}  // namespace moe

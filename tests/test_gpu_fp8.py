@@ -131,3 +131,34 @@ def test_fp8_layer_with_zero_subnormal_and_tiny_scale_codes():
     ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
     check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
     layer.close()
+
+
+def test_fp8_layer_with_wide_activation_range():
+    """Activation rows whose entries span 2^-20 .. 2^6 of their typical size (the E4M3 pieces
+    share one power-of-two scale per row, so small entries sit near the pieces' subnormal
+    floor), plus a row scaled by 2^-60, an all-zero row and a row with one entry 2^10 larger
+    than the rest: the FP8 layer against the oracle on the same inputs."""
+    w = W.Workload("range_T48", T=48, d=512, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX)
+    inp = inputs.make_layer_inputs(w, seed=29, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(7)
+    expo = torch.randint(-20, 7, inp.x.shape, generator=g, device=DEV).float()
+    inp.x.copy_((inp.x.float() * torch.exp2(expo)).to(torch.bfloat16))
+    inp.x[3] = (inp.x[3].float() * 2.0 ** -60).to(torch.bfloat16)
+    inp.x[5] = 0
+    inp.x[7, 11] = (inp.x[7, 11].float() * 2.0 ** 10).to(torch.bfloat16)
+    layer = binding.MoELayer(w, inp)
+    q = layer.quantize_fp8()
+    y = layer.forward_fp8(inp.x, q, None)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    fetch = OracleFp8Fetcher(inp)
+    tok = np.nonzero(same)[0]
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    got = y.double().cpu().numpy()[tok]
+    e, n = check_output(got, ref, label=w.name)
+    print(f"{w.name} (fp8 weights): max elementwise {e:.2e}, normwise {n:.2e}")
+    if 5 in tok:
+        assert np.array_equal(got[list(tok).index(5)], ref[list(tok).index(5)])  # zero row: exactly 0
+    layer.close()
