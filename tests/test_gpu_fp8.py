@@ -162,3 +162,32 @@ def test_fp8_layer_with_wide_activation_range():
     if 5 in tok:
         assert np.array_equal(got[list(tok).index(5)], ref[list(tok).index(5)])  # zero row: exactly 0
     layer.close()
+
+
+# Full sizes, in the launch configuration bench.py times for FP8 weights (its decode leg):
+# routing against the oracle on every token, the output on a few sampled tokens (the oracle
+# quantises and dequantises every expert those tokens touch, a few seconds each).
+FULL_FP8 = [(W.V4FLASH_T64, 4), (W.MIXTRAL_T16, 2)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w,sample", FULL_FP8, ids=lambda v: getattr(v, "name", str(v)))
+def test_fp8_full_size_layer(w, sample):
+    inp = inputs.make_layer_inputs(w, seed=0, device=DEV)
+    layer = binding.MoELayer(w, inp)
+    q = layer.quantize_fp8()
+    y = layer.forward_fp8(inp.x, q, inp.token_ids)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    rng = np.random.default_rng(4321)
+    cand = np.nonzero(same)[0]
+    tok = np.sort(rng.choice(cand, size=min(sample, cand.size), replace=False))
+    fetch = OracleFp8Fetcher(inp)
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
+    print(f"{w.name} full size (fp8 weights), sample of {tok.size}: max elementwise {e:.2e}, normwise {n:.2e}")
+    layer.close()
+    del layer, inp, y, v, q
+    torch.cuda.empty_cache()
