@@ -7,3 +7,4 @@ from .moe_oracle import (DENOM_MIN, SCORES, affinity, bias_update, forward, perm
                          route, router_logits, sigmoid, silu, softmax, softplus,
                          sqrt_softplus, swiglu_expert)
 from . import fp8_weights  # noqa: E402,F401
+from . import mxfp4_weights  # noqa: E402,F401
