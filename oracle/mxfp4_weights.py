@@ -18,8 +18,9 @@ the reading taken here:
     largest s of its 128 x 128 tile minus 14, which is exactly the headroom: a value
     q * 2^t (q on the E2M1 grid) is an E4M3 value for every q iff -8 <= t <= 6, so with the FP8
     tile exponent E = (largest s of the tile) - 6 every sub-block has t = s - E in [-8, 6] and
-    the conversion is exact.  An all-zero sub-block takes the raised value (its codes are 0).
-    So every s fits an int8 (>= -128) and every E is at least -120;
+    the conversion is exact.  An all-zero sub-block (its codes are 0) takes the largest s of
+    its tile, MIN_EXP in an all-zero tile.  So every s fits an int8 (>= -128) and every tile
+    exponent E is at least -120 (within the FP8 tiles' exponent range, >= -126);
   * codes are the round-to-nearest-even of w * 2^-s on the E2M1 grid.
 """
 from __future__ import annotations
@@ -90,7 +91,7 @@ def quantize_mxfp4(w):
             nz = amax[..., i:i + TILE, j:j + TILE // BLOCK] > 0
             top = np.where(nz, f, MIN_EXP).max(axis=(-2, -1), keepdims=True)
             floor = top - HEADROOM
-            exps[..., i:i + TILE, j:j + TILE // BLOCK] = np.where(nz, np.maximum(f, floor), floor)
+            exps[..., i:i + TILE, j:j + TILE // BLOCK] = np.where(nz, np.maximum(f, floor), top)
     scaled = blocks * np.ldexp(1.0, -exps)[..., None]    # exact: power-of-two scaling
     codes = round_to_e2m1_code(scaled).reshape(w.shape)
     return codes, exps

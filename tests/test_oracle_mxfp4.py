@@ -85,9 +85,13 @@ def test_conversion_to_fp8_is_lossless():
     rng = np.random.default_rng(3)
     w = rng.normal(0, 1, (3, 200, 320)) * np.ldexp(1.0, rng.integers(-20, 6, (3, 200, 10)).repeat(32, -1))
     w[1, 128:, :128] = 0.0                # an all-zero FP8 tile
+    w[2, 7, 64:96] = 0.0                  # an all-zero sub-block in a non-zero tile
     codes, exps = M.quantize_mxfp4(w)
     c8, e8 = M.mxfp4_to_fp8(codes, exps)
     assert c8.shape == codes.shape and e8.shape == (3, 2, 3)
+    assert e8[1, 1, 0] == M.MIN_EXP - 6 and (exps[1, 128:, :4] == M.MIN_EXP).all()
+    assert exps[2, 7, 2] == exps[2, :128, :4].max()      # zero sub-block: the tile's largest
+    assert e8.min() >= -126 and exps.min() >= -128
     assert np.array_equal(F8.dequantize_fp8_tiles(c8, e8), M.dequantize_mxfp4(codes, exps))
     # the FP8 tile exponent is the tile's largest sub-block exponent minus 6
     assert e8[0, 0, 0] == exps[0, :128, :4].max() - 6
