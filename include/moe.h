@@ -157,6 +157,29 @@ moe_status moe_permute_noalloc(moe_plan* plan, int32_t T, const int32_t* topk_id
 moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int32_t K, uint8_t* codes,
                             int8_t* exps, moe_stream_t stream);
 
+/* MXFP4 (E2M1) weights with one power-of-two scale per 1 x 32 sub-block ("DeepSeek-V4 MoE",
+ * section "FP4 QAT 怎么做到反量化无损": FP4 E2M1 sub-blocks of 1 x 32, losslessly dequantised to
+ * FP8 E4M3 tiles of 128 x 128 while the sub-block scales inside a tile stay within the FP8
+ * exponent headroom).
+ *   w [n_mats, rows, K] bf16 (device, 16-byte aligned, K a multiple of 32) -> codes
+ *   [n_mats, rows, K/2] uint8 (16-byte aligned; element 2i in the low nibble of byte i; code =
+ *   sign << 3 | index of the magnitude in {0, 0.5, 1, 1.5, 2, 3, 4, 6}) and exps
+ *   [n_mats, rows, K/32] int8.  s = the smallest integer with max|w| <= 6 * 2^s over the
+ *   sub-block (at least -114), raised to (the largest s of its 128 x 128 tile) - 14 where lower;
+ *   an all-zero sub-block takes the tile's largest s.  code = round-to-nearest-even of w * 2^-s
+ *   on the E2M1 grid, zero stored as +0.  Enqueued on `stream`; no plan needed. */
+moe_status moe_quantize_mxfp4(const moe_bf16* w, int32_t n_mats, int32_t rows, int32_t K, uint8_t* codes,
+                              int8_t* exps, moe_stream_t stream);
+
+/* The lossless conversion of MXFP4 weights (as moe_quantize_mxfp4 writes them) to the FP8 form
+ * of moe_quantize_fp8: per 128 x 128 tile, E = (largest sub-block exponent) - 6 and each element
+ * the E4M3 code of q * 2^(s - E), exact because s - E lies in [-8, 6].  codes [n_mats, rows,
+ * K/2], exps [n_mats, rows, K/32] -> q8 [n_mats, rows, K] (16-byte aligned), e8 [n_mats,
+ * ceil(rows/128), ceil(K/128)], ready for moe_forward_fp8.  Exponents from elsewhere that
+ * exceed the headroom are rounded to nearest E4M3 (saturating).  Enqueued on `stream`. */
+moe_status moe_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int32_t n_mats, int32_t rows, int32_t K,
+                            uint8_t* q8, int8_t* e8, moe_stream_t stream);
+
 /* moe_forward with FP8 expert weights (the router stays bf16): q13 [E, 2*d_ff, d] and q2
  * [E, d, d_ff] hold E4M3 codes, e13 [E, ceil(2*d_ff/128), ceil(d/128)] and e2 [E, ceil(d/128),
  * ceil(d_ff/128)] their tile exponents, as moe_quantize_fp8 writes them (shared expert: the

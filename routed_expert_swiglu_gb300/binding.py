@@ -28,7 +28,7 @@ EXPORTED = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_r
             "moe_forward", "moe_forward_routed", "moe_forward_host", "moe_check_status",
             "moe_workspace_views", "moe_forward_stage_count", "moe_plan_set_events",
             "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc",
-            "moe_update_bias", "moe_quantize_fp8", "moe_forward_fp8")
+            "moe_update_bias", "moe_quantize_fp8", "moe_forward_fp8", "moe_quantize_mxfp4", "moe_mxfp4_to_fp8")
 
 
 class MoEError(RuntimeError):
@@ -80,6 +80,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_update_bias": ([P, I, V, V, ctypes.c_float, V], I),
         "moe_quantize_fp8": ([V, I, I, I, V, V, V], I),
         "moe_forward_fp8": ([P, I, V, V, V, V, V, V, V, V, V, V, V, V, V, V, S, V], I),
+        "moe_quantize_mxfp4": ([V, I, I, I, V, V, V], I),
+        "moe_mxfp4_to_fp8": ([V, V, I, I, I, V, V, V], I),
     }
     for name, (argt, rest) in sig.items():
         fn = getattr(lib, name)
@@ -177,6 +179,34 @@ def quantize_fp8(w, stream=None):
     exps = torch.empty(tuple(w.shape[:-2]) + (-(-rows // 128), -(-K // 128)), dtype=torch.int8, device=w.device)
     moe_quantize_fp8(w, codes, exps, stream)
     return codes, exps
+
+
+def quantize_mxfp4(w, stream=None):
+    """MXFP4 codes [.., rows, K/2] (uint8, two per byte) and 1 x 32 sub-block exponents
+    [.., rows, K/32] (int8) of bf16 weights w [.., rows, K]."""
+    rows, K = w.shape[-2:]
+    n = 1
+    for v in w.shape[:-2]:
+        n *= v
+    codes = torch.empty(tuple(w.shape[:-1]) + (K // 2,), dtype=torch.uint8, device=w.device)
+    exps = torch.empty(tuple(w.shape[:-1]) + (K // 32,), dtype=torch.int8, device=w.device)
+    _check(load().moe_quantize_mxfp4(_ptr(w), n, rows, K, _ptr(codes), _ptr(exps), _stream(stream)),
+           "moe_quantize_mxfp4")
+    return codes, exps
+
+
+def mxfp4_to_fp8(codes, exps, stream=None):
+    """The FP8 codes [.., rows, K] and 128 x 128 tile exponents of MXFP4 weights (lossless)."""
+    rows, K = codes.shape[-2], codes.shape[-1] * 2
+    n = 1
+    for v in codes.shape[:-2]:
+        n *= v
+    q8 = torch.empty(tuple(codes.shape[:-1]) + (K,), dtype=torch.uint8, device=codes.device)
+    e8 = torch.empty(tuple(codes.shape[:-2]) + (-(-rows // 128), -(-K // 128)), dtype=torch.int8,
+                     device=codes.device)
+    _check(load().moe_mxfp4_to_fp8(_ptr(codes), _ptr(exps), n, rows, K, _ptr(q8), _ptr(e8), _stream(stream)),
+           "moe_mxfp4_to_fp8")
+    return q8, e8
 
 
 def moe_forward_fp8(plan, T, x, token_ids, w_r, bias, q13, e13, q2, e2, q13_sh, e13_sh, q2_sh, e2_sh, out, ws,
@@ -281,6 +311,20 @@ class MoELayer:
             q["w13_sh"] = quantize_fp8(inp.w13_sh, stream)
             q["w2_sh"] = quantize_fp8(inp.w2_sh, stream)
         return q
+
+    def quantize_mxfp4(self, stream=None):
+        """MXFP4 codes and sub-block exponents of this layer's expert weights."""
+        inp = self.inputs
+        q = {"w13": quantize_mxfp4(inp.w13, stream), "w2": quantize_mxfp4(inp.w2, stream)}
+        if inp.w13_sh is not None:
+            q["w13_sh"] = quantize_mxfp4(inp.w13_sh, stream)
+            q["w2_sh"] = quantize_mxfp4(inp.w2_sh, stream)
+        return q
+
+    @staticmethod
+    def mxfp4_to_fp8(q4, stream=None):
+        """The FP8 form (for forward_fp8) of MXFP4 weights from quantize_mxfp4."""
+        return {k: mxfp4_to_fp8(c, e, stream) for k, (c, e) in q4.items()}
 
     def forward_fp8(self, x, q, token_ids=None, out=None, stream=None):
         """The layer with FP8 expert weights q (from quantize_fp8)."""

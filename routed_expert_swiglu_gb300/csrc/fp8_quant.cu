@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+#include <limits.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -192,6 +193,188 @@ cudaError_t launch_split_rows_e4m3(const void* src, bool bf16_src, const int32_t
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------------
+// MXFP4 (E2M1) weights with one power-of-two scale per 1 x 32 sub-block, and their lossless
+// conversion to the FP8 tiles above ("DeepSeek-V4 MoE", section "FP4 QAT 怎么做到反量化无损":
+// FP4 sub-blocks of 1 x 32, FP8 tiles of 128 x 128, the FP4 -> FP8 dequantisation lossless while
+// the sub-block scales inside a tile stay within the FP8 exponent headroom).
+//
+// E2M1 code = sign << 3 | magnitude index, magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}; two codes
+// per byte, the even column in the low nibble.  Sub-block exponent: the smallest s with
+// amax <= 6 * 2^s (frexp: amax = m * 2^x, s = x - 3 if m <= 0.75 else x - 2), at least -114,
+// then raised to (the largest s of its 128 x 128 tile) - 14; an all-zero sub-block takes the
+// tile's largest s (-114 in an all-zero tile), so that E below is at least -120.  q * 2^t is an E4M3 value for every magnitude q iff -8 <= t <= 6, so with the
+// FP8 tile exponent E = (largest s) - 6 the conversion is exact.  One CTA per 128 x 128 tile,
+// two sub-blocks per thread; deterministic.
+constexpr int MX_BLOCK = 32;
+constexpr int MX_HEADROOM = 14;
+constexpr int MX_MIN_EXP = -114;
+
+// Round-to-nearest-even magnitude index of a (0 <= a <= 6) on the E2M1 grid: the count of grid
+// midpoints below a, a midpoint counting when a passes it towards the neighbour with the even
+// index (0.25 -> 0, 0.75 -> 2, 1.25 -> 2, 1.75 -> 4, 2.5 -> 4, 3.5 -> 6, 5 -> 6).
+__device__ __forceinline__ uint32_t e2m1_index(float a) {
+  return (uint32_t)(a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+}
+
+__device__ __forceinline__ float e2m1_magnitude(uint32_t idx) {
+  // 0, 0.5, 1, 1.5, 2, 3, 4, 6
+  const float lo = (idx & 1u) ? 1.5f : 1.0f;
+  const int e = (int)(idx >> 1) - 1;
+  return idx < 2 ? 0.5f * (float)idx : ldexpf(lo, e);
+}
+
+__global__ void __launch_bounds__(256) quantize_mxfp4_kernel(const __nv_bfloat16* __restrict__ w, int rows, int K,
+                                                             uint8_t* __restrict__ codes, int8_t* __restrict__ exps) {
+  __shared__ int s_top[8];
+  __shared__ int s_tile_top;
+  const int kb = K / MX_BLOCK;                       // sub-blocks per row
+  const int mat = blockIdx.z, r0 = blockIdx.y * QTILE, b0 = blockIdx.x * (QTILE / MX_BLOCK);
+  const size_t base = (size_t)mat * rows * K;
+  int fit[2];
+  bool nz[2], valid[2];
+  int top = INT_MIN;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = threadIdx.x * 2 + u;               // 512 sub-blocks: 128 rows x 4
+    const int r = r0 + (i >> 2), b = b0 + (i & 3);
+    valid[u] = r < rows && b < kb;
+    float m = 0.0f;
+    if (valid[u]) {
+      const uint4* src = reinterpret_cast<const uint4*>(w + base + (size_t)r * K + (size_t)b * MX_BLOCK);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = __ldg(src + q);
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(ww[j] << 16)), fabsf(__uint_as_float(ww[j] & 0xFFFF0000u))));
+      }
+    }
+    nz[u] = m > 0.0f;
+    int x = 0;
+    const float mant = frexpf(nz[u] ? m : 1.0f, &x);
+    fit[u] = max((mant <= 0.75f) ? x - 3 : x - 2, MX_MIN_EXP);
+    if (valid[u] && nz[u]) top = max(top, fit[u]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) top = max(top, __shfl_xor_sync(0xffffffffu, top, o));
+  if ((threadIdx.x & 31) == 0) s_top[threadIdx.x >> 5] = top;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = MX_MIN_EXP;  // an all-zero tile: as if its largest exponent were the minimum
+    for (int i = 0; i < 8; ++i) t = max(t, s_top[i]);
+    s_tile_top = t;
+  }
+  __syncthreads();
+  const int floor_e = s_tile_top - MX_HEADROOM;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (!valid[u]) continue;
+    const int i = threadIdx.x * 2 + u;
+    const int r = r0 + (i >> 2), b = b0 + (i & 3);
+    const int e = nz[u] ? max(fit[u], floor_e) : s_tile_top;
+    exps[((size_t)mat * rows + r) * kb + b] = (int8_t)e;
+    const uint4* src = reinterpret_cast<const uint4*>(w + base + (size_t)r * K + (size_t)b * MX_BLOCK);
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {            // 8 bf16 -> 8 codes -> one 32-bit word
+      const uint4 v = __ldg(src + q);
+      const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t bits = (j & 1) ? (ww[j >> 1] & 0xFFFF0000u) : (ww[j >> 1] << 16);
+        const float val = ldexpf(__uint_as_float(bits), -e);  // exact power-of-two scaling
+        const uint32_t idx = e2m1_index(fabsf(val));
+        const uint32_t code = idx | ((val < 0.0f && idx > 0) ? 8u : 0u);
+        word |= code << (4 * j);
+      }
+      out[q] = word;
+    }
+    *reinterpret_cast<uint4*>(codes + (base + (size_t)r * K + (size_t)b * MX_BLOCK) / 2) =
+        make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+__global__ void __launch_bounds__(256) mxfp4_to_fp8_kernel(const uint8_t* __restrict__ codes, const int8_t* __restrict__ exps,
+                                                           int rows, int K, uint8_t* __restrict__ q8,
+                                                           int8_t* __restrict__ e8) {
+  __shared__ int s_top[8];
+  __shared__ int s_E;
+  const int kb = K / MX_BLOCK;
+  const int nr = (rows + QTILE - 1) / QTILE, nk = (K + QTILE - 1) / QTILE;
+  const int mat = blockIdx.z, r0 = blockIdx.y * QTILE, b0 = blockIdx.x * (QTILE / MX_BLOCK);
+  const size_t base = (size_t)mat * rows * K;
+  int se[2];
+  bool valid[2];
+  int top = INT_MIN;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = threadIdx.x * 2 + u;
+    const int r = r0 + (i >> 2), b = b0 + (i & 3);
+    valid[u] = r < rows && b < kb;
+    se[u] = valid[u] ? (int)exps[((size_t)mat * rows + r) * kb + b] : INT_MIN;
+    top = max(top, se[u]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) top = max(top, __shfl_xor_sync(0xffffffffu, top, o));
+  if ((threadIdx.x & 31) == 0) s_top[threadIdx.x >> 5] = top;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = INT_MIN;
+    for (int i = 0; i < 8; ++i) t = max(t, s_top[i]);
+    s_E = t - 6;
+    e8[((size_t)mat * nr + blockIdx.y) * nk + blockIdx.x] = (int8_t)(t - 6);
+  }
+  __syncthreads();
+  const int E = s_E;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    if (!valid[u]) continue;
+    const int i = threadIdx.x * 2 + u;
+    const int r = r0 + (i >> 2), b = b0 + (i & 3);
+    const size_t off = base + (size_t)r * K + (size_t)b * MX_BLOCK;
+    const uint4 c = *reinterpret_cast<const uint4*>(codes + off / 2);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    const int t = se[u] - E;  // in [-8, 6] for exponents from moe_quantize_mxfp4
+    uint32_t out[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t code = (cw[q] >> (4 * (4 * h + j))) & 0xFu;
+          const float mag = ldexpf(e2m1_magnitude(code & 7u), t);
+          uint32_t b8 = (uint32_t)__nv_cvt_float_to_fp8((code & 8u) ? -mag : mag, __NV_SATFINITE, __NV_E4M3);
+          if ((b8 & 0x7Fu) == 0) b8 = 0;
+          word |= b8 << (8 * j);
+        }
+        out[2 * q + h] = word;
+      }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(q8 + off);
+    dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
+cudaError_t launch_quantize_mxfp4(const void* w, int n_mats, int rows, int K, uint8_t* codes, int8_t* exps,
+                                  cudaStream_t s) {
+  const dim3 grid((K + QTILE - 1) / QTILE, (rows + QTILE - 1) / QTILE, n_mats);
+  quantize_mxfp4_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w), rows, K, codes, exps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int n_mats, int rows, int K, uint8_t* q8,
+                                int8_t* e8, cudaStream_t s) {
+  const dim3 grid((K + QTILE - 1) / QTILE, (rows + QTILE - 1) / QTILE, n_mats);
+  mxfp4_to_fp8_kernel<<<grid, 256, 0, s>>>(codes, exps, rows, K, q8, e8);
+  return cudaGetLastError();
+}
+
 }  // namespace moe
 
 extern "C" moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int32_t K, uint8_t* codes,
@@ -201,6 +384,32 @@ extern "C" moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_
   if ((int64_t)n_mats * rows * K >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(w) & 1u) != 0) return MOE_ERR_ALIGNMENT;
   if (moe::launch_quantize_fp8(w, n_mats, rows, K, codes, exps, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_quantize_mxfp4(const moe_bf16* w, int32_t n_mats, int32_t rows, int32_t K, uint8_t* codes,
+                                         int8_t* exps, moe_stream_t stream) {
+  if (n_mats <= 0 || rows <= 0 || K <= 0 || n_mats > 65535 || K % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (w == nullptr || codes == nullptr || exps == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)n_mats * rows * K >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(w) & 15u) != 0 || (reinterpret_cast<uintptr_t>(codes) & 15u) != 0)
+    return MOE_ERR_ALIGNMENT;
+  if (moe::launch_quantize_mxfp4(w, n_mats, rows, K, codes, exps, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int32_t n_mats, int32_t rows,
+                                       int32_t K, uint8_t* q8, int8_t* e8, moe_stream_t stream) {
+  if (n_mats <= 0 || rows <= 0 || K <= 0 || n_mats > 65535 || K % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (codes == nullptr || exps == nullptr || q8 == nullptr || e8 == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)n_mats * rows * K >= (1ll << 40)) return MOE_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(codes) & 15u) != 0 || (reinterpret_cast<uintptr_t>(q8) & 15u) != 0)
+    return MOE_ERR_ALIGNMENT;
+  if (moe::launch_mxfp4_to_fp8(codes, exps, n_mats, rows, K, q8, e8, reinterpret_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;

@@ -1,0 +1,137 @@
+"""MXFP4 (E2M1, 1 x 32 sub-block scales) expert weights on the GPU, through the C ABI, against
+the oracle: the quantiser's codes and sub-block exponents bit for bit (partial tiles, zero
+sub-blocks and tiles, sub-block ranges wide enough to trigger the headroom raise), the lossless
+conversion to FP8 tiles bit for bit on the oracle's own codes, and the layer run on the
+converted weights against the oracle's layer on its own MXFP4 round trip of the weights."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8_weights as F8
+from oracle import mxfp4_weights as M
+from routed_expert_swiglu_gb300 import binding, inputs, workloads as W
+
+from parity_util import check_output, check_routing, oracle_route, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routed_expert_swiglu_gb300 import build
+    build.build()
+    binding.load()
+
+
+def pack(codes):
+    """Two 4-bit codes per byte, the even column in the low nibble (the library's layout)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def weights(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    w = torch.randn(shape, generator=g)
+    # per-sub-block magnitudes over ~24 binades, so that some tiles span more than the headroom
+    blk = torch.randint(-18, 6, shape[:-1] + (shape[-1] // 32, 1), generator=g).float()
+    return (w * torch.exp2(blk).repeat_interleave(32, dim=-1).reshape(shape)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("shape", [(3, 256, 384), (2, 200, 192), (1, 64, 4096), (4, 128, 96)])
+def test_quantiser_bit_exact(shape):
+    w = weights(shape, sum(shape))
+    if shape[1] > 128 and shape[2] > 128:
+        w[0, 128:, :128] = 0                                     # an all-zero tile
+    w[-1, 3, 32:64] = 0                                          # an all-zero sub-block
+    codes, exps = binding.quantize_mxfp4(w.to(DEV))
+    torch.cuda.synchronize()
+    rc, re = M.quantize_mxfp4(w.double().numpy())
+    assert np.array_equal(exps.cpu().numpy().astype(np.int64), re)
+    assert np.array_equal(codes.cpu().numpy(), pack(rc))
+    assert (re.max() - re.min()) > M.HEADROOM                     # the raise was exercised
+
+
+@pytest.mark.parametrize("shape", [(3, 256, 384), (2, 200, 192)])
+def test_conversion_bit_exact(shape):
+    rc, re = M.quantize_mxfp4(weights(shape, 7 + sum(shape)).double().numpy())
+    want_c, want_e = M.mxfp4_to_fp8(rc, re)
+    q8, e8 = binding.mxfp4_to_fp8(torch.from_numpy(pack(rc)).to(DEV),
+                                  torch.from_numpy(re.astype(np.int8)).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(e8.cpu().numpy().astype(np.int64), want_e)
+    assert np.array_equal(q8.cpu().numpy(), want_c)
+    # and the FP8 form holds exactly the MXFP4 values
+    assert np.array_equal(F8.dequantize_fp8_tiles(q8.cpu().numpy(), e8.cpu().numpy()), M.dequantize_mxfp4(rc, re))
+
+
+class OracleMxfp4Fetcher:
+    """Expert weights as the oracle's own MXFP4 round trip of the bf16 weights (lazily)."""
+
+    def __init__(self, inp):
+        self.inp = inp
+        self.cache = {}
+
+    @staticmethod
+    def _rt(w):
+        return M.dequantize_mxfp4(*M.quantize_mxfp4(to64(w)))
+
+    def __call__(self, e):
+        if e not in self.cache:
+            self.cache[e] = (self._rt(self.inp.w13[e]), self._rt(self.inp.w2[e]))
+        return self.cache[e]
+
+    def shared(self):
+        if self.inp.w13_sh is None:
+            return None
+        return self._rt(self.inp.w13_sh), self._rt(self.inp.w2_sh)
+
+
+CASES = [
+    W.TOY,                                                                  # widening FP8 kernels
+    W.Workload("mid_T64", T=64, d=512, d_ff=256, E=16, k=4, n_shared=1, score=W.SCORE_SIGMOID, use_bias=True),
+    W.Workload("ragged_T150", T=150, d=320, d_ff=192, E=12, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
+    W.Workload("wide_T64", T=64, d=512, d_ff=256, E=64, k=2, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
+               use_bias=True),
+]
+
+
+def run_layer(w, seed, sample=None):
+    inp = inputs.make_layer_inputs(w, seed=seed, device=DEV)
+    layer = binding.MoELayer(w, inp)
+    q8 = layer.mxfp4_to_fp8(layer.quantize_mxfp4())
+    y = layer.forward_fp8(inp.x, q8, inp.token_ids)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    tok = np.nonzero(same)[0]
+    if sample is not None:
+        tok = np.sort(np.random.default_rng(99).choice(tok, size=min(sample, tok.size), replace=False))
+    fetch = OracleMxfp4Fetcher(inp)
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
+    print(f"{w.name} (mxfp4 weights): max elementwise {e:.2e}, normwise {n:.2e}")
+    layer.close()
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_mxfp4_layer_vs_oracle(w):
+    run_layer(w, seed=31)
+
+
+@pytest.mark.slow
+def test_mxfp4_full_size_layer():
+    """The V4-Flash T=64 layer at full size, output on two sampled tokens."""
+    run_layer(W.V4FLASH_T64, seed=0, sample=2)
