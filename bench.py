@@ -218,6 +218,47 @@ def measure_fp8(layer, inp, w, steps, warmup, active, bf16_ms, hbm_peak, world):
             "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, stage)}}
 
 
+def measure_mxfp4(layer, inp, w, steps, warmup, fp8_ms, bf16_ms, world):
+    """The same layer with MXFP4 (E2M1, 1 x 32 sub-block scales) expert weights: quantised once,
+    converted losslessly to the FP8 tile form once per weight set (timed: conversion_ms), then
+    the forward on the converted tiles timed like the FP8 forward."""
+    from routed_expert_swiglu_gb300 import binding
+    q4 = layer.quantize_mxfp4()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    layer.mxfp4_to_fp8(q4)  # warm-up
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    q8 = layer.mxfp4_to_fp8(q4)
+    end.record(stream)
+    torch.cuda.synchronize()
+    conv_ms = start.elapsed_time(end)
+    fwd = lambda x, tok, out: layer.forward_fp8(x, q8, tok, out=out)  # noqa: E731
+    ms, _ = time_layer(layer, inp.x, inp.token_ids, steps, warmup, stream, fwd=fwd, with_stages=False)
+    st = layer.check_status()
+    if st != 0:
+        raise RuntimeError(f"device status {binding.STATUS_NAMES.get(st, st)} on {w.name} (mxfp4 weights)")
+    ms = max_over_ranks(ms, world) / steps
+    at_rest = sum(c.numel() + e.numel() for c, e in q4.values())
+    res = {"weights": "mxfp4 e2m1, one power-of-two scale per 1x32 sub-block", "bytes_at_rest": int(at_rest),
+           "conversion_ms": round(max_over_ranks(conv_ms, world), 4),
+           "converted": {"ms_per_step": round(ms, 4), "tokens_per_s": round(world * w.T / (ms / 1e3), 1),
+                         "what": "moe_forward_fp8 on the losslessly converted fp8 tiles"}}
+    if w.d % 128 == 0 and w.d_ff % 128 == 0:
+        qn = layer.mxfp4_native(q4)
+        fwd = lambda x, tok, out: layer.forward_mxfp4(x, qn, tok, out=out)  # noqa: E731
+        nms, nstage = time_layer(layer, inp.x, inp.token_ids, steps, warmup, stream, fwd=fwd)
+        st = layer.check_status()
+        if st != 0:
+            raise RuntimeError(f"device status {binding.STATUS_NAMES.get(st, st)} on {w.name} (native mxfp4)")
+        nms = max_over_ranks(nms, world) / steps
+        res["native"] = {"ms_per_step": round(nms, 4), "tokens_per_s": round(world * w.T / (nms / 1e3), 1),
+                         "speedup_vs_fp8": round(fp8_ms / nms, 3), "speedup_vs_bf16": round(bf16_ms / nms, 3),
+                         "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, nstage)},
+                         "what": "moe_forward_mxfp4: 4-bit codes streamed, turned into e4m3 on the chip"}
+    return res
+
+
 def measure_e2e(layer, inp, w, steps, warmup, world):
     """Same metric through moe_forward_host: pinned host x in, pinned host y out, copies timed."""
     from routed_expert_swiglu_gb300 import binding
@@ -338,6 +379,8 @@ def run_ours(args, world, rank, local):
         if not args.no_fp8:
             decode["fp8_weights"] = measure_fp8(dl, dinp, wd, max(args.steps, 10), args.warmup, dactive, dms,
                                                 hbm_peak, world)
+            decode["mxfp4_weights"] = measure_mxfp4(dl, dinp, wd, max(args.steps, 10), args.warmup,
+                                                    decode["fp8_weights"]["ms_per_step"], dms, world)
         dl.close()
         del dl, dinp
         torch.cuda.empty_cache()
@@ -483,7 +526,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=240,
                     help="tokens per step of the reference arm (the oracle; about 3 s per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-weight decode measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8- and MXFP4-weight decode measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

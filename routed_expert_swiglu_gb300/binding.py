@@ -28,7 +28,8 @@ EXPORTED = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_r
             "moe_forward", "moe_forward_routed", "moe_forward_host", "moe_check_status",
             "moe_workspace_views", "moe_forward_stage_count", "moe_plan_set_events",
             "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc",
-            "moe_update_bias", "moe_quantize_fp8", "moe_forward_fp8", "moe_quantize_mxfp4", "moe_mxfp4_to_fp8")
+            "moe_update_bias", "moe_quantize_fp8", "moe_forward_fp8", "moe_quantize_mxfp4", "moe_mxfp4_to_fp8",
+            "moe_forward_mxfp4")
 
 
 class MoEError(RuntimeError):
@@ -82,6 +83,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward_fp8": ([P, I, V, V, V, V, V, V, V, V, V, V, V, V, V, V, S, V], I),
         "moe_quantize_mxfp4": ([V, I, I, I, V, V, V], I),
         "moe_mxfp4_to_fp8": ([V, V, I, I, I, V, V, V], I),
+        "moe_forward_mxfp4": ([P, I] + [V] * 18 + [S, V], I),
     }
     for name, (argt, rest) in sig.items():
         fn = getattr(lib, name)
@@ -209,6 +211,31 @@ def mxfp4_to_fp8(codes, exps, stream=None):
     return q8, e8
 
 
+def mxfp4_tile_exps(codes, exps, stream=None):
+    """The 128 x 128 tile exponents of the FP8 form of MXFP4 weights (moe_mxfp4_to_fp8 without
+    the codes): what moe_forward_mxfp4 takes beside the codes and sub-block exponents."""
+    rows, K = codes.shape[-2], codes.shape[-1] * 2
+    n = 1
+    for v in codes.shape[:-2]:
+        n *= v
+    e8 = torch.empty(tuple(codes.shape[:-2]) + (-(-rows // 128), -(-K // 128)), dtype=torch.int8,
+                     device=codes.device)
+    _check(load().moe_mxfp4_to_fp8(_ptr(codes), _ptr(exps), n, rows, K, None, _ptr(e8), _stream(stream)),
+           "moe_mxfp4_to_fp8")
+    return e8
+
+
+def moe_forward_mxfp4(plan, T, x, token_ids, w_r, bias, w13, w2, w13_sh, w2_sh, out, ws, stream=None):
+    """w13, w2, w13_sh, w2_sh: (codes, sub-block exponents, tile exponents) triples (shared: None
+    without a shared expert)."""
+    def trip(q):
+        return (None, None, None) if q is None else tuple(_ptr(t) for t in q)
+    args = [*trip(w13), *trip(w2), *trip(w13_sh), *trip(w2_sh)]
+    _check(load().moe_forward_mxfp4(plan, T, _ptr(x), _ptr(token_ids), _ptr(w_r), _ptr(bias), *args, _ptr(out),
+                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_forward_mxfp4")
+
+
 def moe_forward_fp8(plan, T, x, token_ids, w_r, bias, q13, e13, q2, e2, q13_sh, e13_sh, q2_sh, e2_sh, out, ws,
                     stream=None):
     _check(load().moe_forward_fp8(plan, T, _ptr(x), _ptr(token_ids), _ptr(w_r), _ptr(bias), _ptr(q13), _ptr(e13),
@@ -325,6 +352,21 @@ class MoELayer:
     def mxfp4_to_fp8(q4, stream=None):
         """The FP8 form (for forward_fp8) of MXFP4 weights from quantize_mxfp4."""
         return {k: mxfp4_to_fp8(c, e, stream) for k, (c, e) in q4.items()}
+
+    @staticmethod
+    def mxfp4_native(q4, stream=None):
+        """(codes, sub-block exponents, tile exponents) per weight set, for forward_mxfp4."""
+        return {k: (c, e, mxfp4_tile_exps(c, e, stream)) for k, (c, e) in q4.items()}
+
+    def forward_mxfp4(self, x, q, token_ids=None, out=None, stream=None):
+        """The layer on native MXFP4 expert weights q (from mxfp4_native)."""
+        T = x.shape[0]
+        inp = self.inputs
+        if out is None:
+            out = torch.empty((T, self.w.d), dtype=torch.bfloat16, device=self.device)
+        moe_forward_mxfp4(self.plan, T, x, token_ids, inp.w_r, inp.bias, q["w13"], q["w2"], q.get("w13_sh"),
+                          q.get("w2_sh"), out, self.ws, stream)
+        return out
 
     def forward_fp8(self, x, q, token_ids=None, out=None, stream=None):
         """The layer with FP8 expert weights q (from quantize_fp8)."""

@@ -684,6 +684,425 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ============================================================================ MXFP4 variant
+// Native MXFP4 weights (E2M1 codes, one power-of-two scale 2^s per 1 x 32 sub-block; "DeepSeek-V4
+// MoE", section "FP4 QAT 怎么做到反量化无损": FP4 sub-blocks losslessly dequantised to FP8 E4M3
+// tiles of 128 x 128 for the computation, native FP4 weights at inference).  TMA streams the
+// packed codes (two per byte, 64-byte rows per 128-wide K tile, 64-byte swizzle) with the token
+// rows' E4M3 pieces; groups of four converter warps, one per TMEM lane quadrant, take turns by
+// stage and turn the weight rows into E4M3 bytes of q * 2^(s - E), E the tile's exponent (its
+// largest sub-block exponent - 6, given with the weights), exact since s - E lies in [-8, 6], and
+// store them into a ring of A tiles in Tensor Memory; the 8-bit MMA reads A from there and B (the
+// pieces) from shared memory, and the epilogue is that of the FP8 MMA kernel with 2^E per tile.
+// A code becomes its byte with two byte permutes per four codes: one picks the magnitude from an
+// eight-entry table of E4M3 bytes for the sub-block's s - E, one gathers the bytes holding the
+// codes' sign bits (about 1.5 integer operations per code in all).  Decode-sized token tiles (16
+// rows).  Measured, the integer pipe bounds it near the FP8 kernel's speed: half the weight bytes
+// streamed, twice the codes converted per byte.
+
+// D (+)= A[tmem] * B[smem]^T on 8-bit operands: A's 128 rows in the 128 lanes, K = 32 codes
+// packed four per 32-bit column (8 columns, the lowest k in the lowest byte).
+__device__ __forceinline__ void tc_mma_f8_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Store 8 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// Eight packed E2M1 codes (one word, code i in bits 4i..4i+3) -> eight E4M3 bytes (two words,
+// low word first) with the magnitude table lut (bytes 0..7 of lut_lo, lut_hi).
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
+  const uint32_t m_lo = __byte_perm(lut_lo, lut_hi, w & 0x7777u);          // magnitudes of codes 0..3
+  const uint32_t m_hi = __byte_perm(lut_lo, lut_hi, (w >> 16) & 0x7777u);  // codes 4..7
+  // byte 0 of (w << 4) has code 0's sign in bit 7, byte 0 of w code 1's, and so on
+  const uint32_t w4 = w << 4;
+  const uint32_t s_lo = __byte_perm(w4, w, 0x5140u);
+  const uint32_t s_hi = __byte_perm(w4, w, 0x7362u);
+  return make_uint2(m_lo | (s_lo & 0x80808080u), m_hi | (s_hi & 0x80808080u));
+}
+
+// The parameter block plus the MXFP4 sub-block exponents [mats, rows, K/32] (int8) of the routed
+// and the shared weights.
+struct Fp4Params : GemmParams {
+  const int8_t* a_sub;
+  const int8_t* a_sh_sub;
+};
+
+// Converter groups of the MXFP4 kernel (four warps each).  The conversion is bound by the
+// integer pipe: 2, 3 and 4 groups measured alike (V4-Flash T=64: 0.827 / 0.830 / 0.874 ms); 3
+// fit without register spills.
+#ifndef MOE_F4_CVT_GROUPS
+#define MOE_F4_CVT_GROUPS 3
+#endif
+
+template <int EPI, int MBLK>
+struct F4Shape {
+  static constexpr int TN = 16;
+  static constexpr int BLOCK_K = 128;                   // codes per stage (one FP8 tile of K)
+  static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
+  static constexpr int RAW_SLAB = BLOCK_M * BLOCK_K / 2;  // 128 rows x 64 bytes of codes
+  static constexpr int RAW_A = NUM_A * RAW_SLAB;
+  static constexpr int PIECES = (EPI == EPI_SWIGLU) ? 2 : 4;
+  static constexpr int B_PIECE = TN * BLOCK_K;          // 16 token rows x 128 E4M3 codes
+  static constexpr int RAW_STAGE = RAW_A + PIECES * B_PIECE;
+  static constexpr int A_COLS = BLOCK_K / 4;            // TMEM columns of one converted slab
+  static constexpr int CSTAGES = MOE_F4_CVT_GROUPS;     // converted stages in Tensor Memory
+  static constexpr int CVT_GROUPS = CSTAGES;            // group g converts every CSTAGES-th stage
+  static constexpr int NUM_CVT_WARPS = 4 * CVT_GROUPS;
+  static constexpr int THREADS = (2 + NUM_EPI_WARPS + NUM_CVT_WARPS) * 32;
+  static constexpr int A_RING_COLS = CSTAGES * NUM_A * A_COLS;
+  static constexpr int SLOT_COLS = NUM_A * PIECES * TN;
+  static constexpr int SLOTS = ((512 - A_RING_COLS) / SLOT_COLS) > 8 ? 8 : ((512 - A_RING_COLS) / SLOT_COLS);
+  static constexpr int A_COL0 = SLOTS * SLOT_COLS;      // first column of the A ring
+  static constexpr int RSTAGES_FIT = (SMEM_LIMIT - 1024 - 512) / RAW_STAGE;
+  static constexpr int RSTAGES = RSTAGES_FIT > 8 ? 8 : RSTAGES_FIT;
+  static constexpr int SMEM_BYTES = RSTAGES * RAW_STAGE + 1024 + 512;
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : BLOCK_M * MBLK;
+  static_assert(SLOTS >= 2 && A_COL0 + A_RING_COLS <= 512, "TMEM: partial slots + A ring");
+  static_assert(RSTAGES >= 2, "pipeline needs two raw stages");
+  static_assert(RAW_SLAB % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled tiles on 1024 B");
+  static_assert((2 * RSTAGES + 2 * CSTAGES + 2 * SLOTS) * 8 + 8 <= 512, "barrier area");
+  static_assert(EPI == EPI_F32 || MBLK == 1, "SwiGLU variant");
+  static_assert(PIECES == 2 || PIECES == 4, "pieces are summed in pairs");
+};
+
+template <int EPI, int MBLK>
+__global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
+    fp4mma_gemm_kernel(const __grid_constant__ GemmMaps maps, const Fp4Params p) {
+  using S = F4Shape<EPI, MBLK>;
+  constexpr int TN = S::TN;
+  constexpr int RST = S::RSTAGES;
+  constexpr int CST = S::CSTAGES;
+  constexpr int SL = S::SLOTS;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint2 s_lut[15];  // E4M3 bytes of the eight E2M1 magnitudes times 2^t, t = -8 .. 6
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + RST * S::RAW_STAGE);
+  // bars: full[RST], empty[RST], cfull[CST], cempty[CST], slot_full[SL], slot_empty[SL]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RST + 2 * CST + 2 * SL);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (RST + s); };
+  auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * RST + c); };
+  auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * RST + CST + c); };
+  auto sfull_bar = [&](int c) { return bar0 + 8u * (2 * RST + 2 * CST + c); };
+  auto sempty_bar = [&](int c) { return bar0 + 8u * (2 * RST + 2 * CST + SL + c); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RST; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int c = 0; c < CST; ++c) {
+      mbar_init(cfull_bar(c), 4 * 32);  // the four warps of the slot's converter group
+      mbar_init(cempty_bar(c), 1);
+    }
+    for (int c = 0; c < SL; ++c) {
+      mbar_init(sfull_bar(c), 1);
+      mbar_init(sempty_bar(c), NUM_EPI_WARPS);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x < 15 * 8) {  // the magnitude tables, one byte per thread
+    const int t = threadIdx.x / 8 - 8, idx = threadIdx.x % 8;
+    const float mag = idx < 2 ? 0.5f * (float)idx : ldexpf((idx & 1) ? 1.5f : 1.0f, (idx >> 1) - 1);
+    reinterpret_cast<uint8_t*>(s_lut)[threadIdx.x] =
+        idx == 0 ? 0 : (uint8_t)__nv_cvt_float_to_fp8(ldexpf(mag, t), __NV_SATFINITE, __NV_E4M3);
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a_sh);
+    tma_prefetch_desc(&maps.b[0]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int row_tiles = p.grp != nullptr ? __ldg(&p.grp[p.n_groups_total].z)
+                                         : (p.dense_rows + p.sched_tn - 1) / p.sched_tn;
+  const int total_tiles = row_tiles * p.num_mblocks * (p.sched_tn / TN);
+  const int KB = p.K / S::BLOCK_K;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
+        const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * S::FEATS;
+        const uint32_t bytes = S::RAW_A + S::PIECES * t.n_mma * S::BLOCK_K;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, bytes);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_3d(sr, ta, fb, kb * (S::BLOCK_K / 2), t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);
+          } else {
+            tma_load_2d(sr, ta, fb, kb * (S::BLOCK_K / 2), a_row);
+          }
+#pragma unroll
+          for (int pc = 0; pc < S::PIECES; ++pc)
+            tma_load_3d(sr + S::RAW_A + pc * t.n_mma * S::BLOCK_K, &maps.b[0], fb, kb * S::BLOCK_K, pc, t.b_row);
+          if (++stage == RST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, cs = 0, slot = 0;
+      uint32_t phase = 0, cphase = 0, sphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const uint32_t idesc = idesc_e4m3_f32(S::PIECES * t.n_mma);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+              !mbar_wait(cfull_bar(cs), cphase, abort_flag, p.err) ||
+              !mbar_wait(sempty_bar(slot), sphase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const uint32_t d0 = tmem_base + slot * S::SLOT_COLS;
+          const uint32_t ta = tmem_base + S::A_COL0 + cs * (S::NUM_A * S::A_COLS);
+#pragma unroll
+          for (int kk = 0; kk < S::BLOCK_K / 32; ++kk) {
+            const uint64_t db = smem_desc_sw(sr + S::RAW_A, 128) + 2 * kk;
+#pragma unroll
+            for (int a = 0; a < S::NUM_A; ++a)
+              tc_mma_f8_ta(d0 + a * S::PIECES * TN, ta + a * S::A_COLS + kk * 8, db, idesc, kk ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+          tc_commit(cempty_bar(cs));
+          tc_commit(sfull_bar(slot));
+          if (++stage == RST) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++cs == CST) {
+            cs = 0;
+            cphase ^= 1u;
+          }
+          if (++slot == SL) {
+            slot = 0;
+            sphase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + NUM_EPI_WARPS) {
+    // ------------------------------------------------------------------ epilogue
+    // Warps of half 0 hold the 16 token columns (half 1 has none with 16-row tiles but keeps
+    // the slot protocol).
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    int slot = 0;
+    uint32_t sphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      const bool mine = half == 0;
+      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
+      int erow[S::NUM_A];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        const int base = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M : t.mb * S::FEATS + a * BLOCK_M;
+        erow[a] = min(base >> 7, p.exp_nr - 1) * p.exp_nk;
+      }
+      float acc[S::NUM_A][16];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[a][j] = 0.0f;
+      int e_cur[S::NUM_A];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) e_cur[a] = __ldg(ex + erow[a]);
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16);
+      for (int kb = 0; kb < KB; ++kb) {
+        int e_nxt[S::NUM_A];
+#pragma unroll
+        for (int a = 0; a < S::NUM_A; ++a) e_nxt[a] = (kb + 1 < KB) ? __ldg(ex + erow[a] + kb + 1) : 0;
+        if (!mbar_wait(sfull_bar(slot), sphase, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (mine) {
+          const uint32_t ts = tq + slot * S::SLOT_COLS;
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) {
+            const float sc = __int_as_float((e_cur[a] + 127) << 23);  // 2^E, E in [-126, 121]
+#pragma unroll
+            for (int pc = 0; pc < S::PIECES; ++pc) {  // one piece's 16 columns per wait
+              const float scp = sc * (pc == 0 ? 1.0f : pc == 1 ? 0.0625f : pc == 2 ? 0.00390625f : 0.000244140625f);
+              uint32_t r0[16];
+              tmem_ld16(ts + a * S::PIECES * TN + pc * t.n_mma, r0);
+              tmem_ld_wait();
+              reg_fence16(r0);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[a][j] = fmaf(__uint_as_float(r0[j]), scp, acc[a][j]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty_bar(slot));
+#pragma unroll
+        for (int a = 0; a < S::NUM_A; ++a) e_cur[a] = e_nxt[a];
+        if (++slot == SL) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+      }
+      if (!ok || !mine) continue;
+      const int cols = min(16, t.rows);
+      const bool rvalid = lane < t.rows;
+      const int er = rvalid ? __ldg(p.b_exp + t.b_row + lane) : 0;
+      float cs_l = __int_as_float((127 + er) << 23);  // 2^e_r, e_r in [-126, 120]
+      if (EPI == EPI_F32 && p.row_scale != nullptr && !t.shared && rvalid) cs_l *= __ldg(p.row_scale + t.out_row + lane);
+      float* out = static_cast<float*>(p.out) + (size_t)t.out_row * p.out_ld;
+      if (EPI == EPI_SWIGLU) {
+        const int feat = t.mb * BLOCK_M + quad * 32 + lane;
+        const bool fvalid = feat < p.out_features;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float cs = __shfl_sync(0xffffffffu, cs_l, j);
+          if (j < cols && fvalid) {
+            const float g = acc[0][j] * cs, u = acc[1][j] * cs;
+            out[(size_t)j * p.out_ld + feat] = __fdividef(g, 1.0f + __expf(-g)) * u;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float cs = __shfl_sync(0xffffffffu, cs_l, j);
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) {
+            const int feat = t.mb * S::FEATS + a * BLOCK_M + quad * 32 + lane;
+            if (j < cols && feat < p.out_features) out[(size_t)j * p.out_ld + feat] = acc[a][j] * cs;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ E2M1 -> E4M3 converters
+    // Group g converts the stages n with n % CVT_GROUPS == g into A slot g; warp w owns TMEM lane
+    // quadrant w % 4, i.e. weight rows r = 32 (w % 4) + lane of every slab: the thread reads the
+    // row's 64 code bytes (four 16-byte chunks, chunk c of row r at c ^ ((r >> 1) & 3), the
+    // 64-byte swizzle TMA wrote), i.e. four sub-blocks of 32 codes, and stores 32 columns of
+    // E4M3 bytes per slab.
+    const int quad = warp & 3;
+    const int group = (warp - 2 - NUM_EPI_WARPS) >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t ta = tmem_base + (uint32_t(quad * 32) << 16) + S::A_COL0 + group * (S::NUM_A * S::A_COLS);
+    const int kb32 = p.K / 32;  // sub-blocks per weight row
+    uint32_t n = 0, mine = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
+      const int8_t* sub = t.shared ? p.a_sh_sub : p.a_sub + (size_t)t.g * p.a_rows_per_group * kb32;
+      int srow[S::NUM_A], erow[S::NUM_A];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        const int base = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M : t.mb * S::FEATS + a * BLOCK_M;
+        const int row = min(base + r, p.a_rows_per_group - 1);  // rows past the matrix: any valid row
+        srow[a] = row * kb32;
+        erow[a] = min(base >> 7, p.exp_nr - 1) * p.exp_nk;
+      }
+      for (int kb = 0; kb < KB; ++kb, ++n) {
+        if ((int)(n % S::CVT_GROUPS) != group) continue;
+        // this stage's sub-block exponents (four bytes per slab) and tile exponents, loaded
+        // before the waits
+        uint32_t s4[S::NUM_A];
+        int E[S::NUM_A];
+#pragma unroll
+        for (int a = 0; a < S::NUM_A; ++a) {
+          s4[a] = __ldg(reinterpret_cast<const uint32_t*>(sub + srow[a] + kb * 4));
+          E[a] = __ldg(ex + erow[a] + kb);
+        }
+        const int stage = (int)(n % RST);
+        const uint32_t phase = (n / RST) & 1u;
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
+            !mbar_wait(cempty_bar(group), (mine & 1u) ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        ++mine;
+        tc_fence_after();
+        const uint8_t* src = raw + stage * S::RAW_STAGE;
+#pragma unroll
+        for (int a = 0; a < S::NUM_A; ++a) {
+          const uint8_t* row = src + a * S::RAW_SLAB + r * 64;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {  // sub-block b: 32 codes -> 8 columns
+            int tix = (int)(int8_t)(s4[a] >> (8 * b)) - E[a] + 8;  // s - E + 8, in [0, 14]
+            tix = min(max(tix, 0), 14);
+            const uint2 lut = s_lut[tix];
+            const uint4 q = *reinterpret_cast<const uint4*>(row + ((b ^ ((r >> 1) & 3)) << 4));
+            const uint2 v0 = e2m1x8_to_e4m3x8(q.x, lut.x, lut.y);
+            const uint2 v1 = e2m1x8_to_e4m3x8(q.y, lut.x, lut.y);
+            const uint2 v2 = e2m1x8_to_e4m3x8(q.z, lut.x, lut.y);
+            const uint2 v3 = e2m1x8_to_e4m3x8(q.w, lut.x, lut.y);
+            const uint32_t o[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
+            tmem_st8(ta + a * S::A_COLS + b * 8, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(cfull_bar(group));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
 // ----------------------------------------------------------------------------- host side
 
 // E4M3 weight codes: 2-D uint8 [rows, cols] with boxes of box_k codes x box_rows rows, and the
@@ -812,7 +1231,55 @@ static cudaError_t launch_fp8mma_variant(const GemmLaunch& L, GemmParams p, cuda
   return cudaGetLastError();
 }
 
+template <int EPI, int MBLK>
+static cudaError_t launch_fp4mma_variant(const GemmLaunch& L, GemmParams base, cudaStream_t s) {
+  using Sh = F4Shape<EPI, MBLK>;
+  static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
+  if (base.sched_tn != Sh::TN || L.K % Sh::BLOCK_K != 0 || base.ksplit != 1) return cudaErrorInvalidValue;
+  if (L.a_exp == nullptr || L.a_sub == nullptr || L.b_exp == nullptr) return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr && (L.a_sh_exp == nullptr || L.a_sh_sub == nullptr)) return cudaErrorInvalidValue;
+  if (EPI == EPI_SWIGLU && L.a_up_offset % 128 != 0) return cudaErrorInvalidValue;  // slabs on scale tiles
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  const int64_t kc = L.K / 2;  // code bytes per weight row
+  if (EPI == EPI_SWIGLU) {
+    const int64_t f = L.a_up_offset;
+    if (!make_tmap_u8_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, kc, 64)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8_gateup(&m.a_sh, L.a_sh_ptr, 1, f, kc, 64))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_u8(&m.a, L.a_ptr, L.a_rows, kc, BLOCK_M * MBLK, 64)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, kc, BLOCK_M * MBLK, 64))
+      return cudaErrorInvalidValue;
+  }
+  if (L.a_sh_ptr == nullptr) m.a_sh = m.a;
+  if (!make_tmap_pieces(&m.b[0], L.b_ptr, L.b_rows, Sh::PIECES, L.K, Sh::TN)) return cudaErrorInvalidValue;
+  Fp4Params p;
+  static_cast<GemmParams&>(p) = base;
+  p.a_exp = L.a_exp;
+  p.a_sh_exp = L.a_sh_exp != nullptr ? L.a_sh_exp : L.a_exp;
+  p.exp_nr = (L.a_rows_per_group + 127) / 128;
+  p.exp_nk = (L.K + 127) / 128;
+  p.b_exp = L.b_exp;
+  p.a_sub = L.a_sub;
+  p.a_sh_sub = L.a_sh_sub != nullptr ? L.a_sh_sub : L.a_sub;
+  auto kern = fp4mma_gemm_kernel<EPI, MBLK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int grid = L.num_sms;
+  if (L.max_tiles < grid) grid = L.max_tiles;
+  if (grid < 1) grid = 1;
+  kern<<<grid, Sh::THREADS, Sh::SMEM_BYTES, s>>>(m, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fp8_gemm(const GemmLaunch& L, GemmParams p, int kernel_tn, cudaStream_t s) {
+  if (L.q8 == 3) {
+    // native MXFP4 codes, converted to E4M3 in Tensor Memory, 16-row token tiles
+    if (L.epi == EPI_SWIGLU && kernel_tn == 16) return launch_fp4mma_variant<EPI_SWIGLU, 1>(L, p, s);
+    if (L.epi != EPI_SWIGLU && kernel_tn == 16 && L.mblk == 2) return launch_fp4mma_variant<EPI_F32, 2>(L, p, s);
+    return cudaErrorInvalidValue;
+  }
   if (L.q8 == 2) {
     // FP8 weight codes straight into the MMA, E4M3-piece activations, 16-, 32- or 64-row token
     // tiles (the down projection's 64-row tiles on one 128-feature slab: its four pieces then

@@ -144,6 +144,10 @@ struct GemmLaunch {
   // 2 pieces for SwiGLU, 4 for fp32) with one power-of-two exponent per row (b_exp), shared rows
   // after the routed ones in the same buffers
   const int32_t* b_exp;
+  // q8 = 3: a_ptr / a_sh_ptr hold packed MXFP4 (E2M1) codes [rows, K/2], a_sub / a_sh_sub their
+  // 1 x 32 sub-block exponents [rows, K/32] and a_exp / a_sh_exp the 128 x 128 tile exponents
+  // (largest sub-block exponent - 6); B as for q8 = 2
+  const int8_t* a_sub; const int8_t* a_sh_sub;
   int K;
   int hilo;                // activation operand is the (hi, lo) pair: B rows hold 2*K values
   int pair;                // run on CTA pairs (2-SM MMA, 256 weight rows per tile)

@@ -47,10 +47,8 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.G = E + sh;
   L.TN = token_tile_for(T);
   L.nblk = ceil_div(L.N > 0 ? L.N : 1, PERMUTE_CHUNK);
-  // row tiles of the narrowest schedule a forward may build (the FP8-weight GEMMs' 16 to 64 rows)
-  const int tn_min = L.TN < 64 ? L.TN : 64;
-  const int tn_f8 = fp8_token_tile(T, k, E);
-  const int tn_sched = tn_f8 < tn_min ? tn_f8 : tn_min;
+  // row tiles of the narrowest schedule a forward may build
+  const int tn_sched = 16;  // the narrowest: the MXFP4 kernels' 16-row tiles
   L.max_rt = E + ceil_div(L.N, tn_sched) + sh * ceil_div(T, tn_sched) + 1;
   const size_t rows_h = (size_t)L.N + (size_t)sh * T;
   size_t off = 0;
@@ -249,10 +247,13 @@ bool fp8_mma_shapes(const moe_config& c) {
 }
 
 // Dispatch + grouped GEMMs + combine, from routing in the workspace or the caller's buffers.
-// FP8 (E4M3) expert weights: codes and 128 x 128 tile exponents (see moe_quantize_fp8).
+// FP8 (E4M3) expert weights: codes and 128 x 128 tile exponents (see moe_quantize_fp8).  With
+// the sub-block exponents s* set, MXFP4 weights instead: packed E2M1 codes, 1 x 32 sub-block
+// exponents and the tile exponents of their FP8 form (see moe_quantize_mxfp4).
 struct Fp8Weights {
   const uint8_t* q13; const int8_t* e13; const uint8_t* q2; const int8_t* e2;
   const uint8_t* q13_sh; const int8_t* e13_sh; const uint8_t* q2_sh; const int8_t* e2_sh;
+  const int8_t* s13; const int8_t* s2; const int8_t* s13_sh; const int8_t* s2_sh;
 };
 
 moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_t* ids, const float* w,
@@ -271,7 +272,9 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   pm.n_shared = sh;
   // FP8 weights: a schedule of the FP8 kernels' own row tiles (the widening kernels: 64 rows)
   const bool f8mma = q8 != nullptr && fp8_mma_shapes(c);
-  const int sched_tn = q8 == nullptr ? L.TN : (f8mma ? fp8_token_tile(T, c.top_k, E) : 64);
+  const bool f4 = q8 != nullptr && q8->s13 != nullptr;  // native MXFP4 (16-row token tiles)
+  if (f4 && !f8mma) return MOE_ERR_UNSUPPORTED;
+  const int sched_tn = q8 == nullptr ? L.TN : (f4 ? 16 : f8mma ? fp8_token_tile(T, c.top_k, E) : 64);
   pm.TN = sched_tn;
   pm.nblk = L.nblk;
   pm.blockhist = at<int32_t>(ws, L.blockhist);
@@ -338,7 +341,9 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
     g1.TN = sched_tn;
     g1.kernel_tn = sched_tn;
     if (f8mma) {
-      g1.q8 = 2;
+      g1.q8 = f4 ? 3 : 2;
+      g1.a_sub = f4 ? q8->s13 : nullptr;
+      g1.a_sh_sub = (f4 && sh) ? q8->s13_sh : nullptr;
       g1.b_ptr = at<void>(ws, L.xd);
       g1.b_rows = rows_h;  // routed rows, then the shared expert's
       g1.b_sh_ptr = nullptr;
@@ -395,7 +400,9 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
     g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
     g2.max_tiles = L.max_rt * g2.num_mblocks;
     if (f8mma) {
-      g2.q8 = 2;
+      g2.q8 = f4 ? 3 : 2;
+      g2.a_sub = f4 ? q8->s2 : nullptr;
+      g2.a_sh_sub = (f4 && sh) ? q8->s2_sh : nullptr;
       g2.hilo = 0;
       g2.b_exp = at<int32_t>(ws, L.hexp);
     }
@@ -569,7 +576,41 @@ moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const i
   int32_t* ids = at<int32_t>(ws, L.topk_ids);
   float* w = at<float>(ws, L.topk_w);
   MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
-  const Fp8Weights qw = {q13, e13, q2, e2, q13_sh, e13_sh, q2_sh, e2_sh};
+  const Fp8Weights qw = {q13, e13, q2, e2, q13_sh, e13_sh, q2_sh, e2_sh, nullptr, nullptr, nullptr, nullptr};
+  return run_experts(plan, T, x, ids, w, nullptr, nullptr, nullptr, nullptr, out, ws, sms, s, &qw);
+}
+
+moe_status moe_forward_mxfp4(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
+                             const moe_bf16* w_r, const float* bias, const uint8_t* c13, const int8_t* s13,
+                             const int8_t* t13, const uint8_t* c2, const int8_t* s2, const int8_t* t2,
+                             const uint8_t* c13_sh, const int8_t* s13_sh, const int8_t* t13_sh, const uint8_t* c2_sh,
+                             const int8_t* s2_sh, const int8_t* t2_sh, moe_bf16* out, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  MOE_TRY(check_common(plan, T, ws, ws_bytes));
+  if (T == 0) return MOE_OK;
+  if (!fp8_mma_shapes(plan->cfg)) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_route_ptrs(plan, x, token_ids, w_r, bias));
+  MOE_TRY(need16(c13));
+  MOE_TRY(need16(c2));
+  if (s13 == nullptr || t13 == nullptr || s2 == nullptr || t2 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(s13, 4) || !aligned(s2, 4)) return MOE_ERR_ALIGNMENT;
+  if (plan->cfg.n_shared) {
+    MOE_TRY(need16(c13_sh));
+    MOE_TRY(need16(c2_sh));
+    if (s13_sh == nullptr || t13_sh == nullptr || s2_sh == nullptr || t2_sh == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned(s13_sh, 4) || !aligned(s2_sh, 4)) return MOE_ERR_ALIGNMENT;
+  }
+  MOE_TRY(need16(out));
+  int sms = 0;
+  MOE_TRY(num_sms(&sms));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(plan->cfg, T);
+  record(plan, ST_START, s);
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  int32_t* ids = at<int32_t>(ws, L.topk_ids);
+  float* w = at<float>(ws, L.topk_w);
+  MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
+  const Fp8Weights qw = {c13, t13, c2, t2, c13_sh, t13_sh, c2_sh, t2_sh, s13, s2, s13_sh, s2_sh};
   return run_experts(plan, T, x, ids, w, nullptr, nullptr, nullptr, nullptr, out, ws, sms, s, &qw);
 }
 

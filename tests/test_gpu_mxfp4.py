@@ -135,3 +135,58 @@ def test_mxfp4_layer_vs_oracle(w):
 def test_mxfp4_full_size_layer():
     """The V4-Flash T=64 layer at full size, output on two sampled tokens."""
     run_layer(W.V4FLASH_T64, seed=0, sample=2)
+
+
+# Native MXFP4 weights (the codes streamed and turned into E4M3 on the chip): shapes with d and
+# d_ff multiples of 128.
+NATIVE = [
+    W.Workload("mid_T64", T=64, d=512, d_ff=256, E=16, k=4, n_shared=1, score=W.SCORE_SIGMOID, use_bias=True),
+    W.Workload("wide_T64", T=64, d=512, d_ff=256, E=64, k=2, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
+               use_bias=True),
+    W.Workload("noshared_T40", T=40, d=384, d_ff=384, E=12, k=3, n_shared=0, score=W.SCORE_SOFTMAX),
+    W.Workload("v4flash_E16_T64", T=64, d=4096, d_ff=2048, E=16, k=6, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
+               use_bias=True),
+]
+
+
+def run_native(w, seed, sample=None):
+    inp = inputs.make_layer_inputs(w, seed=seed, device=DEV)
+    layer = binding.MoELayer(w, inp)
+    q4 = layer.quantize_mxfp4()
+    y = layer.forward_mxfp4(inp.x, layer.mxfp4_native(q4), inp.token_ids)
+    assert layer.check_status() == 0
+    y_conv = layer.forward_fp8(inp.x, layer.mxfp4_to_fp8(q4), inp.token_ids)
+    assert layer.check_status() == 0
+    v = layer.views(w.T)
+    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
+    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    tok = np.nonzero(same)[0]
+    if sample is not None:
+        tok = np.sort(np.random.default_rng(98).choice(tok, size=min(sample, tok.size), replace=False))
+    fetch = OracleMxfp4Fetcher(inp)
+    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
+    diff = (y.float() - y_conv.float()).abs().max().item()
+    print(f"{w.name} (native mxfp4): max elementwise {e:.2e}, normwise {n:.2e}; "
+          f"max |native - converted fp8 path| {diff:.2e}")
+    layer.close()
+
+
+@pytest.mark.parametrize("w", NATIVE, ids=lambda w: w.name)
+def test_native_mxfp4_layer_vs_oracle(w):
+    run_native(w, seed=37)
+
+
+@pytest.mark.slow
+def test_native_mxfp4_full_size_layer():
+    run_native(W.V4FLASH_T64, seed=0, sample=2)
+
+
+def test_native_mxfp4_needs_128_multiples():
+    inp = inputs.make_layer_inputs(W.TOY, seed=1, device=DEV)
+    layer = binding.MoELayer(W.TOY, inp)
+    q = layer.mxfp4_native(layer.quantize_mxfp4())
+    with pytest.raises(binding.MoEError) as ei:
+        layer.forward_mxfp4(inp.x, q)
+    assert binding.STATUS_NAMES[ei.value.status] == "MOE_ERR_UNSUPPORTED"
+    layer.close()
