@@ -162,8 +162,9 @@ moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int
  * FP8 E4M3 tiles of 128 x 128 while the sub-block scales inside a tile stay within the FP8
  * exponent headroom).
  *   w [n_mats, rows, K] bf16 (device, 16-byte aligned, K a multiple of 32) -> codes
- *   [n_mats, rows, K/2] uint8 (16-byte aligned; element 2i in the low nibble of byte i; code =
- *   sign << 3 | index of the magnitude in {0, 0.5, 1, 1.5, 2, 3, 4, 6}) and exps
+ *   [n_mats, rows, K/2] uint8 (16-byte aligned; eight consecutive elements per little-endian
+ *   32-bit word: the index of element k's magnitude in {0, 0.5, 1, 1.5, 2, 3, 4, 6} in bits
+ *   4k..4k+2, the sign of element j < 4 in bit 8j+7, that of element 4+j in bit 8j+3) and exps
  *   [n_mats, rows, K/32] int8.  s = the smallest integer with max|w| <= 6 * 2^s over the
  *   sub-block (at least -114), raised to (the largest s of its 128 x 128 tile) - 14 where lower;
  *   an all-zero sub-block takes the tile's largest s.  code = round-to-nearest-even of w * 2^-s

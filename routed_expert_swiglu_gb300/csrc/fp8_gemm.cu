@@ -694,11 +694,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // largest sub-block exponent - 6, given with the weights), exact since s - E lies in [-8, 6], and
 // store them into a ring of A tiles in Tensor Memory; the 8-bit MMA reads A from there and B (the
 // pieces) from shared memory, and the epilogue is that of the FP8 MMA kernel with 2^E per tile.
-// A code becomes its byte with two byte permutes per four codes: one picks the magnitude from an
-// eight-entry table of E4M3 bytes for the sub-block's s - E, one gathers the bytes holding the
-// codes' sign bits (about 1.5 integer operations per code in all).  Decode-sized token tiles (16
-// rows).  Measured, the integer pipe bounds it near the FP8 kernel's speed: half the weight bytes
-// streamed, twice the codes converted per byte.
+// Four codes become their bytes with one byte permute, which picks the magnitudes from an
+// eight-entry table of E4M3 bytes for the sub-block's s - E; the stored layout keeps the signs
+// where the bytes keep theirs (see moe_quantize_mxfp4), so a mask and an OR add them (about 1.2
+// integer operations per code in all).  Decode-sized token tiles (16 rows).  The integer pipe,
+// not the halved weight stream, bounds it.
 
 // D (+)= A[tmem] * B[smem]^T on 8-bit operands: A's 128 rows in the 128 lanes, K = 32 codes
 // packed four per 32-bit column (8 columns, the lowest k in the lowest byte).
@@ -719,16 +719,14 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                : "memory");
 }
 
-// Eight packed E2M1 codes (one word, code i in bits 4i..4i+3) -> eight E4M3 bytes (two words,
-// low word first) with the magnitude table lut (bytes 0..7 of lut_lo, lut_hi).
+// Eight stored E2M1 codes (one word: the magnitude index of code k in bits 4k..4k+2, the sign
+// of code j < 4 in bit 8j+7, that of code 4+j in bit 8j+3) -> eight E4M3 bytes (two words, low
+// word first) with the magnitude table lut (bytes 0..7 of lut_lo, lut_hi): one byte permute
+// picks four magnitudes, the signs are already where the bytes keep theirs.
 __device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
   const uint32_t m_lo = __byte_perm(lut_lo, lut_hi, w & 0x7777u);          // magnitudes of codes 0..3
   const uint32_t m_hi = __byte_perm(lut_lo, lut_hi, (w >> 16) & 0x7777u);  // codes 4..7
-  // byte 0 of (w << 4) has code 0's sign in bit 7, byte 0 of w code 1's, and so on
-  const uint32_t w4 = w << 4;
-  const uint32_t s_lo = __byte_perm(w4, w, 0x5140u);
-  const uint32_t s_hi = __byte_perm(w4, w, 0x7362u);
-  return make_uint2(m_lo | (s_lo & 0x80808080u), m_hi | (s_hi & 0x80808080u));
+  return make_uint2(m_lo | (w & 0x80808080u), m_hi | ((w << 4) & 0x80808080u));
 }
 
 // The parameter block plus the MXFP4 sub-block exponents [mats, rows, K/32] (int8) of the routed
@@ -739,10 +737,10 @@ struct Fp4Params : GemmParams {
 };
 
 // Converter groups of the MXFP4 kernel (four warps each).  The conversion is bound by the
-// integer pipe: 2, 3 and 4 groups measured alike (V4-Flash T=64: 0.827 / 0.830 / 0.874 ms); 3
-// fit without register spills.
+// integer pipe: 2, 3 and 4 groups measured alike (V4-Flash T=64: 0.827 / 0.830 / 0.874 ms); 2
+// leave the epilogue room (96 registers) to sum the pieces exactly as the FP8 kernel does.
 #ifndef MOE_F4_CVT_GROUPS
-#define MOE_F4_CVT_GROUPS 3
+#define MOE_F4_CVT_GROUPS 2
 #endif
 
 template <int EPI, int MBLK>
@@ -972,14 +970,17 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
           for (int a = 0; a < S::NUM_A; ++a) {
             const float sc = __int_as_float((e_cur[a] + 127) << 23);  // 2^E, E in [-126, 121]
 #pragma unroll
-            for (int pc = 0; pc < S::PIECES; ++pc) {  // one piece's 16 columns per wait
-              const float scp = sc * (pc == 0 ? 1.0f : pc == 1 ? 0.0625f : pc == 2 ? 0.00390625f : 0.000244140625f);
-              uint32_t r0[16];
-              tmem_ld16(ts + a * S::PIECES * TN + pc * t.n_mma, r0);
-              tmem_ld_wait();
-              reg_fence16(r0);
+            for (int pp = 0; pp < S::PIECES; pp += 2) {  // two pieces per wait, summed as in the FP8 kernel
+              const float scp = sc * (pp == 0 ? 1.0f : 0.00390625f);  // 2^E * 2^(-4 pp), exact
+              uint32_t r0[2][16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) acc[a][j] = fmaf(__uint_as_float(r0[j]), scp, acc[a][j]);
+              for (int q = 0; q < 2; ++q) tmem_ld16(ts + a * S::PIECES * TN + (pp + q) * t.n_mma, r0[q]);
+              tmem_ld_wait();
+              reg_fence16(r0[0]);
+              reg_fence16(r0[1]);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                acc[a][j] = fmaf(fmaf(__uint_as_float(r0[1][j]), 0.0625f, __uint_as_float(r0[0][j])), scp, acc[a][j]);
             }
           }
         }

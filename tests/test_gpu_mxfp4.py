@@ -28,17 +28,16 @@ def _built():
 
 
 def pack(codes):
-    """Two 4-bit codes per byte, the even column in the low nibble (the library's layout)."""
-    c = np.asarray(codes, dtype=np.uint8)
-    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
-
-
-def unpack(packed):
-    p = np.asarray(packed, dtype=np.uint8)
-    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
-    out[..., 0::2] = p & 0xF
-    out[..., 1::2] = p >> 4
-    return out
+    """The library's storage of E2M1 codes: eight consecutive codes per little-endian 32-bit
+    word, the magnitude index of code k in bits 4k..4k+2, the sign of code j < 4 in bit 8j+7 and
+    that of code 4+j in bit 8j+3."""
+    c = np.asarray(codes, dtype=np.uint64)
+    c = c.reshape(c.shape[:-1] + (c.shape[-1] // 8, 8))
+    word = np.zeros(c.shape[:-1], dtype=np.uint64)
+    for k in range(8):
+        word |= (c[..., k] & 7) << (4 * k)
+        word |= (c[..., k] >> 3) << (8 * k + 7 if k < 4 else 8 * (k - 4) + 3)
+    return word.astype("<u4").view(np.uint8).reshape(codes.shape[:-1] + (codes.shape[-1] // 2,))
 
 
 def weights(shape, seed):
@@ -169,6 +168,8 @@ def run_native(w, seed, sample=None):
     diff = (y.float() - y_conv.float()).abs().max().item()
     print(f"{w.name} (native mxfp4): max elementwise {e:.2e}, normwise {n:.2e}; "
           f"max |native - converted fp8 path| {diff:.2e}")
+    # the same E4M3 values through the same MMA, partials and summation order: bit for bit
+    assert torch.equal(y, y_conv), f"{w.name}: native and converted paths differ by up to {diff:.2e}"
     layer.close()
 
 
