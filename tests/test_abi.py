@@ -104,3 +104,46 @@ def test_hash_plan_requires_token_ids(lib):
     p = ctypes.c_void_p(base)
     assert lib.moe_route(plan, 8, p, None, p, None, p, p, None, p, need, None) == 1
     binding.moe_plan_destroy(plan)
+
+
+def test_weight_format_validation_without_gpu(lib):
+    """FP8 / MXFP4 entry points reject bad shapes, null and misaligned pointers on the host."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p16, nul = ctypes.c_void_p(base), None
+    # quantisers: K a multiple of 32 (MXFP4), positive sizes, non-null, aligned
+    assert lib.moe_quantize_mxfp4(p16, 1, 128, 100, p16, p16, nul) == 1
+    assert lib.moe_quantize_mxfp4(nul, 1, 128, 128, p16, p16, nul) == 1
+    assert lib.moe_quantize_mxfp4(ctypes.c_void_p(base + 2), 1, 128, 128, p16, p16, nul) == 3
+    assert lib.moe_quantize_mxfp4(p16, 1, 128, 128, ctypes.c_void_p(base + 8), p16, nul) == 3
+    assert lib.moe_quantize_fp8(p16, 1, 0, 128, p16, p16, nul) == 1
+    assert lib.moe_quantize_fp8(ctypes.c_void_p(base + 1), 1, 128, 128, p16, p16, nul) == 3
+    # conversion: tile exponents required, codes optional, K a multiple of 32
+    assert lib.moe_mxfp4_to_fp8(p16, p16, 1, 128, 128, p16, nul, nul) == 1
+    assert lib.moe_mxfp4_to_fp8(p16, p16, 1, 128, 96 + 8, p16, p16, nul) == 1
+    assert lib.moe_mxfp4_to_fp8(p16, p16, 1, 128, 128, ctypes.c_void_p(base + 4), p16, nul) == 3
+    # the native MXFP4 forward: arguments, exponent alignment, and the shape rule
+    plan = binding.moe_plan_create(_cfg(max_tokens=64))
+    need = lib.moe_workspace_bytes(plan, 64)
+    ws_buf = ctypes.create_string_buffer(need + 4096)
+    ws = ctypes.c_void_p((ctypes.addressof(ws_buf) + 255) // 256 * 256)
+    w = [p16] * 12
+    assert lib.moe_forward_mxfp4(plan, 65, p16, nul, p16, nul, *w, p16, ws, need, nul) == 1
+    bad = list(w)
+    bad[2] = nul                                        # t13
+    assert lib.moe_forward_mxfp4(plan, 64, p16, nul, p16, nul, *bad, p16, ws, need, nul) == 1
+    bad = list(w)
+    bad[1] = ctypes.c_void_p(base + 2)                  # s13 not 4-byte aligned
+    assert lib.moe_forward_mxfp4(plan, 64, p16, nul, p16, nul, *bad, p16, ws, need, nul) == 3
+    bad = list(w)
+    bad[6] = nul                                        # shared codes of a layer with a shared expert
+    assert lib.moe_forward_mxfp4(plan, 64, p16, nul, p16, nul, *bad, p16, ws, need, nul) == 1
+    assert lib.moe_forward_fp8(plan, 64, p16, nul, p16, nul, p16, nul, p16, p16, p16, p16, p16, p16, p16, ws,
+                               need, nul) == 1         # e13 null
+    binding.moe_plan_destroy(plan)
+    toy = binding.moe_plan_create(binding.config_for(W.TOY, max_tokens=64))   # d_ff = 64
+    need = lib.moe_workspace_bytes(toy, 64)
+    ws_buf = ctypes.create_string_buffer(need + 4096)
+    ws = ctypes.c_void_p((ctypes.addressof(ws_buf) + 255) // 256 * 256)
+    assert lib.moe_forward_mxfp4(toy, 64, p16, nul, p16, nul, *w, p16, ws, need, nul) == 2
+    binding.moe_plan_destroy(toy)
