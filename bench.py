@@ -5,8 +5,11 @@
 One step = one whole layer forward (router GEMM, top-k, dispatch, gate/up grouped GEMM, down
 grouped GEMM, combine) over one batch of T synthetic tokens whose inputs are resident in HBM.
 Default workload: the DeepSeek-V4-Flash-shaped layer at T=8192 (prefill); the same line
-carries a T=64 (decode) measurement.  Multi-GPU runs are independent replicas (one process
-per GPU, each with its own token batch; no collective on the data path).
+carries a T=64 (decode) measurement under "decode", with the same layer on FP8 expert weights
+("fp8_weights") and on MXFP4 expert weights ("mxfp4_weights": the one-time conversion to the FP8
+form, the forward on the converted tiles, and the native forward that streams the 4-bit codes).
+Multi-GPU runs are independent replicas (one process per GPU, each with its own token batch; no
+collective on the data path).
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on bounded
 samples of the same workload, on this machine's host cores.
