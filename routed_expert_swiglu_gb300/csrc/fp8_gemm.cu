@@ -1,9 +1,12 @@
-// FP8 (E4M3) expert weights in the grouped GEMMs: one power-of-two scale per 128 x 128 tile of
-// codes ("DeepSeek-V4 MoE", section "FP4 QAT 怎么做到反量化无损").  Two kernel families:
-//   * fp8mma_gemm_kernel: the codes are the 8-bit MMA's A operand as stored, the activations
+// FP8 (E4M3) and MXFP4 (E2M1) expert weights in the grouped GEMMs ("DeepSeek-V4 MoE", section
+// "FP4 QAT 怎么做到反量化无损": FP8 with one power-of-two scale per 128 x 128 tile, FP4 with one
+// per 1 x 32 sub-block, losslessly dequantised to the FP8 form).  Three kernel families:
+//   * fp8mma_gemm_kernel: FP8 codes as the 8-bit MMA's A operand, as stored; the activations as
 //     E4M3 pieces (d and d_ff multiples of 128);
-//   * fp8w_gemm_kernel: the codes are widened to bf16 into Tensor Memory and multiplied by the
-//     bf16 activations (any shape).
+//   * fp4mma_gemm_kernel: MXFP4 codes turned into the E4M3 bytes of the FP8 form on the chip,
+//     into Tensor Memory, then as fp8mma (same shapes, decode-sized token tiles);
+//   * fp8w_gemm_kernel: FP8 codes widened to bf16 into Tensor Memory and multiplied by the bf16
+//     activations (any shape).
 #include "gemm_common.cuh"
 
 namespace moe {
