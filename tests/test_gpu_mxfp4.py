@@ -145,6 +145,8 @@ NATIVE = [
     W.Workload("noshared_T40", T=40, d=384, d_ff=384, E=12, k=3, n_shared=0, score=W.SCORE_SOFTMAX),
     W.Workload("v4flash_E16_T64", T=64, d=4096, d_ff=2048, E=16, k=6, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
                use_bias=True),
+    # a prefill-sized batch: about 75 rows per expert, five 16-row tiles each, ragged last tiles
+    W.Workload("tall_T300", T=300, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
 ]
 
 
