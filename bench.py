@@ -89,9 +89,13 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
+        """The raw samples go to $MOE_CLOCKS_DIR/clocks_gpu<i>.csv (the system temp directory by
+        default); the bench line carries their summary."""
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        out_dir = os.environ.get("MOE_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_gpu{gpu_index}.csv")
 
     def __enter__(self):
         try:
