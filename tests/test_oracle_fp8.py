@@ -100,3 +100,15 @@ def test_partial_tiles_brute_force():
                         got = F.e4m3_value(codes[n, i * 128 + r, j * 128 + c])
                         assert got in best                               # a nearest grid value
     assert exps[1, 1, 0] == 0 and (codes[1, 128:, :128] == 0).all()
+
+
+def test_round_to_e4m3_matches_ml_dtypes():
+    """A second library: ml_dtypes' float8_e4m3fn conversion of fp32 values agrees too."""
+    ml_dtypes = pytest.importorskip("ml_dtypes")
+    rng = np.random.default_rng(6)
+    grid = F.e4m3_value(np.arange(0, 127, dtype=np.uint8))
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    v = np.concatenate([rng.uniform(-448, 448, 50000), grid, -grid, mids, -mids,
+                        np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(0))]).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    assert np.array_equal(F.round_to_e4m3(v.astype(np.float64)), v.astype(ml_dtypes.float8_e4m3fn).astype(np.float64))

@@ -103,3 +103,19 @@ def test_conversion_rejects_exponents_beyond_the_headroom():
     exps[3, 2] = -15       # 15 binades below the tile's largest: 1.5 * 2^-9 is no E4M3 value
     with pytest.raises(ValueError):
         M.mxfp4_to_fp8(codes, exps)
+
+
+def test_rounding_matches_ml_dtypes_float4():
+    """One rounding to E2M1 agrees with ml_dtypes' float4_e2m1fn conversion (round to nearest,
+    ties to even) over the range, on the grid, on every midpoint and on its fp32 neighbours."""
+    ml_dtypes = pytest.importorskip("ml_dtypes")
+    rng = np.random.default_rng(5)
+    grid = np.concatenate([M.GRID, -M.GRID])
+    mids = np.sort(M.GRID)
+    mids = ((mids[1:] + mids[:-1]) / 2).astype(np.float32)
+    near = np.concatenate([np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(0))])
+    v = np.concatenate([rng.uniform(-6, 6, 50000), grid, mids, -mids, near, -near]).astype(np.float32)
+    ours = M.e2m1_value(M.round_to_e2m1_code(v.astype(np.float64)))
+    ref = v.astype(ml_dtypes.float4_e2m1fn).astype(np.float64)
+    assert np.array_equal(np.abs(ours), np.abs(ref))
+    assert np.array_equal(np.sign(ours), np.sign(ref) * (ref != 0))    # zero is stored as +0 here
