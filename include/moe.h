@@ -191,9 +191,9 @@ moe_status moe_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int32_t n_
  * the activations as sums of E4M3 pieces (piece p weighted 2^(-4p)) and one power-of-two scale
  * per row: x in two pieces, exact for every value above 2^-13.8 of its row's largest magnitude
  * and within 2^-21 of that magnitude below it; h in four pieces, within 2^-16 of each value plus
- * 2^-29 of the row's largest magnitude.  Other shapes widen the codes
- * to bf16 into Tensor Memory and run the bf16 MMA.  Code pointers 16-byte aligned; same
- * workspace and outputs as moe_forward. */
+ * 2^-29 of the row's largest magnitude.  Other shapes widen the codes to bf16 into Tensor
+ * Memory and run the bf16 MMA.  Code pointers 16-byte aligned; same workspace and outputs as
+ * moe_forward. */
 moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                            const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,
                            const uint8_t* q2, const int8_t* e2, const uint8_t* q13_sh, const int8_t* e13_sh,
