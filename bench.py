@@ -52,6 +52,22 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- distributed
 
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_replicas(n: int) -> int:
+    """`--gpus N` without a launcher's environment: start N rank processes of this same command
+    (torch.distributed.run, one process per GPU, rendezvous on 127.0.0.1) and return their
+    exit status.  Rank 0 prints the JSON line."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -328,20 +344,25 @@ def measured_traffic(workload_name):
 
 def gate_up_bytes(w, active):
     """Algorithmic HBM bytes of one gate/up grouped-GEMM launch: the w13 slabs of the active
-    experts (+ shared), the dispatched rows and x it reads, h it writes (bf16)."""
+    experts (+ shared) and the layer input x, read once.  The dispatched rows it reads and the
+    activations it writes are intermediates of this implementation, reported separately
+    (gate_up_intermediate_bytes)."""
     bf = 2
-    weights = (active + w.n_shared) * 2 * w.d * w.d_ff * bf
-    acts_in = (w.N + w.n_shared * w.T) * w.d * bf
-    h_out = (w.N + w.n_shared * w.T) * w.d_ff * bf
-    return weights + acts_in + h_out
+    return (active + w.n_shared) * 2 * w.d * w.d_ff * bf + w.T * w.d * bf
+
+
+def gate_up_intermediate_bytes(w):
+    """Bytes the gate/up launch moves beyond its algorithmic ones: the dispatched routed rows
+    read (the shared expert reads x itself) and the (hi, lo) activation pair written."""
+    bf = 2
+    return w.N * w.d * bf + (w.N + w.n_shared * w.T) * 2 * w.d_ff * bf
 
 
 def run_ours(args, world, rank, local):
     from routed_expert_swiglu_gb300 import binding, build
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if not os.path.exists(binding.LIB_PATH):
-        build.build()
+    build.build()  # recompiles whatever is older than its sources; a no-op when up to date
     binding.load()
     peaks, peak_src = load_peaks()
     w = workloads.BY_NAME[args.workload]
@@ -412,7 +433,7 @@ def run_ours(args, world, rank, local):
         "roofline": {"kernel": "gate_up_gemm", "bound": "hbm", "achieved": round(g1_gbs, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(g1_gbs / hbm_peak, 4),
                      "peak_source": peak_src, "traffic": measured_traffic(w.name), "algorithmic_bytes": int(g1_bytes),
-                     "avg_ms": round(g1_ms, 4)},
+                     "intermediate_bytes": int(gate_up_intermediate_bytes(w)), "avg_ms": round(g1_ms, 4)},
         "layer_roofline": {"flops": int(layer_flops), "bytes": int(layer_bytes), "active_experts": active,
                            "roofline_ms": round(roof_s * 1e3, 4), "frac": round(roof_s * 1e3 / ms_per_step, 4),
                            "peaks": f"{peaks['bf16_tflops_sustained']} TFLOP/s sustained bf16, {hbm_peak} GB/s "
@@ -537,6 +558,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_replicas(args.gpus))
     world, rank, local = dist_setup(args)
     try:
         if args.impl == "reference":

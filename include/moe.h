@@ -141,9 +141,18 @@ moe_status moe_permute(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32
  * ~0.33 MB array of device memory inside the library (held by every GPU that loads it until
  * exit); T * top_k above 131072 returns MOE_ERR_UNSUPPORTED.  Every call shares that array:
  * calls whose work overlaps on the GPU (unordered streams) race.  The first call on a device
- * looks up the array's address; make it before any stream capture.  Nothing is allocated. */
+ * looks up the array's address; make it before any stream capture.  Nothing is allocated.
+ * An expert id outside [0, E) is clamped into range as in moe_permute and flagged in the
+ * array's error word (cleared by every call); this call itself returns MOE_OK regardless,
+ * and moe_permute_noalloc_status reports the flag. */
 moe_status moe_permute_noalloc(moe_plan* plan, int32_t T, const int32_t* topk_ids, int32_t* counts,
                                int32_t* offsets, int32_t* perm_tok, int32_t* inv, moe_stream_t stream);
+
+/* Device-data status of the most recent moe_permute_noalloc call on the current device (whatever
+ * its stream): synchronises `stream` (which should be the one that call ran on), then returns
+ * MOE_ERR_DEVICE_INPUT if that call met an expert id outside [0, E), else MOE_OK (also when no
+ * call has run on this device).  Allocates nothing. */
+moe_status moe_permute_noalloc_status(moe_stream_t stream);
 
 /* FP8 (E4M3) weights with one power-of-two scale per 128 x 128 tile ("DeepSeek-V4 MoE",
  * section "FP4 QAT 怎么做到反量化无损": FP8 E4M3 weights, one scale per 128 x 128 tile).

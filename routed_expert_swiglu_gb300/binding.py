@@ -27,7 +27,7 @@ SCORE_CODES = {W.SCORE_SOFTMAX_TOPK: 0, W.SCORE_SOFTMAX: 1, W.SCORE_SIGMOID: 2, 
 EXPORTED = ("moe_plan_create", "moe_plan_destroy", "moe_workspace_bytes", "moe_route", "moe_permute",
             "moe_forward", "moe_forward_routed", "moe_forward_host", "moe_check_status",
             "moe_workspace_views", "moe_forward_stage_count", "moe_plan_set_events",
-            "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc",
+            "moe_forward_launch_count", "moe_status_string", "moe_permute_noalloc", "moe_permute_noalloc_status",
             "moe_update_bias", "moe_quantize_fp8", "moe_forward_fp8", "moe_quantize_mxfp4", "moe_mxfp4_to_fp8",
             "moe_forward_mxfp4")
 
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward_launch_count": ([P, I], I),
         "moe_status_string": ([I], ctypes.c_char_p),
         "moe_permute_noalloc": ([P, I, V, V, V, V, V, V], I),
+        "moe_permute_noalloc_status": ([V], I),
         "moe_update_bias": ([P, I, V, V, ctypes.c_float, V], I),
         "moe_quantize_fp8": ([V, I, I, I, V, V, V], I),
         "moe_forward_fp8": ([P, I, V, V, V, V, V, V, V, V, V, V, V, V, V, V, S, V], I),
@@ -152,6 +153,12 @@ def moe_permute_noalloc(plan, T, topk_ids, counts, offsets, perm_tok, inv, strea
     library keeps a fixed scratch array on each device; T * top_k <= 131072)."""
     _check(load().moe_permute_noalloc(plan, T, _ptr(topk_ids), _ptr(counts), _ptr(offsets), _ptr(perm_tok),
                                       _ptr(inv), _stream(stream)), "moe_permute_noalloc")
+
+
+def moe_permute_noalloc_status(stream=None):
+    """Status code of the latest moe_permute_noalloc call on the current device (synchronises
+    the stream): MOE_OK, or MOE_ERR_DEVICE_INPUT if it met an expert id outside [0, E)."""
+    return int(load().moe_permute_noalloc_status(_stream(stream)))
 
 
 def moe_update_bias(plan, T, counts, bias, gamma=0.001, stream=None):

@@ -41,11 +41,6 @@ struct GemmParams {
   long long split_stride;
   int dense_rows;
   int* err;
-  // gathered B (pair gate/up): routed row r of a group is row b_idx[r] of b_x ([*, b_ld] bf16),
-  // a shared-expert row r is row r + shared_b_shift of b_x
-  const __nv_bfloat16* b_x;
-  const int32_t* b_idx;
-  int b_ld;
   // FP8 weights: int8 tile exponents [mats, exp_nr, exp_nk] of the routed (a_exp) and shared
   // (a_sh_exp) weight codes, one per 128 x 128 tile of each matrix
   const int8_t* a_exp;

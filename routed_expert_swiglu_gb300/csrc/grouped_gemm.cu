@@ -263,13 +263,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //           [64 r, 64 r + 64) followed by the up rows of the same features, so gate and up of
 //           one feature sit in TMEM lanes i and i + 64 of one CTA (exchanged through smem).
 //   fp32:   the pair covers 256 output features, CTA r the features [128 r, 128 r + 128).
-// MB = 2 gives each CTA two 128-row weight slabs against the same token rows (twice the MMA work
-// per byte of B landed; both accumulators fill the 512 TMEM columns, one buffer):
-//   SwiGLU: slab 0 = the gate rows, slab 1 = the up rows of the CTA's 128 features (the pair
-//           covers 256), so gate and up of a feature sit in the same TMEM lane of accumulators
-//           0 and 1 and the epilogue needs no exchange;
-//   fp32:   two adjacent 128-feature blocks (the pair covers 512 output features).
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int MB, bool BG>
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
 struct PairShape {
   static constexpr int BLOCK_K = BK;
   static constexpr int ROW_BYTES = BK * 2;
@@ -277,57 +271,38 @@ struct PairShape {
   static constexpr int A_BYTES = BLOCK_M * BK * 2;                  // one 128-row weight slab
   static constexpr int NUM_B = HILO ? 2 : 1;
   static constexpr int B_BYTES = HALF * BK * 2;
-  static constexpr int STAGE_BYTES = MB * A_BYTES + NUM_B * B_BYTES;
-  static constexpr bool GU = (EPI == EPI_SWIGLU) && MB == 2;       // gate slab + up slab
-  static constexpr int XCH = (EPI == EPI_SWIGLU && !GU) ? 4 : 0;    // gate/up warp pairs
+  static constexpr int STAGE_BYTES = A_BYTES + NUM_B * B_BYTES;
+  static constexpr int XCH = (EPI == EPI_SWIGLU) ? 4 : 0;           // gate/up warp pairs
   static constexpr int XBUF_BYTES = XCH * 2 * 16 * 32 * 4;          // 2 slots of 16 x 32 fp32
-  static constexpr int ACC_COLS = MB * TN;                          // MB accumulators of TN columns
+  static constexpr int ACC_COLS = TN;                               // one accumulator of TN columns
   static constexpr int NUM_BUF = (TMEM_ALLOC / ACC_COLS) >= 2 ? 2 : 1;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 512 - XBUF_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + XBUF_BYTES + 1024 + 512;
-  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? (GU ? 2 * BLOCK_M : BLOCK_M) : 2 * BLOCK_M * MB;
-  static constexpr int A_BOX = (EPI == EPI_SWIGLU) ? (GU ? BLOCK_M : BLOCK_M / 2) : BLOCK_M;
-  // BG: the token rows are gathered by NBW loader warps with 16-byte cp.async copies, and one
-  // relay warp reports their completed stages to the pair's even CTA
-  static constexpr int NBW = BG ? 4 : 0;
-  static constexpr int THREADS = (2 + NUM_EPI_WARPS + NBW + (BG ? 1 : 0)) * 32;
-  static constexpr int CHUNKS = ROW_BYTES / 16;                     // 16-byte chunks per token row
-  static constexpr int ROWS_PER_PASS = BG ? NBW * 32 / CHUNKS : 1;
-  static constexpr int ROWS_PER_THREAD = BG ? HALF / ROWS_PER_PASS : 0;
-  static_assert(!BG || (EPI == EPI_SWIGLU && !HILO && BK == 64 && HALF % ROWS_PER_PASS == 0),
-                "gathered token rows: gate/up, 128-byte rows");
-  // barriers (full, empty per stage; acc full/empty x2; exchange full/empty x2 per channel;
-  // BG: gathered-rows landed per stage), then the TMEM address slot and the abort flag, in the
-  // last 512 bytes
-  static constexpr int NUM_LBAR = BG ? STAGES : 0;
-  static_assert((2 * STAGES + 4 + 4 * XCH + NUM_LBAR) * 8 + 8 <= 512, "barrier area");
+  static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : 2 * BLOCK_M;
+  static constexpr int A_BOX = (EPI == EPI_SWIGLU) ? BLOCK_M / 2 : BLOCK_M;
+  static constexpr int THREADS = (2 + NUM_EPI_WARPS) * 32;
+  // barriers (full, empty per stage; acc full/empty x2; exchange full/empty x2 per channel),
+  // then the TMEM address slot and the abort flag, in the last 512 bytes
+  static_assert((2 * STAGES + 4 + 4 * XCH) * 8 + 8 <= 512, "barrier area");
   static_assert(TN % 32 == 0 && TN <= 256, "pair token tile");
   static_assert(TMEM_ALLOC >= ACC_COLS && TMEM_ALLOC <= 512, "TMEM allocation");
   static_assert(STAGES >= 2, "pipeline needs two stages");
   static_assert(BK == 64 || BK == 32, "stage K");
-  static_assert(MB == 1 || MB == 2, "weight slabs per CTA");
 };
 
-// NP = CTA pairs per cluster.  With NP = 2 the two pairs of a cluster work on the same token
-// rows and on adjacent feature blocks; each CTA TMA-loads a quarter of the token rows and
-// multicasts it to the CTA holding the same half in the other pair, so each SM requests only
-// half of its B half.  The multicast's bytes are counted on each destination pair's even-CTA
-// barrier, and a stage is refilled only after both pairs' MMAs released it.
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB, bool BG>
-__global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, BG>::THREADS, 1)
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
+__global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>::THREADS, 1)
     pair_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, BG>;
-  static_assert(!BG || NP == 1, "gathered token rows with one pair per cluster");
+  using S = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
   constexpr int STAGES = S::STAGES;
   constexpr int BLOCK_K = S::BLOCK_K;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * S::STAGE_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES + S::XBUF_BYTES);
-  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], xfull[XCH][2], xempty[XCH][2],
-  // landed[NUM_LBAR]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4 + 4 * S::XCH + S::NUM_LBAR);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], xfull[XCH][2], xempty[XCH][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4 + 4 * S::XCH);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -336,20 +311,16 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   auto xfull_bar = [&](int x, int sl) { return bar0 + 8u * (2 * STAGES + 4 + 2 * x + sl); };
   auto xempty_bar = [&](int x, int sl) { return bar0 + 8u * (2 * STAGES + 4 + 2 * S::XCH + 2 * x + sl); };
-  auto landed_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 4 + 4 * S::XCH + s); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;    // position in the CTA pair
-  const uint32_t pp = crank >> 1;      // which pair of the cluster
-  const uint32_t lrank = crank & ~1u;  // cluster rank of this pair's even CTA
+  const uint32_t rank = cluster_ctarank() & 1u;  // position in the CTA pair
   const bool leader = (rank == 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), BG ? 3 : 1);  // the even CTA's expect-tx arrival (+ both relays)
-      mbar_init(empty_bar(s), NP);  // one commit per pair of the cluster
+      mbar_init(full_bar(s), 1);   // the even CTA's expect-tx arrival
+      mbar_init(empty_bar(s), 1);  // the MMA commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
@@ -360,7 +331,6 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
         mbar_init(xfull_bar(x, sl), 32);
         mbar_init(xempty_bar(x, sl), 32);
       }
-    for (int s = 0; s < S::NUM_LBAR; ++s) mbar_init(landed_bar(s), S::NBW * 32);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -378,8 +348,8 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int pair = blockIdx.x / (2 * NP);   // cluster index
-  const int npairs = gridDim.x / (2 * NP);  // clusters
+  const int pair = blockIdx.x / 2;   // cluster index
+  const int npairs = gridDim.x / 2;  // clusters
   int total_tiles;
   if (p.grp != nullptr) {
     total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks * (p.sched_tn / TN);
@@ -397,58 +367,38 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
       for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
         const Tile t = decode_tile<TN>(tile, p);
         if (t.rows <= 0) continue;
-        const int mb = t.mb * NP + (int)pp;  // this pair's feature block
-        const int unit = 32 * NP;
-        const int n_mma = max(unit, (t.rows + unit - 1) / unit * unit);
+        const int n_mma = max(32, (t.rows + 31) / 32 * 32);
         const int half = n_mma >> 1;         // token rows per CTA
-        const int qh = half / NP;            // token rows this CTA loads (NP = 2: multicast)
         const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
         const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
         const int base = t.shared ? 0 : t.g * p.a_rows_per_group;
-        const int b_off = (NP == 2) ? (int)pp * qh : 0;  // rows into this CTA's half
-        const int b_row = t.b_row + (int)rank * half + b_off;
-        const uint32_t b_land = BG ? 0u : S::NUM_B * half * BLOCK_K * 2;  // TMA B bytes landing in one CTA
-        const uint32_t expect = 2u * (MB * S::A_BYTES + b_land);  // both CTAs' A and B, on the even CTA
-        const uint16_t mc_mask = (uint16_t)((1u << rank) | (1u << (2 + rank)));
+        const int b_row = t.b_row + (int)rank * half;
+        const uint32_t expect = 2u * (S::A_BYTES + S::NUM_B * half * BLOCK_K * 2);  // both CTAs, on the even CTA
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
-          const uint32_t fbc = mapa_shared(full_bar(stage), lrank);  // the pair's even CTA's full barrier
+          const uint32_t fbc = mapa_shared(full_bar(stage), 0);  // the pair's even CTA's full barrier
           if (leader) mbar_arrive_expect_tx(full_bar(stage), expect);
           const int k0 = kb * BLOCK_K;
-          if (S::GU) {
-            // gate rows, then up rows, of this CTA's 128 features: one 3-D box, two slabs
-            tma_load_3d_pair(sa, ta, fbc, k0, mb * 2 * BLOCK_M + (int)rank * BLOCK_M, t.shared ? 0 : 2 * t.g);
+          if (EPI == EPI_SWIGLU) {
+            // this CTA's gate and up slabs (64 features each) in one 3-D box
+            tma_load_3d_pair(sa, ta, fbc, k0, t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2), t.shared ? 0 : 2 * t.g);
           } else {
-#pragma unroll
-            for (int ms = 0; ms < MB; ++ms) {
-              const int fb = mb * MB + ms;  // 128-row weight slab of the pair
-              if (EPI == EPI_SWIGLU) {
-                // this CTA's gate and up slabs (64 features each) in one 3-D box
-                tma_load_3d_pair(sa + ms * S::A_BYTES, ta, fbc, k0, fb * BLOCK_M + (int)rank * (BLOCK_M / 2),
-                                 t.shared ? 0 : 2 * t.g);
-              } else {
-                tma_load_2d_pair(sa + ms * S::A_BYTES, ta, fbc, k0,
-                                 base + fb * 2 * BLOCK_M + (int)rank * BLOCK_M);
-              }
-            }
+            tma_load_2d_pair(sa, ta, fbc, k0, base + t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M);
           }
 #pragma unroll
-          for (int bp = 0; bp < (BG ? 0 : S::NUM_B); ++bp) {
-            const uint32_t sb = sa + MB * S::A_BYTES + bp * S::B_BYTES + b_off * S::ROW_BYTES;
+          for (int bp = 0; bp < S::NUM_B; ++bp) {
+            const uint32_t sb = sa + S::A_BYTES + bp * S::B_BYTES;
             const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
             int off = 0;
 #pragma unroll
             for (int i = NUM_BOX_H - 1; i >= 0; --i) {
               const int h = B_BOX << i;
-              if (h <= S::HALF && (qh - off) >= h) {
-                if (NP == 2)
-                  tma_load_2d_pair_mc(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off, mc_mask);
-                else
-                  tma_load_2d_pair(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off);
+              if (h <= S::HALF && (half - off) >= h) {
+                tma_load_2d_pair(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off);
                 off += h;
               }
             }
@@ -472,8 +422,7 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
       for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
         const Tile t = decode_tile<TN>(tile, p);
         if (t.rows <= 0) continue;
-        const int unit = 32 * NP;
-        const int n_mma = max(unit, (t.rows + unit - 1) / unit * unit);
+        const int n_mma = max(32, (t.rows + 31) / 32 * 32);
         if (!mbar_wait_cluster(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32_m256(n_mma);
@@ -487,24 +436,21 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
           const uint32_t sa = smem_u32(smem + stage * S::STAGE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+            const uint64_t da = smem_desc_sw(sa, S::ROW_BYTES) + 2 * kk;
 #pragma unroll
-            for (int ms = 0; ms < MB; ++ms) {
-              const uint64_t da = smem_desc_sw(sa + ms * S::A_BYTES, S::ROW_BYTES) + 2 * kk;
-#pragma unroll
-              for (int bp = 0; bp < S::NUM_B; ++bp) {
-                const uint64_t db = smem_desc_sw(sa + MB * S::A_BYTES + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
-                tc_mma_pair(d + ms * TN, da, db, idesc, (kb | kk | bp) ? 1u : 0u);
-              }
+            for (int bp = 0; bp < S::NUM_B; ++bp) {
+              const uint64_t db = smem_desc_sw(sa + S::A_BYTES + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
+              tc_mma_pair(d, da, db, idesc, (kb | kk | bp) ? 1u : 0u);
             }
           }
-          tc_commit_pair_mc(empty_bar(stage), (uint16_t)((1u << (2 * NP)) - 1u));  // every CTA
+          tc_commit_pair_mc(empty_bar(stage), (uint16_t)0x3u);  // both CTAs
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair_mc(accf_bar(buf), (uint16_t)(0x3u << lrank));
+        tc_commit_pair_mc(accf_bar(buf), (uint16_t)0x3u);
         if (++buf == S::NUM_BUF) {
           buf = 0;
           buf_phase ^= 1u;
@@ -512,7 +458,7 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
       }
     }
     __syncwarp();
-  } else if (warp < 2 + NUM_EPI_WARPS) {
+  } else {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int ew = warp - 2;
     const int quad = warp & 3;
@@ -522,38 +468,57 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
     uint32_t buf_phase = 0;
     uint32_t xiter = 0;                      // SwiGLU: chunks exchanged so far on this channel
     bool ok = true;
-    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), lrank);
-    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), lrank);
+    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
     for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
       const Tile t = decode_tile<TN>(tile, p);
       if (t.rows <= 0) continue;
       if (!mbar_wait_cluster(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
       tc_fence_after();
       const int nchunk = (t.rows + 15) >> 4;
-      for (int ms = 0; ok && ms < (S::GU ? 1 : MB); ++ms) {
-        const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS + ms * TN;
-        const int fb = (t.mb * NP + (int)pp) * MB + ms;  // 128-row weight slab of this accumulator
-        if (S::GU) {
-          // lane = feature; gate in accumulator 0, up in accumulator 1 of the same lane
-          const int feat = (t.mb * NP + (int)pp) * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
-          const int col = ((feat >> 6) << 7) + (feat & 63);
-          const bool fvalid = feat < p.out_features;
-          for (int ci = half; ci < nchunk; ci += 2) {
-            const int c0 = ci * 16;
-            uint32_t rg[16], ru[16];
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
+      if (EPI == EPI_SWIGLU) {
+        float* xb = xbuf + xch * (2 * 16 * 32);
+        for (int ci = half; ci < nchunk; ci += 2, ++xiter) {
+          const int sl = xiter & 1;
+          const uint32_t par = (xiter >> 1) & 1u;
+          const int c0 = ci * 16;
+          if (quad >= 2) {
+            // up lanes: hand the 16 up values of this chunk to the gate warp of the channel
+            uint32_t ru[16];
+            tmem_ld16(tq + c0, ru);
+            tmem_ld_wait();
+            reg_fence16(ru);
+            if (!mbar_wait(xempty_bar(xch, sl), par ^ 1u, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xb[(sl * 16 + j) * 32 + lane] = __uint_as_float(ru[j]);
+            mbar_arrive(xfull_bar(xch, sl));
+          } else {
+            uint32_t rg[16];
             tmem_ld16(tq + c0, rg);
-            tmem_ld16(tq + TN + c0, ru);
             tmem_ld_wait();
             reg_fence16(rg);
-            reg_fence16(ru);
-            if (fvalid) {
+            if (!mbar_wait(xfull_bar(xch, sl), par, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            float u[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
+            mbar_arrive(xempty_bar(xch, sl));
+            const int feat = t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
+            if (feat < p.out_features) {
+              const int col = ((feat >> 6) << 7) + (feat & 63);
               __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
               const int nr = min(16, t.rows - c0);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 if (j < nr) {
                   const float g = __uint_as_float(rg[j]);
-                  const float h = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(ru[j]);
+                  const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
                   const __nv_bfloat16 hi = __float2bfloat16_rn(h);
                   const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
                   out[(size_t)j * p.out_ld] = hi;
@@ -562,82 +527,30 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
               }
             }
           }
-        } else if (EPI == EPI_SWIGLU) {
-          float* xb = xbuf + xch * (2 * 16 * 32);
-          for (int ci = half; ci < nchunk; ci += 2, ++xiter) {
-            const int sl = xiter & 1;
-            const uint32_t par = (xiter >> 1) & 1u;
-            const int c0 = ci * 16;
-            if (quad >= 2) {
-              // up lanes: hand the 16 up values of this chunk to the gate warp of the channel
-              uint32_t ru[16];
-              tmem_ld16(tq + c0, ru);
-              tmem_ld_wait();
-              reg_fence16(ru);
-              if (!mbar_wait(xempty_bar(xch, sl), par ^ 1u, abort_flag, p.err)) {
-                ok = false;
-                break;
-              }
+        }
+        if (!ok) break;
+      } else {
+        const bool scaled = (p.row_scale != nullptr) && !t.shared;
+        const int feat = t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
+        for (int ci = half; ci < nchunk; ci += 2) {
+          const int c0 = ci * 16;
+          uint32_t r[16];
+          tmem_ld16(tq + c0, r);
+          tmem_ld_wait();
+          reg_fence16(r);
+          if (feat < p.out_features) {
+            float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+            const int nr = min(16, t.rows - c0);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) xb[(sl * 16 + j) * 32 + lane] = __uint_as_float(ru[j]);
-              mbar_arrive(xfull_bar(xch, sl));
-            } else {
-              uint32_t rg[16];
-              tmem_ld16(tq + c0, rg);
-              tmem_ld_wait();
-              reg_fence16(rg);
-              if (!mbar_wait(xfull_bar(xch, sl), par, abort_flag, p.err)) {
-                ok = false;
-                break;
-              }
-              float u[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
-              mbar_arrive(xempty_bar(xch, sl));
-              const int feat = fb * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
-              if (feat < p.out_features) {
-                const int col = ((feat >> 6) << 7) + (feat & 63);
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
-                const int nr = min(16, t.rows - c0);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  if (j < nr) {
-                    const float g = __uint_as_float(rg[j]);
-                    const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(h);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
-                    out[(size_t)j * p.out_ld] = hi;
-                    out[(size_t)j * p.out_ld + 64] = lo;
-                  }
-                }
-              }
-            }
-          }
-          if (!ok) break;
-        } else {
-          const bool scaled = (p.row_scale != nullptr) && !t.shared;
-          const int feat = fb * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
-          for (int ci = half; ci < nchunk; ci += 2) {
-            const int c0 = ci * 16;
-            uint32_t r[16];
-            tmem_ld16(tq + c0, r);
-            tmem_ld_wait();
-            reg_fence16(r);
-            if (feat < p.out_features) {
-              float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
-              const int nr = min(16, t.rows - c0);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                if (j < nr) {
-                  const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
-                  out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
-                }
+            for (int j = 0; j < 16; ++j) {
+              if (j < nr) {
+                const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
+                out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
               }
             }
           }
         }
       }
-      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf == 0 ? acce_leader0 : acce_leader1);
@@ -645,82 +558,6 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, B
         buf = 0;
         buf_phase ^= 1u;
       }
-    }
-  } else if constexpr (BG) {
-    // ------------------------------------------------------------------ token-row loaders (both CTAs)
-    // Loader thread b copies 16-byte chunk (b % CHUNKS) of rows b / CHUNKS + j * ROWS_PER_PASS
-    // of this CTA's half of the tile's token rows, straight from x by the permuted token ids,
-    // into the 128-byte-swizzled layout TMA would have written (chunk c of row r at
-    // c ^ (r & 7)), and arrives on the stage's landed barrier when its copies complete.  The
-    // relay lane, which issues no copies, waits for each stage to land, fences the writes to the
-    // async proxy and reports the stage to the even CTA's full barrier.
-    const bool relay = (warp == 2 + NUM_EPI_WARPS + S::NBW);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    if (relay) {
-      if (lane == 0) {
-        for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
-          const Tile t = decode_tile<TN>(tile, p);
-          if (t.rows <= 0) continue;
-          for (int kb = 0; kb < KB; ++kb) {
-            if (!mbar_wait(landed_bar(stage), phase, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive_cluster(mapa_shared(full_bar(stage), lrank));
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-      }
-      __syncwarp();
-    } else {
-      constexpr int RPT = S::ROWS_PER_THREAD;
-      const int b = (warp - 2 - NUM_EPI_WARPS) * 32 + lane;
-      const int chunk = b % S::CHUNKS;
-      const int r0 = b / S::CHUNKS;
-      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
-        const Tile t = decode_tile<TN>(tile, p);
-        if (t.rows <= 0) continue;
-        const int n_mma = max(32, (t.rows + 31) / 32 * 32);
-        const int half = n_mma >> 1;
-        const __nv_bfloat16* src[RPT];
-#pragma unroll
-        for (int j = 0; j < RPT; ++j) {
-          const int r = r0 + j * S::ROWS_PER_PASS;  // row within this CTA's half
-          const int g = (int)rank * half + r;        // row within the tile
-          src[j] = nullptr;
-          if (r < half && g < t.rows) {
-            const int tok = t.shared ? t.out_row + g + p.shared_b_shift : __ldg(p.b_idx + t.out_row + g);
-            src[j] = p.b_x + (size_t)tok * p.b_ld + chunk * 8;
-          }
-        }
-        for (int kb = 0; kb < KB; ++kb) {
-          bool got = true;
-          if (lane == 0) got = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err);
-          if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sb = smem_u32(smem + stage * S::STAGE_BYTES + MB * S::A_BYTES);
-#pragma unroll
-          for (int j = 0; j < RPT; ++j) {
-            const int r = r0 + j * S::ROWS_PER_PASS;
-            if (src[j] != nullptr) cp_async16(sb + r * S::ROW_BYTES + ((chunk ^ (r & 7)) << 4), src[j] + kb * BLOCK_K);
-          }
-          cp_async_arrive_noinc(landed_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      cp_async_commit();  // copies never committed so far form the last group
-      cp_async_wait<0>();
     }
   }
 
@@ -812,22 +649,16 @@ static cudaError_t launch_variant(const GemmLaunch& L, GemmParams p, cudaStream_
   return cudaGetLastError();
 }
 
-template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC, int NP, int MB, bool BG = false>
+template <int EPI, int TN, bool HILO, int BK, int TMEM_ALLOC>
 static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
-  using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC, MB, BG>;
+  using Sh = PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>;
   static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
   if (p.sched_tn % TN != 0 || L.K % BK != 0) return cudaErrorInvalidValue;
   GemmMaps m;
   memset(&m, 0, sizeof(m));
   const int kb_cols = HILO ? 2 * L.K : L.K;
   if (!make_a_maps(m, L, EPI == EPI_SWIGLU, Sh::A_BOX, BK)) return cudaErrorInvalidValue;
-  if (BG) {
-    if (L.b_gather_x == nullptr || L.b_gather_idx == nullptr) return cudaErrorInvalidValue;
-    p.b_x = static_cast<const __nv_bfloat16*>(L.b_gather_x);
-    p.b_idx = L.b_gather_idx;
-    p.b_ld = L.K;
-  }
-  for (int i = 0; i < (BG ? 0 : NUM_BOX_H); ++i) {
+  for (int i = 0; i < NUM_BOX_H; ++i) {
     const int h = B_BOX << i;
     if (h > Sh::HALF) break;
     if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h, BK)) return cudaErrorInvalidValue;
@@ -837,12 +668,9 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
       m.b_sh[i] = m.b[i];
     }
   }
-  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC, NP, MB, BG>;
+  auto kern = pair_gemm_kernel<EPI, TN, HILO, BK, TMEM_ALLOC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  // the schedule counts pair feature blocks of one slab; a CTA of MB slabs, in a cluster of NP
-  // pairs, covers MB * NP of them
-  p.num_mblocks = (p.num_mblocks + NP * MB - 1) / (NP * MB);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.blockDim = dim3(Sh::THREADS);
@@ -850,7 +678,7 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2 * NP;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -858,20 +686,20 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
   // as many clusters as can be resident at once (persistent kernel), at most one per tile
   static int max_clusters = 0;
   if (max_clusters == 0) {
-    cfg.gridDim = dim3(2 * NP * (L.num_sms / (2 * NP)));
+    cfg.gridDim = dim3(2 * (L.num_sms / 2));
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();
-      n = L.num_sms / (2 * NP);
+      n = L.num_sms / 2;
     }
     max_clusters = n;
   }
   int clusters = max_clusters;
   if (MOE_PAIR_MAX_CLUSTERS > 0 && clusters > MOE_PAIR_MAX_CLUSTERS) clusters = MOE_PAIR_MAX_CLUSTERS;
-  const int tiles = (L.max_tiles + NP * MB - 1) / (NP * MB) * (p.sched_tn / TN);
+  const int tiles = L.max_tiles * (p.sched_tn / TN);
   if (tiles < clusters) clusters = tiles;
   if (clusters < 1) clusters = 1;
-  cfg.gridDim = dim3(2 * NP * clusters);
+  cfg.gridDim = dim3(2 * clusters);
   e = cudaLaunchKernelEx(&cfg, kern, m, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -900,9 +728,6 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.split_stride = L.split_stride;
   p.dense_rows = L.dense_rows;
   p.err = L.err;
-  p.b_x = nullptr;
-  p.b_idx = nullptr;
-  p.b_ld = 0;
   p.a_exp = nullptr;
   p.a_sh_exp = nullptr;
   p.exp_nr = p.exp_nk = 0;
@@ -911,23 +736,10 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   constexpr int TNP = MOE_TN_PREFILL;
   constexpr int TN2 = MOE_TN_DOWN;
   if (L.pair) {
-    // two weight slabs per CTA where the pair feature blocks divide evenly, else one
-    const bool even = (L.num_mblocks % (2 * (L.epi == EPI_SWIGLU ? MOE_G1_NP : MOE_G2_NP))) == 0;
-    if (L.epi == EPI_SWIGLU && kernel_tn == TNP && L.b_gather_x != nullptr) {
-      if (MOE_G1_MB == 2 && even)
-        return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, 1, 2, true>(L, p, s);
-      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, 1, 1, true>(L, p, s);
-    }
-    if (L.epi == EPI_SWIGLU && kernel_tn == TNP) {
-      if (MOE_G1_MB == 2 && even)
-        return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, MOE_G1_NP, 2>(L, p, s);
-      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM, MOE_G1_NP, 1>(L, p, s);
-    }
-    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == TN2 && L.mblk == 2) {
-      if (MOE_G2_MB == 2 && even)
-        return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM, MOE_G2_NP, 2>(L, p, s);
-      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM, MOE_G2_NP, 1>(L, p, s);
-    }
+    if (L.epi == EPI_SWIGLU && kernel_tn == TNP)
+      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM>(L, p, s);
+    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == TN2 && L.mblk == 2)
+      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM>(L, p, s);
     return cudaErrorInvalidValue;
   }
   if (L.epi == EPI_SWIGLU) {

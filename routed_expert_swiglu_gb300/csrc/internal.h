@@ -44,34 +44,10 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 #ifndef MOE_PAIR_TMEM
 #define MOE_PAIR_TMEM 512
 #endif
-// 128-row weight slabs per CTA of the pair GEMMs (1 or 2; 2 fills all 512 TMEM columns with one
-// accumulator buffer)
-#ifndef MOE_G1_MB
-#define MOE_G1_MB 1
-#endif
-#ifndef MOE_G2_MB
-#define MOE_G2_MB 1
-#endif
 // Upper bound on the resident clusters a pair GEMM launches (0: as many as fit).
 #ifndef MOE_PAIR_MAX_CLUSTERS
 #define MOE_PAIR_MAX_CLUSTERS 0
 #endif
-// CTA pairs per cluster of the prefill GEMMs (2: token rows multicast between the pairs).
-#ifndef MOE_G1_NP
-#define MOE_G1_NP 1
-#endif
-#ifndef MOE_G2_NP
-#define MOE_G2_NP 1
-#endif
-
-// 1: the prefill gate/up GEMM gathers its token rows from x itself (cp.async by the permuted
-// token ids) instead of reading the dispatched copy by TMA.  Off: on GB300 the cp.async row
-// copies land ~11 GB/s per SM, and the gate/up GEMM of the V4-Flash T=8192 layer takes 4.3 ms
-// instead of 1.64 ms, far more than the 0.09 ms gather launch it saves.
-#ifndef MOE_G1_GATHER
-#define MOE_G1_GATHER 0
-#endif
-
 // 1: FP8 expert weights run the kernels that feed the E4M3 codes straight to the tensor cores
 // (tcgen05 kind::f8f6f4, activations split into E4M3 pieces) where the shapes allow it
 // (d and d_ff multiples of 128); 0: always the kernels that widen the codes to bf16 first.
@@ -100,10 +76,6 @@ inline int fp8_token_tile(int T, int k, int E) {
   const long long rows = (long long)T * k;
   return rows <= 8LL * E ? 16 : rows <= 24LL * E ? 32 : 64;
 }
-
-// True when a batch of T tokens runs the gate/up GEMM with fused row gathering (no
-// dispatched-row buffer, no gather launch).
-inline bool gate_up_gathers(int T) { return !is_decode(T) && MOE_G1_PAIR && MOE_G1_GATHER; }
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -134,9 +106,6 @@ struct GemmLaunch {
   const void* a_sh_ptr; int64_t a_sh_rows;
   const void* b_ptr; int64_t b_rows;
   const void* b_sh_ptr; int64_t b_sh_rows;
-  // gathered B (pair gate/up only): routed row r of a group reads row b_gather_idx[r] of
-  // b_gather_x ([*, K] bf16); b_ptr is then unused
-  const void* b_gather_x; const int32_t* b_gather_idx;
   // FP8 weights (q8 = 1): a_ptr / a_sh_ptr hold E4M3 codes and a_exp / a_sh_exp the int8
   // exponents of their 128 x 128 tiles ([mats, ceil(rows/128), ceil(K/128)])
   int q8; const int8_t* a_exp; const int8_t* a_sh_exp;

@@ -75,7 +75,7 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.inv = take((size_t)L.N * 4);
   L.row_w = take((size_t)L.N * 4);
   // dispatched rows (bf16), or with FP8 weights the routed and shared rows as two E4M3 pieces
-  L.xd = take(gate_up_gathers(T) ? 0 : rows_h * d * 2);
+  L.xd = take(rows_h * d * 2);
   L.xexp = take(rows_h * 4);
   L.h = take(rows_h * 2 * f * 2);  // hi/lo bf16 pair per activation (FP8 weights: fp32, then 4 pieces)
   L.hexp = take(rows_h * 4);
@@ -286,12 +286,10 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   pm.inv = at<int32_t>(ws, L.inv);
   pm.row_w = at<float>(ws, L.row_w);
   pm.err = err;
-  const bool fused_gather = gate_up_gathers(T);
-  if (fused_gather && q8 != nullptr) return MOE_ERR_UNSUPPORTED;  // the FP8 kernels read dispatched rows
   // FP8 weights straight into the MMA: the activation rows go in as E4M3 pieces (the gather
   // from x builds them, so the dispatch copies no rows)
   pm.x = x;
-  pm.xd = (fused_gather || f8mma) ? nullptr : at<void>(ws, L.xd);
+  pm.xd = f8mma ? nullptr : at<void>(ws, L.xd);
   pm.d = d;
   pm.num_sms = sms;
   MOE_CUDA(launch_permute(pm, s));
@@ -311,10 +309,6 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.a_sh_rows = 2 * f;
   g1.b_ptr = pm.xd;
   g1.b_rows = L.N;
-  if (fused_gather) {
-    g1.b_gather_x = x;
-    g1.b_gather_idx = pm.perm_tok;
-  }
   g1.b_sh_ptr = sh ? x : nullptr;
   g1.b_sh_rows = T;
   g1.K = d;
@@ -747,7 +741,7 @@ moe_status moe_plan_set_events(moe_plan* plan, moe_event_t* events, int32_t n_ev
 
 int32_t moe_forward_launch_count(const moe_plan* plan, int32_t T) {
   if (plan == nullptr || T <= 0) return 0;
-  return 2 /* router GEMM, top-k */ + permute_launch_count(!gate_up_gathers(T)) + 2 /* grouped GEMMs */ +
+  return 2 /* router GEMM, top-k */ + permute_launch_count(true) + 2 /* grouped GEMMs */ +
          1 /* combine */;
 }
 

@@ -12,6 +12,8 @@
 //
 // The array is shared by every call on a device and keeps the last call's contents; the
 // entry point clears the one word that must start at zero (the error word) on every call.
+// An expert id outside [0, E) is clamped into range (as moe_permute does) and flagged in that
+// word, which moe_permute_noalloc_status reads back.
 // Two calls whose work overlaps on the GPU (different streams, no ordering between them)
 // race on the array.  The first call on a device looks up the array's device address
 // (cudaGetSymbolAddress, once per device, with that device current); make that first call
@@ -33,7 +35,9 @@ namespace {
 constexpr int NOALLOC_MAX_ASSIGN = 131072;
 constexpr int NOALLOC_MAX_BLOCKS = NOALLOC_MAX_ASSIGN / PERMUTE_CHUNK;
 constexpr int NOALLOC_MAX_GROUPS = MAX_EXPERTS + 1;  // routed + shared
-// row tiles of the schedule: at most E + ceil(N / 64) + ceil(T / 64) + 1 with T <= N
+// row tiles of the schedule: at most E + ceil(N / 64) + ceil(T / 64) + 1 with T <= N, for the
+// schedule's row tiles of token_tile_for(T) >= 64 rows
+static_assert(MOE_TN_PREFILL >= 64, "the fixed scratch is sized for row tiles of at least 64 rows");
 constexpr int NOALLOC_MAX_ROWTILES = MAX_EXPERTS + 2 * (NOALLOC_MAX_ASSIGN / 64) + 2;
 
 constexpr size_t OFF_ERR = 0;
@@ -112,4 +116,22 @@ extern "C" moe_status moe_permute_noalloc(moe_plan* plan, int32_t T, const int32
   pm.num_sms = sms;
   if (launch_permute(pm, s) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" moe_status moe_permute_noalloc_status(moe_stream_t stream) {
+  using namespace moe;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= MAX_DEVICES) return MOE_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    scratch = g_scratch_ptr[dev];
+  }
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (scratch == nullptr) return MOE_OK;  // no call on this device yet: nothing flagged
+  int v = 0;
+  if (cudaMemcpy(&v, static_cast<char*>(scratch) + OFF_ERR, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return v != 0 ? MOE_ERR_DEVICE_INPUT : MOE_OK;
 }

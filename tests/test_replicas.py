@@ -57,3 +57,21 @@ def test_two_rank_harness():
     assert [m for _, m, _ in res] == [15.0, 15.0]          # max over ranks on every rank
     assert '"impl": "reference"' in res[0][2]             # rank 0 prints the reference line
     assert res[1][2] == ""                                # rank 1 exits without work
+
+
+def test_gpus_flag_spawns_the_ranks():
+    """`bench.py --gpus 2` with no launcher environment starts its two rank processes itself
+    (gloo on this CPU-only host) and rank 0 prints one line for the whole job."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR",
+                                                           "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                          "--workload", "toy_T64", "--steps", "1", "--warmup", "3", "--ref-tokens", "2"],
+                         capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2
