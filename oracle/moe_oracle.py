@@ -28,8 +28,8 @@ What the layer computes (source pages, by title and section):
     communication", section 七.3; "DeepSeek-V4 MoE", section "负载均衡为什么要 Auxiliary-Loss-Free".
 
 Readings where the pages are silent (each is listed with its reason in the design notes):
-  * Selection keys are compared in fp32 (the kernel's precision), ties go to the lower
-    expert id, and the k ids are returned in descending key order.
+  * Selection keys and group scores are compared in fp64 (like every other step here), ties
+    go to the lower expert (group) id, and the k ids are returned in descending key order.
   * The expert FFN is the plain definition, with no rounding of the activation h between the
     two projections (the layer definition on "MoE compute and communication", sec. 二.1/二.2,
     has none; the FP8 re-quantisation in the "DeepSeek-V4 MoE" stage table belongs to that
@@ -101,19 +101,48 @@ def affinity(logits, score):
 
 # ----------------------------------------------------------------------------- selection
 
-def _topk_desc(keys32, k):
-    """Indices of the k largest fp32 keys per row, descending; equal keys -> lower index
-    first (a stable sort of the negated keys)."""
-    order = np.argsort(-keys32, axis=1, kind="stable")
+def _topk_desc(keys, k):
+    """Indices of the k largest keys per row, descending; equal keys -> lower index first (a
+    stable sort of the negated keys)."""
+    order = np.argsort(-keys, axis=1, kind="stable")
     return order[:, :k]
 
 
-def _fp32_sum_sequential(vals32):
-    """Left-to-right fp32 sum along the last axis (the order the values are given in)."""
-    acc = vals32[..., 0].astype(np.float32)
-    for j in range(1, vals32.shape[-1]):
-        acc = (acc + vals32[..., j]).astype(np.float32)
+def selection_keys(logits, score, bias=None):
+    """Key q[t, e] that top-k ranks: the raw logit for softmax_topk, else the unbiased score
+    plus the selection bias (0 when None).  "MoE compute and communication", section 七.3:
+    the bias shifts the choice only."""
+    logits = np.asarray(logits, np.float64)
+    s = affinity(logits, score)
+    base = logits if s is None else s
+    return base + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
+
+
+def group_scores(keys, n_groups, group_topk):
+    """Score of each contiguous group of E / n_groups experts: the sum of its group_topk
+    largest keys, added largest first ("DeepSeek-V4 MoE", section "V3 的节点路由约束")."""
+    keys = np.asarray(keys, np.float64)
+    T, E = keys.shape
+    top = -np.sort(-keys.reshape(T, n_groups, E // n_groups), axis=2)[:, :, :group_topk]
+    acc = top[..., 0].copy()
+    for j in range(1, group_topk):
+        acc = acc + top[..., j]
     return acc
+
+
+def gate_weights(logits, ids, score):
+    """Gate weights of the selected experts ids [T, k]: the softmax of the k selected logits
+    (softmax_topk), else the unbiased scores of the selected experts renormalised to sum 1
+    (denominator clamped to DENOM_MIN).  For "softmax" the score is the softmax over all E, so
+    this is its renormalisation over the k."""
+    logits = np.asarray(logits, np.float64)
+    ids = np.asarray(ids, np.int64)
+    rows = np.arange(logits.shape[0])[:, None]
+    s = affinity(logits, score)
+    if s is None:
+        return softmax(logits[rows, ids], axis=1)
+    sel = s[rows, ids]
+    return sel / np.maximum(sel.sum(axis=1, keepdims=True), DENOM_MIN)
 
 
 def route(logits, k, score, bias=None, n_groups=0, topk_groups=0, group_topk=0,
@@ -129,46 +158,35 @@ def route(logits, k, score, bias=None, n_groups=0, topk_groups=0, group_topk=0,
     """
     logits = np.asarray(logits, np.float64)
     T, E = logits.shape
-    s = affinity(logits, score)
     order_margin = np.full(T, np.inf)
+    margin = np.full(T, np.inf)
     if tid2eid is not None:
         # HashTopK: ids looked up by token id, in table order; no comparison decides them.
         ids = np.asarray(tid2eid)[np.asarray(token_ids, np.int64)].astype(np.int32)
-        margin = np.full(T, np.inf)
     else:
-        base = logits if s is None else s
-        key = base + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
-        key32 = key.astype(np.float32)
-        margin = np.full(T, np.inf)
+        key = selection_keys(logits, score, bias)
         if n_groups:
             gsize = E // n_groups
-            kg = key32.reshape(T, n_groups, gsize)
-            top_in_group = -np.sort(-kg, axis=2)[:, :, :group_topk]
-            gscore = _fp32_sum_sequential(top_in_group)                  # [T, G] fp32
+            gscore = group_scores(key, n_groups, group_topk)                # [T, G]
             gorder = np.argsort(-gscore, axis=1, kind="stable")
             keep = gorder[:, :topk_groups]
             if topk_groups < n_groups:
-                gs_sorted = np.take_along_axis(gscore, gorder, axis=1).astype(np.float64)
+                gs_sorted = np.take_along_axis(gscore, gorder, axis=1)
                 margin = np.minimum(margin, gs_sorted[:, topk_groups - 1] - gs_sorted[:, topk_groups])
             group_mask = np.zeros((T, n_groups), bool)
             np.put_along_axis(group_mask, keep, True, axis=1)
             expert_mask = np.repeat(group_mask, gsize, axis=1)
-            key32 = np.where(expert_mask, key32, np.float32(-np.inf))
-        ids = _topk_desc(key32, k).astype(np.int32)
-        sel_keys = np.take_along_axis(key32, ids.astype(np.int64), axis=1).astype(np.float64)
+            key = np.where(expert_mask, key, -np.inf)
+        ids = _topk_desc(key, k).astype(np.int32)
+        sel_keys = np.take_along_axis(key, ids.astype(np.int64), axis=1)
         if k > 1:
             order_margin = np.min(sel_keys[:, :-1] - sel_keys[:, 1:], axis=1)
         if k < E:
-            ks = -np.sort(-key32, axis=1)
-            kth, nxt = ks[:, k - 1].astype(np.float64), ks[:, k].astype(np.float64)
+            ks = -np.sort(-key, axis=1)
+            kth, nxt = ks[:, k - 1], ks[:, k]
             gap = np.where(np.isfinite(nxt), kth - nxt, np.inf)
             margin = np.minimum(margin, gap)
-    rows = np.arange(T)[:, None]
-    if s is None:  # softmax over the k selected logits
-        w = softmax(logits[rows, ids], axis=1)
-    else:
-        sel = s[rows, ids]
-        w = sel / np.maximum(sel.sum(axis=1, keepdims=True), DENOM_MIN)
+    w = gate_weights(logits, ids, score)
     if return_order_margin:
         return ids, w, margin, order_margin
     return ids, w, margin

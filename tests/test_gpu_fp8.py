@@ -14,7 +14,7 @@ import oracle
 from oracle import fp8_weights as F
 from routed_expert_swiglu_gb300 import binding, inputs, workloads as W
 
-from parity_util import check_output, check_routing, oracle_route, to64
+from parity_util import check_output, check_routing, oracle_routing, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -94,11 +94,12 @@ def test_fp8_layer_vs_oracle(w):
     y = layer.forward_fp8(inp.x, q, inp.token_ids)
     assert layer.check_status() == 0
     v = layer.views(w.T)
-    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
-    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    gids = v["topk_ids"].cpu().numpy()
+    ref_w, _ = check_routing(w, gids, v["topk_w"].cpu().numpy(), oracle_routing(w, inp))
+    same = np.ones(w.T, bool)  # every token: the oracle is fed the GPU's ids
     fetch = OracleFp8Fetcher(inp)
     tok = np.nonzero(same)[0]
-    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    ref = oracle.forward(to64(inp.x), gids, ref_w, fetch, fetch.shared(), tokens=tok)
     e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
     print(f"{w.name} (fp8 weights): max elementwise {e:.2e}, normwise {n:.2e}")
     layer.close()
@@ -124,11 +125,12 @@ def test_fp8_layer_with_zero_subnormal_and_tiny_scale_codes():
     y = layer.forward_fp8(inp.x, q, None)
     assert layer.check_status() == 0
     v = layer.views(w.T)
-    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
-    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    gids = v["topk_ids"].cpu().numpy()
+    ref_w, _ = check_routing(w, gids, v["topk_w"].cpu().numpy(), oracle_routing(w, inp))
+    same = np.ones(w.T, bool)  # every token: the oracle is fed the GPU's ids
     fetch = OracleFp8Fetcher(inp)
     tok = np.nonzero(same)[0]
-    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    ref = oracle.forward(to64(inp.x), gids, ref_w, fetch, fetch.shared(), tokens=tok)
     check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
     layer.close()
 
@@ -151,11 +153,12 @@ def test_fp8_layer_with_wide_activation_range():
     y = layer.forward_fp8(inp.x, q, None)
     assert layer.check_status() == 0
     v = layer.views(w.T)
-    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
-    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    gids = v["topk_ids"].cpu().numpy()
+    ref_w, _ = check_routing(w, gids, v["topk_w"].cpu().numpy(), oracle_routing(w, inp))
+    same = np.ones(w.T, bool)  # every token: the oracle is fed the GPU's ids
     fetch = OracleFp8Fetcher(inp)
     tok = np.nonzero(same)[0]
-    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    ref = oracle.forward(to64(inp.x), gids, ref_w, fetch, fetch.shared(), tokens=tok)
     got = y.double().cpu().numpy()[tok]
     e, n = check_output(got, ref, label=w.name)
     print(f"{w.name} (fp8 weights): max elementwise {e:.2e}, normwise {n:.2e}")
@@ -179,13 +182,14 @@ def test_fp8_full_size_layer(w, sample):
     y = layer.forward_fp8(inp.x, q, inp.token_ids)
     assert layer.check_status() == 0
     v = layer.views(w.T)
-    _, rids, rw, margin, om = oracle_route(w, inp, with_order=True)
-    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, om)
+    gids = v["topk_ids"].cpu().numpy()
+    ref_w, _ = check_routing(w, gids, v["topk_w"].cpu().numpy(), oracle_routing(w, inp))
+    same = np.ones(w.T, bool)  # every token: the oracle is fed the GPU's ids
     rng = np.random.default_rng(4321)
     cand = np.nonzero(same)[0]
     tok = np.sort(rng.choice(cand, size=min(sample, cand.size), replace=False))
     fetch = OracleFp8Fetcher(inp)
-    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
+    ref = oracle.forward(to64(inp.x), gids, ref_w, fetch, fetch.shared(), tokens=tok)
     e, n = check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
     print(f"{w.name} full size (fp8 weights), sample of {tok.size}: max elementwise {e:.2e}, normwise {n:.2e}")
     layer.close()

@@ -8,7 +8,8 @@ import torch
 import oracle
 from routed_expert_swiglu_gb300 import binding, inputs, workloads as W
 
-from parity_util import (ExpertFetcher, check_output, check_routing, oracle_route, to64)
+from parity_util import (ExpertFetcher, check_output, check_routing, oracle_output, oracle_route,
+                         oracle_routing, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,14 +50,14 @@ def test_router_logits_and_routing(w):
     layer = binding.MoELayer(w, inp)
     ids, wts, logits = layer.route(inp.x, inp.token_ids, with_logits=True)
     assert layer.check_status() == 0
-    ref_logits, rids, rw, margin, omargin = oracle_route(w, inp, with_order=True)
+    R = oracle_routing(w, inp)
     # fp32 accumulation of d bf16 products: error bounded by a few ulps of sum |x_i w_i|
     bound = np.abs(to64(inp.x)) @ np.abs(to64(inp.w_r)).T
-    err = np.abs(logits.double().cpu().numpy() - ref_logits)
+    err = np.abs(logits.double().cpu().numpy() - R.logits)
     assert (err <= 1e-5 * bound + 1e-6).all(), f"logit error {(err / (bound + 1e-6)).max():.3e} of sum|xw|"
-    same = check_routing(w, ids.cpu().numpy(), wts.cpu().numpy(), rids, rw, margin, omargin)
-    print(f"{w.name}: {int((~same).sum())} tokens inside the margin routed differently; "
-          f"{int((margin <= 1e-3).sum())} tokens within margin")
+    _, moved = check_routing(w, ids.cpu().numpy(), wts.cpu().numpy(), R)
+    print(f"{w.name}: {moved} tokens inside the margin routed differently; "
+          f"{int((R.margin <= 1e-3).sum())} tokens within margin")
     layer.close()
 
 
@@ -128,12 +129,9 @@ def test_forward_vs_oracle(w):
     y = layer.forward(inp.x, inp.token_ids)
     assert layer.check_status() == 0
     v = layer.views(w.T)
-    _, rids, rw, margin, omargin = oracle_route(w, inp, with_order=True)
-    same = check_routing(w, v["topk_ids"].cpu().numpy(), v["topk_w"].cpu().numpy(), rids, rw, margin, omargin)
-    fetch = ExpertFetcher(inp)
-    tok = np.nonzero(same)[0]
-    ref = oracle.forward(to64(inp.x), rids, rw, fetch, fetch.shared(), tokens=tok)
-    check_output(y.double().cpu().numpy()[tok], ref, label=w.name)
+    gids = v["topk_ids"].cpu().numpy()
+    ref_w, _ = check_routing(w, gids, v["topk_w"].cpu().numpy(), oracle_routing(w, inp))
+    check_output(y.double().cpu().numpy(), oracle_output(inp, gids, ref_w), label=w.name)
     layer.close()
 
 

@@ -158,7 +158,7 @@ def test_group_limited_brute_force_tiny():
         logits = rng.normal(size=(1, E))
         bias = rng.normal(size=E) * 0.3
         ids, _, _ = oracle.route(logits, k, "sigmoid", bias=bias, n_groups=G, topk_groups=M, group_topk=gt)
-        key = (scipy.special.expit(logits[0]) + bias).astype(np.float32).astype(np.float64)
+        key = scipy.special.expit(logits[0]) + bias
         gscore = [sum(sorted(key[g * gsz:(g + 1) * gsz])[-gt:]) for g in range(G)]
         best_groups = max(itertools.combinations(range(G), M), key=lambda S: sum(gscore[g] for g in S))
         cand = [e for g in best_groups for e in range(g * gsz, (g + 1) * gsz)]
@@ -173,7 +173,7 @@ def test_group_limited_invariants_v3_shape():
     logits = rng.normal(size=(T, E)) * 1.3
     bias = rng.normal(size=E) * 0.01
     ids, w, margin = oracle.route(logits, k, "sigmoid", bias=bias, n_groups=G, topk_groups=M, group_topk=2)
-    key = (oracle.sigmoid(logits) + bias).astype(np.float32)
+    key = oracle.sigmoid(logits) + bias
     for t in range(T):
         groups = set(int(e) // (E // G) for e in ids[t])
         assert len(groups) <= M                         # spans at most M groups
@@ -388,3 +388,39 @@ def test_bias_update_moves_selection_towards_balance():
             spread0 = counts.max() - counts.min()
         bias = oracle.bias_update(counts, bias, T * k, gamma=0.01)
     assert counts.max() - counts.min() < spread0 / 2
+
+
+# ----------------------------------------------------------------------------- selection helpers
+
+def test_gate_weights_of_given_ids_on_the_worked_example():
+    """Router page, "Router 的选择过程": experts {3, 0} of the printed scores get 0.7109 / 0.2891
+    whichever order they are listed in, and in softmax-over-all mode the same after renormalising."""
+    g = golden("router_worked_example.json")
+    logits = np.array([g["scores"]])
+    p3 = 1.0 / (1.0 + math.exp(-(2.1 - 1.2)))
+    for mode in ("softmax_topk", "softmax"):
+        w = oracle.gate_weights(logits, np.array([[3, 0]]), mode)
+        np.testing.assert_allclose(w[0], g["printed_weights"], atol=g["printed_precision"])
+        np.testing.assert_allclose(w[0], [p3, 1.0 - p3], rtol=1e-13)
+        w_rev = oracle.gate_weights(logits, np.array([[0, 3]]), mode)
+        np.testing.assert_allclose(w_rev[0], [1.0 - p3, p3], rtol=1e-13)
+
+
+def test_group_scores_brute_force():
+    """Sum of the group_topk largest keys of each contiguous group, against a loop over groups."""
+    rng = np.random.default_rng(11)
+    keys = rng.normal(size=(5, 24))
+    for G, gt in ((4, 2), (3, 3), (8, 1)):
+        got = oracle.group_scores(keys, G, gt)
+        gsz = 24 // G
+        for t in range(5):
+            for g in range(G):
+                assert got[t, g] == pytest.approx(sum(sorted(keys[t, g * gsz:(g + 1) * gsz])[-gt:]), abs=1e-12)
+
+
+def test_selection_keys_add_the_bias_to_the_unbiased_score():
+    rng = np.random.default_rng(12)
+    logits, bias = rng.normal(size=(3, 6)), rng.normal(size=6)
+    np.testing.assert_array_equal(oracle.selection_keys(logits, "softmax_topk"), logits)
+    np.testing.assert_allclose(oracle.selection_keys(logits, "sigmoid", bias),
+                               scipy.special.expit(logits) + bias, rtol=1e-15)
