@@ -424,3 +424,24 @@ def test_selection_keys_add_the_bias_to_the_unbiased_score():
     np.testing.assert_array_equal(oracle.selection_keys(logits, "softmax_topk"), logits)
     np.testing.assert_allclose(oracle.selection_keys(logits, "sigmoid", bias),
                                scipy.special.expit(logits) + bias, rtol=1e-15)
+
+
+def test_a_single_bf16_activation_misses_the_output_tolerance():
+    """Why the down projection carries h as a (hi, lo) pair of bf16 values: on a V4-Flash-shaped
+    layer (d=4096, d_ff=2048, one shared expert), rounding h once to bf16 between the two
+    projections ("MoE compute and communication", sec. 二.1: FFN = W2(SiLU(W1 x) * W3 x), no such
+    rounding) moves outputs near zero far beyond max|err| / (|y| + 1e-2) <= 2e-2, while the exact
+    h with only the bf16 rounding of y meets it."""
+    import dataclasses
+    from routed_expert_swiglu_gb300 import inputs, workloads as W
+    w = dataclasses.replace(W.V4FLASH_T8192, T=64, E=8, name="v4flash_E8_T64")
+    inp = inputs.make_layer_inputs(w, seed=0, device="cpu")
+    f64 = lambda t: t.double().numpy()  # noqa: E731
+    x = f64(inp.x)
+    ids, wts, _ = oracle.route(oracle.router_logits(x, f64(inp.w_r)), w.k, w.score, bias=f64(inp.bias))
+    fetch = lambda e: (f64(inp.w13[e]), f64(inp.w2[e]))  # noqa: E731
+    sh = (f64(inp.w13_sh), f64(inp.w2_sh))
+    ref = oracle.forward(x, ids, wts, fetch, sh)
+    elem = lambda y: (np.abs(y - ref) / (np.abs(ref) + 1e-2)).max()  # noqa: E731
+    assert elem(oracle.round_to_bf16(oracle.forward(x, ids, wts, fetch, sh, cast_h=True))) > 0.1
+    assert elem(oracle.round_to_bf16(ref)) < 5e-3
