@@ -5,7 +5,8 @@
 One step = one whole layer forward (router GEMM, top-k, dispatch, gate/up grouped GEMM, down
 grouped GEMM, combine) over one batch of T synthetic tokens whose inputs are resident in HBM.
 Default workload: the DeepSeek-V4-Flash-shaped layer at T=8192 (prefill); the same line
-carries a T=64 (decode) measurement under "decode", with the same layer on FP8 expert weights
+carries the same layer with Zipf-skewed routing under "skewed", and a T=64 (decode)
+measurement under "decode", with the same layer on FP8 expert weights
 ("fp8_weights") and on MXFP4 expert weights ("mxfp4_weights": the one-time conversion to the FP8
 form, the forward on the converted tiles, and the native forward that streams the 4-bit codes).
 Multi-GPU runs are independent replicas (one process per GPU, each with its own token batch; no
@@ -392,6 +393,24 @@ def run_ours(args, world, rank, local):
     del layer, inp
     torch.cuda.empty_cache()
 
+    skewed = None
+    if args.skew_workload not in ("none", args.workload):
+        ws = workloads.BY_NAME[args.skew_workload]
+        sl, sinp, sms_, sstage, sactive, _ = measure_workload(ws, max(args.steps // 2, 5), args.warmup, device,
+                                                              seed=rank, world=world, rank=rank)
+        sms_ = max_over_ranks(sms_, world) / max(args.steps // 2, 5)
+        s_roof = cost.roofline_seconds(cost.layer_flops(ws), cost.layer_bytes(ws, sactive),
+                                       float(peaks["bf16_tflops_sustained"]), hbm_peak)
+        counts = sl.views(ws.T)["counts"].cpu().numpy()
+        skewed = {"workload": ws.name, "T": ws.T, "ms_per_step": round(sms_, 4),
+                  "tokens_per_s": round(world * ws.T / (sms_ / 1e3), 1), "active_experts": sactive,
+                  "rows_hottest_expert": int(counts.max()), "rows_median_expert": int(np.median(counts)),
+                  "layer_roofline_ms": round(s_roof * 1e3, 4), "layer_roofline_frac": round(s_roof * 1e3 / sms_, 4),
+                  "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, sstage)}}
+        sl.close()
+        del sl, sinp
+        torch.cuda.empty_cache()
+
     decode = None
     if args.decode_workload not in ("none", args.workload):
         wd = workloads.BY_NAME[args.decode_workload]
@@ -446,6 +465,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "decode": decode,
+        "skewed": skewed,
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -548,6 +568,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v4flash_T8192", choices=sorted(workloads.BY_NAME))
     ap.add_argument("--decode-workload", default="v4flash_T64", help="second (decode) workload, or none")
+    ap.add_argument("--skew-workload", default="v4flash_zipf_T8192",
+                    help="the same layer with Zipf-skewed routing, timed alongside (or none)")
     ap.add_argument("--cpu-tokens", type=int, default=8192,
                     help="tokens of the workload the CPU-baseline oracle runs, at most T (the whole "
                          "V4-Flash T=8192 batch: about 10 s on 16 Grace cores)")

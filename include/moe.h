@@ -42,7 +42,9 @@
  *     tid2eid entry or topk id outside [0, E)) is clamped into range, computed, and flagged
  *     in the workspace error word; moe_check_status() reports it as MOE_ERR_DEVICE_INPUT.
  *     A kernel whose internal pipeline wait exceeds ~2 s stops, flags MOE_ERR_TIMEOUT in the
- *     same word and returns (no GPU trap).
+ *     same word and returns (no GPU trap).  A library built with MOE_DEBUG_BOUNDS=1 also checks
+ *     the internal row indices of the dispatch, the grouped GEMMs' stores and the combine;
+ *     a failed check skips that access and is reported as MOE_ERR_INTERNAL.
  *   - T = 0 is valid and enqueues nothing.
  */
 #ifndef MOE_GB300_H
@@ -68,7 +70,9 @@ typedef enum {
   MOE_ERR_WORKSPACE = 4,    /* ws_bytes < moe_workspace_bytes(plan, T)                    */
   MOE_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed             */
   MOE_ERR_DEVICE_INPUT = 6, /* device data out of range (clamped); from moe_check_status */
-  MOE_ERR_TIMEOUT = 7       /* a kernel pipeline wait timed out; from moe_check_status   */
+  MOE_ERR_TIMEOUT = 7,      /* a kernel pipeline wait timed out; from moe_check_status   */
+  MOE_ERR_INTERNAL = 8      /* an internal index check failed (library built with
+                               MOE_DEBUG_BOUNDS=1 only); from moe_check_status           */
 } moe_status;
 
 typedef enum {
@@ -270,7 +274,8 @@ moe_status moe_forward_host(moe_plan* plan, int32_t T, const moe_bf16* x_host,
                             void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronise `stream` and read the workspace error word written by the last call that used
- * `ws`: MOE_OK, MOE_ERR_DEVICE_INPUT (clamped bad ids) or MOE_ERR_TIMEOUT. */
+ * `ws`: MOE_OK, MOE_ERR_DEVICE_INPUT (clamped bad ids), MOE_ERR_TIMEOUT, or (debug-bounds
+ * builds) MOE_ERR_INTERNAL; a timeout takes precedence, then an internal check. */
 moe_status moe_check_status(moe_plan* plan, const void* ws, moe_stream_t stream);
 
 /* Device addresses, inside `ws`, of the intermediates of the last forward with T tokens.

@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
-                4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_INPUT", 7: "MOE_ERR_TIMEOUT"}
+                4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_INPUT", 7: "MOE_ERR_TIMEOUT",
+                8: "MOE_ERR_INTERNAL"}
 SCORE_CODES = {W.SCORE_SOFTMAX_TOPK: 0, W.SCORE_SOFTMAX: 1, W.SCORE_SIGMOID: 2, W.SCORE_SQRT_SOFTPLUS: 3}
 
 # Every symbol include/moe.h declares.

@@ -10,16 +10,22 @@
 namespace moe {
 
 __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__ o, const int32_t* __restrict__ inv,
-                                                      int k, int d4, int N, int n_shared, uint2* __restrict__ out) {
+                                                      int k, int d4, int N, int n_shared, uint2* __restrict__ out,
+                                                      int T, int* err) {
   __shared__ int rows[MAX_TOPK + 1];
   const int t = blockIdx.x;
-  if (threadIdx.x < k) rows[threadIdx.x] = __ldg(inv + (size_t)t * k + threadIdx.x);
+  if (threadIdx.x < k) {
+    const int r = __ldg(inv + (size_t)t * k + threadIdx.x);
+    // debug-bounds builds: a routed row outside [0, N) is reported and left out of the sum
+    rows[threadIdx.x] = bad_index(r, N, err) ? -1 : r;
+  }
   if (threadIdx.x == 0 && n_shared) rows[k] = N + t;
   __syncthreads();
   const int nr = k + n_shared;
   for (int c = threadIdx.x; c < d4; c += blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < nr; ++j) {
+      if (MOE_DEBUG_BOUNDS && rows[j] < 0) continue;
       const float4 v = __ldg(o + (size_t)rows[j] * d4 + c);
       acc.x += v.x;
       acc.y += v.y;
@@ -38,7 +44,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float4* __restrict__
 cudaError_t launch_combine(const CombineLaunch& L, cudaStream_t s) {
   const int d4 = L.d / 4;
   combine_kernel<<<L.T, 256, 0, s>>>(static_cast<const float4*>(static_cast<const void*>(L.o)), L.inv, L.k, d4, L.N,
-                                     L.n_shared, static_cast<uint2*>(L.out));
+                                     L.n_shared, static_cast<uint2*>(L.out), L.T, L.err);
   return cudaGetLastError();
 }
 

@@ -15,9 +15,37 @@ enum : int {
   DEVERR_TID2EID = 2,      // tid2eid entry outside [0, E) (clamped)
   DEVERR_TOPK_ID = 4,      // topk id outside [0, E) (clamped)
   DEVERR_TIMEOUT = 8,      // a pipeline wait exceeded its limit; the kernel stopped early
+  DEVERR_BOUNDS = 16,      // (MOE_DEBUG_BOUNDS builds) an internal row index out of range; skipped
 };
 
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+// MOE_DEBUG_BOUNDS=1 builds check internal row indices before they are used to address memory
+// (dispatch rows, grouped-GEMM output rows, combine rows).  A failed check records DEVERR_BOUNDS
+// in the error word and the access is skipped.  Default builds compile the checks away.
+#ifndef MOE_DEBUG_BOUNDS
+#define MOE_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool bad_index(long long i, long long n, int* err) {
+#if MOE_DEBUG_BOUNDS
+  if (i < 0 || i >= n) {
+    if (err != nullptr) atomicOr(err, DEVERR_BOUNDS);
+    return true;
+  }
+#endif
+  return false;
+}
+
+// Longest a pipeline wait may last before the kernel gives up (2 s; a build may set it lower).
+#ifndef MOE_WAIT_LIMIT_NS
+#define MOE_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr unsigned long long WAIT_LIMIT_NS = MOE_WAIT_LIMIT_NS;
+
+// Quiet period before a CTA that gave up a wait releases its shared memory and Tensor Memory.
+// When a role stops early, asynchronous operations issued before (TMA loads into this CTA's
+// shared memory, by this CTA or its pair peer; tensor-core MMAs reading it and writing Tensor
+// Memory; the mbarrier arrivals of their commits) may still be completing.  None of them waits
+// on anything once issued, and each completes within microseconds; 1 ms lets them all land.
+constexpr unsigned long long QUIET_NS = 1000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -93,6 +121,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         return false;
       }
     }
+  }
+}
+
+// End of a warp-specialised kernel, called by every thread after its role's loop: a CTA barrier,
+// then, if any role of this CTA gave up a wait, the quiet period (one thread sleeps, the others
+// wait at a second barrier).  After the first barrier no role writes the flag any more, so every
+// thread takes the same branch.
+__device__ __forceinline__ void sync_and_quiesce(volatile int* abort_flag) {
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      const unsigned long long t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < QUIET_NS) __nanosleep(1000);
+    }
+    __syncthreads();
   }
 }
 

@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(Fp8Shape<EPI, TN, MBLK, HILO>::THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  sync_and_quiesce(abort_flag);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, S::TMEM_COLS);
@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  sync_and_quiesce(abort_flag);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  sync_and_quiesce(abort_flag);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);

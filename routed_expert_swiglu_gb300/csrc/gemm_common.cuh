@@ -28,6 +28,7 @@ struct GemmParams {
   int a_up_offset;      // SwiGLU: row offset of the up rows (W3) after the gate rows (W1)
   int out_features;
   int out_ld;
+  int out_rows;         // rows of `out` (per K slice), checked in debug-bounds builds; 0 = unchecked
   void* out;
   const float* row_scale;
   int n_routed;
@@ -120,9 +121,10 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, const GemmParams& p
       tmem_ld_wait();
       reg_fence16(rg);
       reg_fence16(ru);
-      if (fvalid) {
+      const int nr = min(16, t.rows - c0);
+      if (fvalid && !(p.out_rows > 0 && (bad_index(t.out_row + c0, p.out_rows, p.err) ||
+                                         bad_index(t.out_row + c0 + nr - 1, p.out_rows, p.err)))) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
-        const int nr = min(16, t.rows - c0);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           if (j < nr) {
@@ -147,9 +149,10 @@ __device__ __forceinline__ void epilogue_tile(const Tile& t, const GemmParams& p
       tmem_ld16(tq + a * TN + c0, r);
       tmem_ld_wait();
       reg_fence16(r);
-      if (feat < p.out_features) {
+      const int nr = min(16, t.rows - c0);
+      if (feat < p.out_features && !(p.out_rows > 0 && (bad_index(t.out_row + c0, p.out_rows, p.err) ||
+                                                        bad_index(t.out_row + c0 + nr - 1, p.out_rows, p.err)))) {
         float* out = static_cast<float*>(p.out) + out_shift + (size_t)(t.out_row + c0) * p.out_ld + feat;
-        const int nr = min(16, t.rows - c0);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           if (j < nr) {

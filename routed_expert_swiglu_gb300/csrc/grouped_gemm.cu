@@ -227,6 +227,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = ew >> 2;       // which 16-column chunks: half, half+2, half+4, ...
     int buf = 0;
     uint32_t buf_phase = 0;
+#if MOE_TEST_UNSET_WAIT
+    // test build: wait on a phase nothing completes (only these warps arrive on it), so the
+    // wait runs out and the kernel takes its abort path
+    mbar_wait(acce_bar(0), 0, abort_flag, p.err);
+#endif
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<TN>(tile / ksplit, p);
       if (t.rows <= 0) continue;
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  sync_and_quiesce(abort_flag);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, S::TMEM_COLS);
@@ -466,6 +471,11 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>::THRE
     const int xch = half * 2 + (quad & 1);  // SwiGLU: exchange channel of this gate/up warp pair
     int buf = 0;
     uint32_t buf_phase = 0;
+#if MOE_TEST_UNSET_WAIT
+    // test build: wait on a phase nothing completes (only the epilogue warps arrive on it, the
+    // even CTA's), so the wait runs out and both CTAs take their abort path
+    mbar_wait(acce_bar(0), 0, abort_flag, p.err);
+#endif
     uint32_t xiter = 0;                      // SwiGLU: chunks exchanged so far on this channel
     bool ok = true;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
@@ -510,10 +520,11 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>::THRE
             for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
             mbar_arrive(xempty_bar(xch, sl));
             const int feat = t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
-            if (feat < p.out_features) {
+            const int nr = min(16, t.rows - c0);
+            if (feat < p.out_features && !(p.out_rows > 0 && (bad_index(t.out_row + c0, p.out_rows, p.err) ||
+                                                              bad_index(t.out_row + c0 + nr - 1, p.out_rows, p.err)))) {
               const int col = ((feat >> 6) << 7) + (feat & 63);
               __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
-              const int nr = min(16, t.rows - c0);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 if (j < nr) {
@@ -538,9 +549,10 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>::THRE
           tmem_ld16(tq + c0, r);
           tmem_ld_wait();
           reg_fence16(r);
-          if (feat < p.out_features) {
+          const int nr = min(16, t.rows - c0);
+          if (feat < p.out_features && !(p.out_rows > 0 && (bad_index(t.out_row + c0, p.out_rows, p.err) ||
+                                                            bad_index(t.out_row + c0 + nr - 1, p.out_rows, p.err)))) {
             float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
-            const int nr = min(16, t.rows - c0);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               if (j < nr) {
@@ -562,7 +574,7 @@ __global__ void __launch_bounds__(PairShape<EPI, TN, HILO, BK, TMEM_ALLOC>::THRE
   }
 
   tc_fence_before();
-  __syncthreads();
+  sync_and_quiesce(abort_flag);
   cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
@@ -695,7 +707,6 @@ static cudaError_t launch_pair_variant(const GemmLaunch& L, GemmParams p, cudaSt
     max_clusters = n;
   }
   int clusters = max_clusters;
-  if (MOE_PAIR_MAX_CLUSTERS > 0 && clusters > MOE_PAIR_MAX_CLUSTERS) clusters = MOE_PAIR_MAX_CLUSTERS;
   const int tiles = L.max_tiles * (p.sched_tn / TN);
   if (tiles < clusters) clusters = tiles;
   if (clusters < 1) clusters = 1;
@@ -716,6 +727,7 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.a_up_offset = L.a_up_offset;
   p.out_features = L.out_features;
   p.out_ld = L.out_ld;
+  p.out_rows = L.out_rows;
   p.out = L.out;
   p.row_scale = L.row_scale;
   p.n_routed = L.n_routed;
@@ -734,22 +746,19 @@ cudaError_t launch_grouped_gemm(const GemmLaunch& L, cudaStream_t s) {
   p.b_exp = nullptr;
   if (L.q8) return launch_fp8_gemm(L, p, kernel_tn, s);
   constexpr int TNP = MOE_TN_PREFILL;
-  constexpr int TN2 = MOE_TN_DOWN;
+  constexpr int TN2 = MOE_TN_PREFILL;
   if (L.pair) {
     if (L.epi == EPI_SWIGLU && kernel_tn == TNP)
-      return launch_pair_variant<EPI_SWIGLU, TNP, false, MOE_G1_BK, MOE_PAIR_TMEM>(L, p, s);
+      return launch_pair_variant<EPI_SWIGLU, TNP, false, 64, MOE_PAIR_TMEM>(L, p, s);
     if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == TN2 && L.mblk == 2)
-      return launch_pair_variant<EPI_F32, TN2, true, MOE_G2_BK, MOE_PAIR_TMEM>(L, p, s);
+      return launch_pair_variant<EPI_F32, TN2, true, 64, MOE_PAIR_TMEM>(L, p, s);
     return cudaErrorInvalidValue;
   }
   if (L.epi == EPI_SWIGLU) {
-    if (kernel_tn == TNP) return launch_variant<EPI_SWIGLU, TNP, 1, false, MOE_G1_BK>(L, p, s);
     if (kernel_tn == 64) return launch_variant<EPI_SWIGLU, 64, 1, false, 64>(L, p, s);
     return cudaErrorInvalidValue;
   }
   if (L.hilo) {
-    if (kernel_tn == TN2 && L.mblk == MOE_G2_MBLK) return launch_variant<EPI_F32, TN2, MOE_G2_MBLK, true, MOE_G2_BK>(L, p, s);
-    if (kernel_tn == 64 && L.mblk == 1) return launch_variant<EPI_F32, 64, 1, true, 64>(L, p, s);
     if (kernel_tn == 64 && L.mblk == 2) return launch_variant<EPI_F32, 64, 2, true, 64>(L, p, s);
     return cudaErrorInvalidValue;
   }

@@ -17,36 +17,19 @@ constexpr int MAX_GROUPS = 32;
 constexpr int MAX_TOKENS = 1 << 20;
 constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch kernels
 
-// Token-tile width of the grouped GEMMs for large batches, and m-blocks (128 output features
-// each) per down-projection tile.  Compile-time so that kernel variants can be swept.
+// Token-tile width of the grouped GEMMs for large batches (compile-time, so that it can be swept),
+// and TMEM columns per CTA of the CTA-pair (2-SM MMA) prefill kernels.
 #ifndef MOE_TN_PREFILL
 #define MOE_TN_PREFILL 256
-#endif
-#ifndef MOE_TN_DOWN
-#define MOE_TN_DOWN 256
-#endif
-#ifndef MOE_G2_MBLK
-#define MOE_G2_MBLK 2
-#endif
-#ifndef MOE_G1_BK
-#define MOE_G1_BK 64
-#endif
-#ifndef MOE_G2_BK
-#define MOE_G2_BK 64
-#endif
-// CTA-pair (2-SM MMA) variants of the prefill grouped GEMMs and their TMEM columns per CTA.
-#ifndef MOE_G1_PAIR
-#define MOE_G1_PAIR 1
-#endif
-#ifndef MOE_G2_PAIR
-#define MOE_G2_PAIR 1
 #endif
 #ifndef MOE_PAIR_TMEM
 #define MOE_PAIR_TMEM 512
 #endif
-// Upper bound on the resident clusters a pair GEMM launches (0: as many as fit).
-#ifndef MOE_PAIR_MAX_CLUSTERS
-#define MOE_PAIR_MAX_CLUSTERS 0
+// 1 (test builds only, with a short MOE_WAIT_LIMIT_NS): the epilogue warps of the bf16 grouped
+// GEMMs first wait on a barrier phase nothing completes, so that every such launch runs out of
+// time and reports MOE_ERR_TIMEOUT through its abort path.
+#ifndef MOE_TEST_UNSET_WAIT
+#define MOE_TEST_UNSET_WAIT 0
 #endif
 // 1: FP8 expert weights run the kernels that feed the E4M3 codes straight to the tensor cores
 // (tcgen05 kind::f8f6f4, activations split into E4M3 pieces) where the shapes allow it
@@ -122,6 +105,7 @@ struct GemmLaunch {
   int pair;                // run on CTA pairs (2-SM MMA, 256 weight rows per tile)
   int mblk;                // fp32 variant: 128-feature m-blocks per tile (1 or 2)
   int num_mblocks, a_rows_per_group, a_up_offset, out_features, out_ld;
+  int out_rows;            // rows of `out` (per K slice): checked in MOE_DEBUG_BOUNDS builds, 0 = unchecked
   void* out;
   const float* row_scale;
   int n_routed, shared_b_shift;
@@ -165,6 +149,7 @@ cudaError_t launch_split_rows_e4m3(const void* src, bool bf16_src, const int32_t
 
 struct CombineLaunch {
   const float* o; const int32_t* inv; int T, k, d, N, n_shared; void* out;
+  int* err;  // MOE_DEBUG_BOUNDS builds: row checks
 };
 cudaError_t launch_combine(const CombineLaunch& L, cudaStream_t s);
 

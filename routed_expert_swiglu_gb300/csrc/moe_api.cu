@@ -3,6 +3,7 @@
 // combine on the caller's stream.  No device allocation, no host synchronisation (except
 // moe_check_status).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -184,6 +185,13 @@ void record(const moe_plan* p, int stage, cudaStream_t s) {
   if (p->events != nullptr && stage < p->n_events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(p->events[stage]), s);
 }
 
+// Host-side NVTX range around one launch ("moe.<kernel>"), closed on every return path.  NVTX is
+// header-only here and costs nothing unless a profiler is attached.
+struct LaunchRange {
+  explicit LaunchRange(const char* name) { nvtxRangePushA(name); }
+  ~LaunchRange() { nvtxRangePop(); }
+};
+
 // Router GEMM + top-k into the given outputs.
 moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t* token_ids, const moe_bf16* w_r,
                      const float* bias, float* logits, int32_t* ids, float* w, void* ws, int sms, cudaStream_t s) {
@@ -203,6 +211,7 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   g.num_mblocks = ceil_div(c.n_experts, gemm_features_per_tile(1, g.mblk));
   g.out_features = c.n_experts;
   g.out_ld = c.n_experts;
+  g.out_rows = T;
   g.out = logits;
   g.n_routed = 1;
   g.dense_rows = T;
@@ -212,7 +221,10 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   g.max_tiles = ceil_div(T, g.TN) * g.num_mblocks;
   g.err = err;
   g.num_sms = sms;
-  MOE_CUDA(launch_grouped_gemm(g, s));
+  {
+    LaunchRange r("moe.router_gemm");
+    MOE_CUDA(launch_grouped_gemm(g, s));
+  }
   record(p, ST_ROUTER_GEMM, s);
   TopkLaunch tk;
   tk.nsplit = g.ksplit;
@@ -234,7 +246,10 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   tk.topk_ids = ids;
   tk.topk_w = w;
   tk.err = err;
-  MOE_CUDA(launch_topk(tk, s));
+  {
+    LaunchRange r("moe.topk");
+    MOE_CUDA(launch_topk(tk, s));
+  }
   record(p, ST_TOPK, s);
   return MOE_OK;
 }
@@ -292,11 +307,16 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   pm.xd = f8mma ? nullptr : at<void>(ws, L.xd);
   pm.d = d;
   pm.num_sms = sms;
-  MOE_CUDA(launch_permute(pm, s));
+  {
+    LaunchRange r("moe.dispatch");
+    MOE_CUDA(launch_permute(pm, s));
+  }
   const int64_t rows_h = (int64_t)L.N + (int64_t)sh * T;
-  if (f8mma)
+  if (f8mma) {
+    LaunchRange r("moe.split_rows_e4m3");
     MOE_CUDA(launch_split_rows_e4m3(x, true, pm.perm_tok, L.N, (int)rows_h, d, 2, at<uint8_t>(ws, L.xd),
                                     at<int32_t>(ws, L.xexp), s));
+  }
   record(p, ST_DISPATCH, s);
 
   GemmLaunch g1;
@@ -313,12 +333,13 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.b_sh_rows = T;
   g1.K = d;
   g1.mblk = 1;
-  g1.pair = !is_decode(T) && MOE_G1_PAIR;
+  g1.pair = !is_decode(T);
   g1.num_mblocks = ceil_div(f, gemm_features_per_tile(0, 1));
   g1.a_rows_per_group = 2 * f;
   g1.a_up_offset = f;
   g1.out_features = f;
   g1.out_ld = 2 * f;
+  g1.out_rows = (int)rows_h;
   g1.out = at<void>(ws, L.h);
   g1.n_routed = E;
   g1.shared_b_shift = -L.N;
@@ -348,10 +369,15 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   }
   g1.err = err;
   g1.num_sms = sms;
-  MOE_CUDA(launch_grouped_gemm(g1, s));
-  if (f8mma)  // h (fp32) -> four E4M3 pieces per row, in place
+  {
+    LaunchRange r("moe.gate_up_gemm");
+    MOE_CUDA(launch_grouped_gemm(g1, s));
+  }
+  if (f8mma) {  // h (fp32) -> four E4M3 pieces per row, in place
+    LaunchRange r("moe.split_rows_e4m3");
     MOE_CUDA(launch_split_rows_e4m3(at<void>(ws, L.h), false, nullptr, 0, (int)rows_h, f, 4, at<uint8_t>(ws, L.h),
                                     at<int32_t>(ws, L.hexp), s));
+  }
   record(p, ST_GATE_UP, s);
 
   GemmLaunch g2;
@@ -366,14 +392,14 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.b_rows = rows_h;
   g2.K = f;
   g2.hilo = 1;         // B rows hold the (hi, lo) pair: 2*f values, each pair against one W2 block
-  g2.mblk = is_decode(T) ? 2 : MOE_G2_MBLK;
-  g2.kernel_tn = is_decode(T) ? L.TN : MOE_TN_DOWN;
-  g2.pair = !is_decode(T) && MOE_G2_PAIR;
-  if (g2.pair) g2.mblk = 2;  // a pair tile covers 256 output features
+  g2.mblk = 2;         // decode: two 128-feature blocks per CTA; prefill: a pair tile covers 256
+  g2.kernel_tn = L.TN;
+  g2.pair = !is_decode(T);
   g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
   g2.a_rows_per_group = d;
   g2.out_features = d;
   g2.out_ld = d;
+  g2.out_rows = (int)rows_h;
   g2.out = at<void>(ws, L.o);
   g2.row_scale = pm.row_w;
   g2.n_routed = E;
@@ -403,7 +429,10 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   }
   g2.err = err;
   g2.num_sms = sms;
-  MOE_CUDA(launch_grouped_gemm(g2, s));
+  {
+    LaunchRange r("moe.down_gemm");
+    MOE_CUDA(launch_grouped_gemm(g2, s));
+  }
   record(p, ST_DOWN, s);
 
   CombineLaunch cb;
@@ -415,7 +444,11 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   cb.N = L.N;
   cb.n_shared = sh;
   cb.out = out;
-  MOE_CUDA(launch_combine(cb, s));
+  cb.err = err;
+  {
+    LaunchRange r("moe.combine");
+    MOE_CUDA(launch_combine(cb, s));
+  }
   record(p, ST_COMBINE, s);
   return MOE_OK;
 }
@@ -704,6 +737,7 @@ moe_status moe_check_status(moe_plan* plan, const void* ws, moe_stream_t stream)
   int v = 0;
   MOE_CUDA(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost));  // the error word is at offset 0
   if (v & DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  if (v & DEVERR_BOUNDS) return MOE_ERR_INTERNAL;
   if (v != 0) return MOE_ERR_DEVICE_INPUT;
   return MOE_OK;
 }
@@ -755,6 +789,7 @@ const char* moe_status_string(moe_status status) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_INPUT: return "device input out of range (clamped)";
     case MOE_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case MOE_ERR_INTERNAL: return "internal index check failed";
   }
   return "unknown status";
 }

@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* _
   __syncthreads();
   if (valid) {
     const int row = __ldg(offsets + e) + blockbase[(size_t)blockIdx.x * E + e] + wcnt[warp * E + e] + rank;
+    if (bad_index(row, N, err)) return;
     if (perm_tok) perm_tok[row] = i / k;
     if (inv) inv[i] = row;
     if (row_w) row_w[row] = __ldg(w + i);
@@ -157,12 +158,14 @@ __global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* _
 // flight.  Used for small batches, where one warp per token would leave most SMs idle.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int4* __restrict__ x, int4* __restrict__ xd,
                                                           const int32_t* __restrict__ perm_tok, int N,
-                                                          int vec_per_row) {
+                                                          int vec_per_row, int T, int* err) {
   constexpr int U = 8;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += nwarps) {
-    const int4* src = x + (size_t)__ldg(perm_tok + r) * vec_per_row;
+    const int tok = __ldg(perm_tok + r);
+    if (bad_index(tok, T, lane == 0 ? err : nullptr)) continue;
+    const int4* src = x + (size_t)tok * vec_per_row;
     int4* dst = xd + (size_t)r * vec_per_row;
     for (int v0 = 0; v0 < vec_per_row; v0 += 32 * U) {
       int4 buf[U];
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int4* __restrict
 // in flight.
 __global__ void __launch_bounds__(256) dispatch_rows_kernel(const int4* __restrict__ x, int4* __restrict__ xd,
                                                             const int32_t* __restrict__ inv, int T, int k,
-                                                            int vec_per_row) {
+                                                            int vec_per_row, int* err) {
   constexpr int U = 8;
   const int lane = threadIdx.x & 31;
   const int nwarps = gridDim.x * (blockDim.x >> 5);
@@ -203,7 +206,9 @@ __global__ void __launch_bounds__(256) dispatch_rows_kernel(const int4* __restri
 #pragma unroll
       for (int j = 0; j < MAX_TOPK; ++j) {
         if (j < k) {
-          int4* dst = xd + (size_t)__shfl_sync(0xffffffffu, my_row, j) * vec_per_row;
+          const int row = __shfl_sync(0xffffffffu, my_row, j);
+          if (bad_index(row, (long long)T * k, lane == 0 ? err : nullptr)) continue;
+          int4* dst = xd + (size_t)row * vec_per_row;
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int v = v0 + u * 32 + lane;
@@ -240,11 +245,11 @@ cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s) {
       if (L.inv == nullptr) return cudaErrorInvalidValue;  // the token-major copy goes by the inverse map
       const int blocks = std::min((L.T + 7) / 8, cap);
       dispatch_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const int4*>(L.x), static_cast<int4*>(L.xd), L.inv,
-                                                  L.T, L.k, vec);
+                                                  L.T, L.k, vec, L.err);
     } else {
       const int blocks = std::min((N + 7) / 8, cap);
       gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const int4*>(L.x), static_cast<int4*>(L.xd),
-                                                L.perm_tok, N, vec);
+                                                L.perm_tok, N, vec, L.T, L.err);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
