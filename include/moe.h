@@ -199,14 +199,16 @@ moe_status moe_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int32_t n_
  * [E, d, d_ff] hold E4M3 codes, e13 [E, ceil(2*d_ff/128), ceil(d/128)] and e2 [E, ceil(d/128),
  * ceil(d_ff/128)] their tile exponents, as moe_quantize_fp8 writes them (shared expert: the
  * same with E = 1; NULL without one).  The layer is moe_forward on the dequantised weights
- * q * 2^e, with the activations kept at bf16-level precision.  When d and d_ff are multiples of
- * 128, the GEMMs feed the codes (half the weight bytes) straight to the FP8 tensor-core MMA, with
- * the activations as sums of E4M3 pieces (piece p weighted 2^(-4p)) and one power-of-two scale
- * per row: x in two pieces, exact for every value above 2^-13.8 of its row's largest magnitude
- * and within 2^-21 of that magnitude below it; h in four pieces, within 2^-16 of each value plus
- * 2^-29 of the row's largest magnitude.  Other shapes widen the codes to bf16 into Tensor
- * Memory and run the bf16 MMA.  Code pointers 16-byte aligned; same workspace and outputs as
- * moe_forward. */
+ * q * 2^e, with the activations kept at bf16-level precision.  Batches above 64 tokens stream
+ * the codes (half the weight bytes) into CTA-pair kernels that widen them to bf16 q * 2^e in
+ * shared memory and run the bf16 MMA on the same activations as moe_forward (bf16 x, the (hi,
+ * lo) bf16 pair for h).  Batches of at most 64 tokens with d and d_ff multiples of 128 feed the
+ * codes straight to the FP8 tensor-core MMA, with the activations as sums of E4M3 pieces (piece p
+ * weighted 2^(-4p)) and one power-of-two scale per row: x in two pieces, exact for every value
+ * above 2^-13.8 of its row's largest magnitude and within 2^-21 of that magnitude below it; h in
+ * four pieces, within 2^-16 of each value plus 2^-29 of the row's largest magnitude; other shapes
+ * widen the codes to bf16 into Tensor Memory.  Code pointers 16-byte aligned; same workspace and
+ * outputs as moe_forward. */
 moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                            const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,
                            const uint8_t* q2, const int8_t* e2, const uint8_t* q13_sh, const int8_t* e13_sh,
@@ -236,9 +238,11 @@ moe_status moe_forward(moe_plan* plan, int32_t T, const moe_bf16* x, const int32
  * sub-block exponents (as moe_quantize_mxfp4 writes them), t13 [E, 2*d_ff/128, d/128] and t2
  * [E, d/128, d_ff/128] the tile exponents of their FP8 form (moe_mxfp4_to_fp8 with q8 = NULL);
  * shared expert the same with E = 1 (NULL without one).  The GEMMs stream the 4-bit codes and
- * turn them into the exact E4M3 values of the FP8 form on the chip, so the layer equals
- * moe_forward_fp8 on moe_mxfp4_to_fp8's output (activations as E4M3 pieces, see there).  Needs
- * d and d_ff multiples of 128 (else MOE_ERR_UNSUPPORTED); 16-row token tiles, a decode path.
+ * turn them into the exact E4M3 values of the FP8 form on the chip, so the layer is the bf16
+ * layer on the dequantised weights with the activations as E4M3 pieces (see moe_forward_fp8);
+ * for batches of at most 64 tokens it equals moe_forward_fp8 on moe_mxfp4_to_fp8's output bit
+ * for bit.  Needs d and d_ff multiples of 128 (else MOE_ERR_UNSUPPORTED); 16-row token tiles, a
+ * decode path (at prefill, moe_forward_fp8 on the converted weights is the faster form).
  * Code pointers 16-byte aligned, sub-block exponents 4-byte aligned; same workspace and
  * outputs as moe_forward. */
 moe_status moe_forward_mxfp4(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,

@@ -1107,6 +1107,438 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
   }
 }
 
+// ============================================================================ CTA-pair FP8 (prefill)
+// FP8 weights at prefill batches, on the 2-SM MMA of the bf16 CTA-pair kernels.  TMA streams each
+// CTA's 128 weight rows as E4M3 codes (64-byte rows per 64-wide K step: half the bf16 bytes) with
+// the token rows as bf16 (the dispatched x rows, or the (hi, lo) activation pair), four converter
+// warps per CTA widen the codes to bf16 q * 2^e (exact; e the 128 x 128 tile's exponent) into a
+// ring of 128-byte-swizzled A slabs in shared memory, and the even CTA's MMA thread multiplies
+// them with bf16 MMAs exactly as the bf16 pair kernel does.  The layer is then the bf16 layer on
+// the dequantised weights with bf16 activations, the definition the FP8 weight format has.  Roles
+// (704 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer (even CTA), warps 2..9
+// epilogue, warps 10..21 converters in three groups of four that take the stages in turn (thread r
+// of a group widens weight row r of its stages).  Measured (V4-Flash T=8192): one group 8.28 ms,
+// two 5.48, three 4.82 ms per forward (the earlier single-CTA FP8 prefill kernels: 5.87 ms); with
+// the conversion replaced by a plain copy, two groups gave 4.35 ms: the conversion's integer work
+// and its place in each stage's round trip (codes landed -> widened -> multiplied -> released)
+// bound it, not the halved weight stream.
+template <int EPI, bool HILO>
+struct Fp8PairShape {
+  static constexpr int TN = 256;
+  static constexpr int HALF = TN / 2;
+  static constexpr int BLOCK_K = 64;
+  static constexpr int ROW_BYTES = 128;                // bf16 rows of B and of the widened A
+  static constexpr int RAW_A = BLOCK_M * BLOCK_K;      // 128 rows x 64 codes (64-byte swizzle)
+  static constexpr int NUM_B = HILO ? 2 : 1;
+  static constexpr int B_BYTES = HALF * ROW_BYTES;     // one activation operand, this CTA's rows
+  static constexpr int RAW_STAGE = RAW_A + NUM_B * B_BYTES;
+  static constexpr int A_BYTES = BLOCK_M * ROW_BYTES;  // one widened slab
+  static constexpr int CSLOTS = 4;                     // widened slabs in flight
+  static constexpr int XCH = (EPI == EPI_SWIGLU) ? 4 : 0;
+  static constexpr int XBUF_BYTES = XCH * 2 * 16 * 32 * 4;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 512 - XBUF_BYTES - CSLOTS * A_BYTES) / RAW_STAGE;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = CSLOTS * A_BYTES + STAGES * RAW_STAGE + XBUF_BYTES + 1024 + 512;
+  static constexpr int ACC_COLS = TN;
+  static constexpr int NUM_BUF = 2;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int CVT_GROUPS = 3;                 // groups of four converter warps, stages in turn
+  static constexpr int NUM_CVT_WARPS = 4 * CVT_GROUPS;
+  static constexpr int CVT_WARP0 = 2 + NUM_EPI_WARPS;
+  static constexpr int THREADS = (2 + NUM_EPI_WARPS + NUM_CVT_WARPS) * 32;
+  static constexpr int A_BOX = (EPI == EPI_SWIGLU) ? BLOCK_M / 2 : BLOCK_M;  // code rows per box
+  // barriers: full, rfull, empty per stage; cfull, cempty per slab; acc full/empty x2; exchange
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * CSLOTS + 4 + 4 * XCH;
+  static_assert(NUM_BARS * 8 + 8 <= 512, "barrier area");
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(RAW_STAGE % 1024 == 0 && A_BYTES % 1024 == 0 && RAW_A % 1024 == 0, "swizzled tiles on 1024 B");
+};
+
+template <int EPI, bool HILO>
+__global__ void __launch_bounds__(Fp8PairShape<EPI, HILO>::THREADS, 1)
+    fp8w_pair_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  using S = Fp8PairShape<EPI, HILO>;
+  constexpr int TN = S::TN;
+  constexpr int STAGES = S::STAGES;
+  constexpr int CS = S::CSLOTS;
+  constexpr int BLOCK_K = S::BLOCK_K;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* aslab = smem;                                 // CSLOTS widened A slabs
+  uint8_t* raw = smem + CS * S::A_BYTES;                 // STAGES x (codes, B)
+  float* xbuf = reinterpret_cast<float*>(raw + STAGES * S::RAW_STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + STAGES * S::RAW_STAGE + S::XBUF_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };                      // B bytes, even CTA
+  auto rfull_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };          // this CTA's codes
+  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };      // stage consumed
+  auto cfull_bar = [&](int c) { return bar0 + 8u * (3 * STAGES + c); };      // slab widened (even CTA)
+  auto cempty_bar = [&](int c) { return bar0 + 8u * (3 * STAGES + CS + c); };  // slab consumed
+  auto accf_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + 2 * CS + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (3 * STAGES + 2 * CS + 2 + a); };
+  auto xfull_bar = [&](int x, int sl) { return bar0 + 8u * (3 * STAGES + 2 * CS + 4 + 2 * x + sl); };
+  auto xempty_bar = [&](int x, int sl) { return bar0 + 8u * (3 * STAGES + 2 * CS + 4 + 2 * S::XCH + 2 * x + sl); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank() & 1u;
+  const bool leader = (rank == 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(rfull_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int c = 0; c < CS; ++c) {
+      mbar_init(cfull_bar(c), 2 * 4);  // the four warps of one converter group, in both CTAs
+      mbar_init(cempty_bar(c), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 2 * NUM_EPI_WARPS);
+    }
+    for (int x = 0; x < S::XCH; ++x)
+      for (int sl = 0; sl < 2; ++sl) {
+        mbar_init(xfull_bar(x, sl), 32);
+        mbar_init(xempty_bar(x, sl), 32);
+      }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.a_sh);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), S::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int pair = blockIdx.x / 2;
+  const int npairs = gridDim.x / 2;
+  const int total_tiles = __ldg(&p.grp[p.n_groups_total].z) * p.num_mblocks;
+  const int KB = p.K / BLOCK_K;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const int n_mma = max(32, (t.rows + 31) / 32 * 32);
+        const int half = n_mma >> 1;  // token rows per CTA
+        const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
+        const CUtensorMap* tb = t.shared ? maps.b_sh : maps.b;
+        const int base = t.shared ? 0 : t.g * p.a_rows_per_group;
+        const int b_row = t.b_row + (int)rank * half;
+        const uint32_t expect = 2u * (uint32_t)(S::NUM_B * half * S::ROW_BYTES);  // both CTAs' token rows
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const int k0 = kb * BLOCK_K;
+          // this CTA's weight codes, counted on its own barrier (its converters wait there)
+          mbar_arrive_expect_tx(rfull_bar(stage), S::RAW_A);
+          if (EPI == EPI_SWIGLU) {
+            // gate and up codes of this CTA's 64 features in one 3-D box
+            tma_load_3d(sr, ta, rfull_bar(stage), k0, t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2),
+                        t.shared ? 0 : 2 * t.g);
+          } else {
+            tma_load_2d(sr, ta, rfull_bar(stage), k0, base + t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M);
+          }
+          // both CTAs' token rows, counted on the even CTA's barrier (its MMA thread waits there)
+          const uint32_t fbc = mapa_shared(full_bar(stage), 0);
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), expect);
+#pragma unroll
+          for (int bp = 0; bp < S::NUM_B; ++bp) {
+            const uint32_t sb = sr + S::RAW_A + bp * S::B_BYTES;
+            // the (hi, lo) pair: per 64 features, 64 hi columns then 64 lo columns
+            const int kc = HILO ? (k0 >> 6) * 128 + (k0 & 63) + bp * 64 : k0;
+            int off = 0;
+#pragma unroll
+            for (int i = NUM_BOX_H - 1; i >= 0; --i) {
+              const int h = B_BOX << i;
+              if (h <= S::HALF && (half - off) >= h) {
+                tma_load_2d_pair(sb + off * S::ROW_BYTES, tb + i, fbc, kc, b_row + off);
+                off += h;
+              }
+            }
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      int stage = 0, cs = 0, buf = 0;
+      uint32_t phase = 0, cphase = 0, buf_phase = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+        const Tile t = decode_tile<TN>(tile, p);
+        if (t.rows <= 0) continue;
+        const int n_mma = max(32, (t.rows + 31) / 32 * 32);
+        if (!mbar_wait_cluster(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32_m256(n_mma);
+        const uint32_t d = tmem_base + buf * S::ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          // both CTAs' token rows have landed, and both CTAs' converters have widened the slab
+          if (!mbar_wait_cluster(full_bar(stage), phase, abort_flag, p.err) ||
+              !mbar_wait_cluster(cfull_bar(cs), cphase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(aslab + cs * S::A_BYTES);
+          const uint32_t sb = smem_u32(raw + stage * S::RAW_STAGE + S::RAW_A);
+#pragma unroll
+          for (int kk = 0; kk < BLOCK_K / 16; ++kk) {
+            const uint64_t da = smem_desc_sw(sa, S::ROW_BYTES) + 2 * kk;
+#pragma unroll
+            for (int bp = 0; bp < S::NUM_B; ++bp) {
+              const uint64_t db = smem_desc_sw(sb + bp * S::B_BYTES, S::ROW_BYTES) + 2 * kk;
+              tc_mma_pair(d, da, db, idesc, (kb | kk | bp) ? 1u : 0u);
+            }
+          }
+          tc_commit_pair_mc(empty_bar(stage), (uint16_t)0x3u);  // the stage, in both CTAs
+          tc_commit_pair_mc(cempty_bar(cs), (uint16_t)0x3u);    // the widened slab, in both CTAs
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++cs == CS) {
+            cs = 0;
+            cphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(accf_bar(buf), (uint16_t)0x3u);
+        if (++buf == S::NUM_BUF) {
+          buf = 0;
+          buf_phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < S::CVT_WARP0) {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int half = ew >> 2;
+    const int xch = half * 2 + (quad & 1);  // SwiGLU: exchange channel of this gate/up warp pair
+    int buf = 0;
+    uint32_t buf_phase = 0;
+#if MOE_TEST_UNSET_WAIT
+    // test build: wait on a phase nothing completes (only the epilogue warps arrive on it, the
+    // even CTA's), so the wait runs out and both CTAs take their abort path
+    mbar_wait(acce_bar(0), 0, abort_flag, p.err);
+#endif
+    uint32_t xiter = 0;                      // SwiGLU: chunks exchanged so far on this channel
+    bool ok = true;
+    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
+    for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      if (!mbar_wait_cluster(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int nchunk = (t.rows + 15) >> 4;
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
+      if (EPI == EPI_SWIGLU) {
+        float* xb = xbuf + xch * (2 * 16 * 32);
+        for (int ci = half; ci < nchunk; ci += 2, ++xiter) {
+          const int sl = xiter & 1;
+          const uint32_t par = (xiter >> 1) & 1u;
+          const int c0 = ci * 16;
+          if (quad >= 2) {
+            // up lanes: hand the 16 up values of this chunk to the gate warp of the channel
+            uint32_t ru[16];
+            tmem_ld16(tq + c0, ru);
+            tmem_ld_wait();
+            reg_fence16(ru);
+            if (!mbar_wait(xempty_bar(xch, sl), par ^ 1u, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xb[(sl * 16 + j) * 32 + lane] = __uint_as_float(ru[j]);
+            mbar_arrive(xfull_bar(xch, sl));
+          } else {
+            uint32_t rg[16];
+            tmem_ld16(tq + c0, rg);
+            tmem_ld_wait();
+            reg_fence16(rg);
+            if (!mbar_wait(xfull_bar(xch, sl), par, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            float u[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) u[j] = xb[(sl * 16 + j) * 32 + lane];
+            mbar_arrive(xempty_bar(xch, sl));
+            const int feat = t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2) + quad * 32 + lane;
+            const int nr = min(16, t.rows - c0);
+            if (feat < p.out_features && !(p.out_rows > 0 && (bad_index(t.out_row + c0, p.out_rows, p.err) ||
+                                                              bad_index(t.out_row + c0 + nr - 1, p.out_rows, p.err)))) {
+              const int col = ((feat >> 6) << 7) + (feat & 63);
+              __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + col;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (j < nr) {
+                  const float g = __uint_as_float(rg[j]);
+                  const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
+                  const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+                  const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+                  out[(size_t)j * p.out_ld] = hi;
+                  out[(size_t)j * p.out_ld + 64] = lo;
+                }
+              }
+            }
+          }
+        }
+        if (!ok) break;
+      } else {
+        const bool scaled = (p.row_scale != nullptr) && !t.shared;
+        const int feat = t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M + quad * 32 + lane;
+        for (int ci = half; ci < nchunk; ci += 2) {
+          const int c0 = ci * 16;
+          uint32_t r[16];
+          tmem_ld16(tq + c0, r);
+          tmem_ld_wait();
+          reg_fence16(r);
+          const int nr = min(16, t.rows - c0);
+          if (feat < p.out_features && !(p.out_rows > 0 && (bad_index(t.out_row + c0, p.out_rows, p.err) ||
+                                                            bad_index(t.out_row + c0 + nr - 1, p.out_rows, p.err)))) {
+            float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld + feat;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (j < nr) {
+                const float sc = scaled ? __ldg(p.row_scale + t.out_row + c0 + j) : 1.0f;
+                out[(size_t)j * p.out_ld] = __uint_as_float(r[j]) * sc;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf == 0 ? acce_leader0 : acce_leader1);
+      if (++buf == S::NUM_BUF) {
+        buf = 0;
+        buf_phase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ code -> bf16 converters
+    // Thread r widens weight row r of every stage: its 64 codes (four 16-byte chunks; chunk c at
+    // c ^ ((r >> 1) & 3), the 64-byte swizzle TMA wrote) times 2^e of the row's 128 x 128 tile, into
+    // row r of the stage's slab (eight 16-byte chunks; chunk c at c ^ (r & 7), the 128-byte swizzle
+    // the MMA reads).  The thread keeps the exponents of the current and the next 128-wide K tile.
+    const int r = ((warp - S::CVT_WARP0) & 3) * 32 + lane;  // the group's four warps cover 128 rows
+    const int group = (warp - S::CVT_WARP0) >> 2;  // widens the stages n with n % CVT_GROUPS == group
+    const int nk = p.exp_nk;
+    int stage = 0, cs = 0;
+    uint32_t phase = 0, cphase = 0;
+    uint32_t n = 0;  // stage counter over all tiles of this CTA
+    bool ok = true;
+    for (int tile = pair; ok && tile < total_tiles; tile += npairs) {
+      const Tile t = decode_tile<TN>(tile, p);
+      if (t.rows <= 0) continue;
+      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * nk;
+      int mrow;  // this row's row in its weight matrix
+      if (EPI == EPI_SWIGLU) {
+        const int f0 = t.mb * BLOCK_M + (int)rank * (BLOCK_M / 2);  // first feature of this CTA
+        mrow = r < BLOCK_M / 2 ? f0 + r : p.a_up_offset + f0 + (r - BLOCK_M / 2);
+      } else {
+        mrow = t.mb * 2 * BLOCK_M + (int)rank * BLOCK_M + r;
+      }
+      const int trow = min(mrow >> 7, p.exp_nr - 1);  // rows past the matrix are zero codes
+      int e_cur = __ldg(ex + trow * nk);
+      int e_nxt = nk > 1 ? __ldg(ex + trow * nk + 1) : 0;
+      for (int kb = 0; kb < KB; ++kb, ++n) {
+        if (kb > 0 && ((kb * BLOCK_K) & 127) == 0) {  // a new 128-wide K tile: rotate, fetch the next
+          const int kn = ((kb * BLOCK_K) >> 7) + 1;
+          e_cur = e_nxt;
+          e_nxt = kn < nk ? __ldg(ex + trow * nk + kn) : 0;
+        }
+        if ((int)(n % S::CVT_GROUPS) == group) {
+          if (!mbar_wait(rfull_bar(stage), phase, abort_flag, p.err) ||
+              !mbar_wait(cempty_bar(cs), cphase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t row = smem_u32(raw + stage * S::RAW_STAGE + r * BLOCK_K);
+          const uint32_t dst = smem_u32(aslab + cs * S::A_BYTES + r * S::ROW_BYTES);
+          const int e = e_cur;
+          const uint32_t bias2 = (uint32_t)(120 + e) * 0x00800080u;
+          const float scale = __int_as_float((e + 127) << 23);
+          const bool tiny = e < -120;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // K codes [16 c, 16 c + 16) -> widened chunks 2c, 2c + 1
+            const uint4 q = ld_shared_v4(row + ((c ^ ((r >> 1) & 3)) << 4));
+            uint2 v0, v1, v2, v3;
+            // normal codes and an ordinary scale (the common case): integer path; otherwise (a zero
+            // or subnormal code, or a scale below 2^-120) the conversion instruction
+            if (!tiny && !(e4m3x4_has_small(q.x) | e4m3x4_has_small(q.y) | e4m3x4_has_small(q.z) |
+                           e4m3x4_has_small(q.w))) {
+              v0 = e4m3x4_normal_to_bf16x4(q.x, bias2);
+              v1 = e4m3x4_normal_to_bf16x4(q.y, bias2);
+              v2 = e4m3x4_normal_to_bf16x4(q.z, bias2);
+              v3 = e4m3x4_normal_to_bf16x4(q.w, bias2);
+            } else {
+              v0 = make_uint2(e4m3x2_to_bf16x2_exact(q.x, scale), e4m3x2_to_bf16x2_exact(q.x >> 16, scale));
+              v1 = make_uint2(e4m3x2_to_bf16x2_exact(q.y, scale), e4m3x2_to_bf16x2_exact(q.y >> 16, scale));
+              v2 = make_uint2(e4m3x2_to_bf16x2_exact(q.z, scale), e4m3x2_to_bf16x2_exact(q.z >> 16, scale));
+              v3 = make_uint2(e4m3x2_to_bf16x2_exact(q.w, scale), e4m3x2_to_bf16x2_exact(q.w >> 16, scale));
+            }
+            st_shared_v4(dst + (((2 * c) ^ (r & 7)) << 4), v0.x, v0.y, v1.x, v1.y);
+            st_shared_v4(dst + (((2 * c + 1) ^ (r & 7)) << 4), v2.x, v2.y, v3.x, v3.y);
+          }
+          // the widened row is read by the tensor cores (async proxy) once the MMA thread of the
+          // even CTA has seen the group's four converter warps of both CTAs arrive
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(cfull_bar(cs), 0));
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++cs == CS) {
+          cs = 0;
+          cphase ^= 1u;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  sync_and_quiesce(abort_flag);
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
+  }
+}
+
 // ----------------------------------------------------------------------------- host side
 
 // E4M3 weight codes: 2-D uint8 [rows, cols] with boxes of box_k codes x box_rows rows, and the
@@ -1126,12 +1558,12 @@ static bool make_tmap_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t 
 }
 
 static bool make_tmap_u8_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t cols,
-                                int box_k = 64) {
+                                int box_k = 64, int box_rows = BLOCK_M) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
   cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(d_ff * cols)};
-  cuuint32_t box[3] = {(cuuint32_t)box_k, (cuuint32_t)BLOCK_M, 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_k, (cuuint32_t)box_rows, 2};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -1277,7 +1709,85 @@ static cudaError_t launch_fp4mma_variant(const GemmLaunch& L, GemmParams base, c
   return cudaGetLastError();
 }
 
+
+template <int EPI, bool HILO>
+static cudaError_t launch_fp8w_pair_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
+  using Sh = Fp8PairShape<EPI, HILO>;
+  static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
+  if (p.sched_tn != Sh::TN || L.K % Sh::BLOCK_K != 0 || p.ksplit != 1 || p.grp == nullptr || L.a_exp == nullptr)
+    return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr && L.a_sh_exp == nullptr) return cudaErrorInvalidValue;
+  GemmMaps m;
+  memset(&m, 0, sizeof(m));
+  if (EPI == EPI_SWIGLU) {
+    const int64_t f = L.a_up_offset;
+    if (!make_tmap_u8_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, L.K, 64, Sh::A_BOX)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8_gateup(&m.a_sh, L.a_sh_ptr, 1, f, L.K, 64, Sh::A_BOX))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_u8(&m.a, L.a_ptr, L.a_rows, L.K, Sh::A_BOX)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_u8(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, Sh::A_BOX))
+      return cudaErrorInvalidValue;
+  }
+  if (L.a_sh_ptr == nullptr) m.a_sh = m.a;
+  const int kb_cols = HILO ? 2 * L.K : L.K;
+  for (int i = 0; i < NUM_BOX_H; ++i) {
+    const int h = B_BOX << i;
+    if (h > Sh::HALF) break;
+    if (!make_tmap(&m.b[i], L.b_ptr, L.b_rows, kb_cols, h, 64)) return cudaErrorInvalidValue;
+    if (L.b_sh_ptr != nullptr) {
+      if (!make_tmap(&m.b_sh[i], L.b_sh_ptr, L.b_sh_rows, kb_cols, h, 64)) return cudaErrorInvalidValue;
+    } else {
+      m.b_sh[i] = m.b[i];
+    }
+  }
+  p.a_exp = L.a_exp;
+  p.a_sh_exp = L.a_sh_exp != nullptr ? L.a_sh_exp : L.a_exp;
+  p.exp_nr = (L.a_rows_per_group + 127) / 128;
+  p.exp_nk = (L.K + 127) / 128;
+  auto kern = fp8w_pair_gemm_kernel<EPI, HILO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.blockDim = dim3(Sh::THREADS);
+  cfg.dynamicSmemBytes = Sh::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many clusters as can be resident at once (persistent kernel), at most one per tile
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (L.num_sms / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = L.num_sms / 2;
+    }
+    max_clusters = n;
+  }
+  int clusters = max_clusters;
+  if (L.max_tiles < clusters) clusters = L.max_tiles;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(2 * clusters);
+  e = cudaLaunchKernelEx(&cfg, kern, m, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fp8_gemm(const GemmLaunch& L, GemmParams p, int kernel_tn, cudaStream_t s) {
+  if (L.q8 == 1 && L.pair) {
+    // prefill: codes widened to bf16 in shared memory, CTA-pair bf16 MMA, 256-row token tiles
+    if (L.epi == EPI_SWIGLU && kernel_tn == 256) return launch_fp8w_pair_variant<EPI_SWIGLU, false>(L, p, s);
+    if (L.epi != EPI_SWIGLU && L.hilo && kernel_tn == 256 && L.mblk == 2)
+      return launch_fp8w_pair_variant<EPI_F32, true>(L, p, s);
+    return cudaErrorInvalidValue;
+  }
   if (L.q8 == 3) {
     // native MXFP4 codes, converted to E4M3 in Tensor Memory, 16-row token tiles
     if (L.epi == EPI_SWIGLU && kernel_tn == 16) return launch_fp4mma_variant<EPI_SWIGLU, 1>(L, p, s);

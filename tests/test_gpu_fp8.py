@@ -70,19 +70,26 @@ def small(w, T, **kw):
     return dataclasses.replace(w, T=T, name=f"{w.name.rsplit('_T', 1)[0]}_T{T}", **kw)
 
 
+# Batches above 64 tokens (prefill) run the CTA-pair kernels that widen the codes to bf16 in shared
+# memory (any d, d_ff multiple of 64); decode batches the direct 8-bit MMA (d, d_ff multiples of
+# 128) or, for other shapes, the single-CTA widening kernels.
 CASES = [
     W.TOY,                                                                  # decode kernels
-    small(W.TOY, 333),                                                      # prefill batch, 64-row sub-tiles
+    small(W.TOY, 333),                                                      # prefill: CTA-pair widening
     W.Workload("mid_T64", T=64, d=512, d_ff=256, E=16, k=4, n_shared=1, score=W.SCORE_SIGMOID, use_bias=True),
     W.Workload("ragged_T150", T=150, d=320, d_ff=192, E=12, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
+    # decode with d, d_ff not multiples of 128: single-CTA widening kernels
+    W.Workload("ragged_T48", T=48, d=320, d_ff=192, E=12, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
+    # decode with 64-row direct-MMA tiles (T k > 24 E)
+    W.Workload("deep_T64", T=64, d=256, d_ff=256, E=16, k=8, n_shared=0, score=W.SCORE_SOFTMAX),
     small(W.V3_T4096, 96, E=32, n_groups=8, topk_groups=4, group_topk=2, d=1024, d_ff=256),
     small(W.V4FLASH_T64, 64, E=16),                                         # V4-Flash dims, 16 experts
     small(W.V4PRO_HASH_T16384, 40, E=24, d=1024, d_ff=384),
-    # direct-MMA path at each schedule width: 16-row tiles (2 mean rows per expert; the shared
-    # expert's 64 rows span four tiles) and 64-row tiles with several tiles per expert
+    # direct-MMA path with 16-row tiles (2 mean rows per expert; the shared expert's 64 rows span
+    # four tiles), and a prefill batch with several 256-row tiles per expert
     W.Workload("wide_T64", T=64, d=512, d_ff=256, E=64, k=2, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
                use_bias=True),
-    W.Workload("tall_T600", T=600, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
+    W.Workload("tall_T1500", T=1500, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
 ]
 
 
@@ -167,10 +174,10 @@ def test_fp8_layer_with_wide_activation_range():
     layer.close()
 
 
-# Full sizes, in the launch configuration bench.py times for FP8 weights (its decode leg):
+# Full sizes, in the launch configuration bench.py times for FP8 weights (its decode and prefill legs):
 # routing against the oracle on every token, the output on a few sampled tokens (the oracle
 # quantises and dequantises every expert those tokens touch, a few seconds each).
-FULL_FP8 = [(W.V4FLASH_T64, 4), (W.MIXTRAL_T16, 2)]
+FULL_FP8 = [(W.V4FLASH_T64, 4), (W.MIXTRAL_T16, 2), (W.V4FLASH_T8192, 32)]
 
 
 @pytest.mark.slow

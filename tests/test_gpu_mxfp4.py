@@ -172,8 +172,14 @@ def run_native(w, seed, sample=None):
     diff = (y.float() - y_conv.float()).abs().max().item()
     print(f"{w.name} (native mxfp4): max elementwise {e:.2e}, normwise {n:.2e}; "
           f"max |native - converted fp8 path| {diff:.2e}")
-    # the same E4M3 values through the same MMA, partials and summation order: bit for bit
-    assert torch.equal(y, y_conv), f"{w.name}: native and converted paths differ by up to {diff:.2e}"
+    if w.T <= 64:
+        # decode: the same E4M3 values through the same MMA, partials and summation order: bit for bit
+        assert torch.equal(y, y_conv), f"{w.name}: native and converted paths differ by up to {diff:.2e}"
+    else:
+        # prefill: the converted weights run the CTA-pair kernels on bf16 activations, the native
+        # ones the E4M3-piece kernels; both are checked against the oracle above, and must agree
+        # with each other within the same tolerance
+        check_output(y.double().cpu().numpy(), y_conv.double().cpu().numpy(), label=f"{w.name} native vs converted")
     layer.close()
 
 
