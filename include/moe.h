@@ -175,9 +175,9 @@ moe_status moe_quantize_fp8(const moe_bf16* w, int32_t n_mats, int32_t rows, int
  * FP8 E4M3 tiles of 128 x 128 while the sub-block scales inside a tile stay within the FP8
  * exponent headroom).
  *   w [n_mats, rows, K] bf16 (device, 16-byte aligned, K a multiple of 32) -> codes
- *   [n_mats, rows, K/2] uint8 (16-byte aligned; eight consecutive elements per little-endian
- *   32-bit word: the index of element k's magnitude in {0, 0.5, 1, 1.5, 2, 3, 4, 6} in bits
- *   4k..4k+2, the sign of element j < 4 in bit 8j+7, that of element 4+j in bit 8j+3) and exps
+ *   [n_mats, rows, K/2] uint8 (16-byte aligned; two elements per byte, element 2i of a row in
+ *   the low nibble of byte i, each nibble an E2M1 code: sign << 3 | the index of the magnitude
+ *   in {0, 0.5, 1, 1.5, 2, 3, 4, 6}) and exps
  *   [n_mats, rows, K/32] int8.  s = the smallest integer with max|w| <= 6 * 2^s over the
  *   sub-block (at least -114), raised to (the largest s of its 128 x 128 tile) - 14 where lower;
  *   an all-zero sub-block takes the tile's largest s.  code = round-to-nearest-even of w * 2^-s
@@ -190,7 +190,7 @@ moe_status moe_quantize_mxfp4(const moe_bf16* w, int32_t n_mats, int32_t rows, i
  * the E4M3 code of q * 2^(s - E), exact because s - E lies in [-8, 6].  codes [n_mats, rows,
  * K/2], exps [n_mats, rows, K/32] -> q8 [n_mats, rows, K] (16-byte aligned), e8 [n_mats,
  * ceil(rows/128), ceil(K/128)], ready for moe_forward_fp8.  q8 may be NULL: only e8 is
- * written (the tile exponents moe_forward_mxfp4 takes).  Exponents from elsewhere that exceed
+ * written.  Exponents from elsewhere that exceed
  * the headroom are rounded to nearest E4M3 (saturating).  Enqueued on `stream`. */
 moe_status moe_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int32_t n_mats, int32_t rows, int32_t K,
                             uint8_t* q8, int8_t* e8, moe_stream_t stream);
@@ -235,22 +235,19 @@ moe_status moe_forward(moe_plan* plan, int32_t T, const moe_bf16* x, const int32
 
 /* moe_forward with native MXFP4 expert weights (the router stays bf16): c13 [E, 2*d_ff, d/2]
  * and c2 [E, d, d_ff/2] packed E2M1 codes, s13 [E, 2*d_ff, d/32] and s2 [E, d, d_ff/32] their
- * sub-block exponents (as moe_quantize_mxfp4 writes them), t13 [E, 2*d_ff/128, d/128] and t2
- * [E, d/128, d_ff/128] the tile exponents of their FP8 form (moe_mxfp4_to_fp8 with q8 = NULL);
- * shared expert the same with E = 1 (NULL without one).  The GEMMs stream the 4-bit codes and
- * turn them into the exact E4M3 values of the FP8 form on the chip, so the layer is the bf16
- * layer on the dequantised weights with the activations as E4M3 pieces (see moe_forward_fp8);
- * for batches of at most 64 tokens it equals moe_forward_fp8 on moe_mxfp4_to_fp8's output bit
- * for bit.  Needs d and d_ff multiples of 128 (else MOE_ERR_UNSUPPORTED); 16-row token tiles, a
- * decode path (at prefill, moe_forward_fp8 on the converted weights is the faster form).
- * Code pointers 16-byte aligned, sub-block exponents 4-byte aligned; same workspace and
- * outputs as moe_forward. */
+ * sub-block exponents, as moe_quantize_mxfp4 writes them; shared expert the same with E = 1
+ * (NULL without one).  The GEMMs feed the stored 4-bit codes to the block-scaled tensor-core MMA
+ * with their 1 x 32 sub-block scales 2^s (as UE8M0 scales, s below -127 taken as -127) and the
+ * activations as E4M3 pieces (see moe_forward_fp8), accumulating in fp32: the layer is the bf16
+ * layer on the dequantised weights q * 2^s up to the pieces' precision and the order of the
+ * fp32 sums.  Needs d and d_ff multiples of 128 (else MOE_ERR_UNSUPPORTED); 16-, 32- or 64-row
+ * token tiles by batch size.  Code pointers 32-byte aligned, sub-block exponents 4-byte aligned
+ * (else MOE_ERR_ALIGNMENT); same workspace and outputs as moe_forward. */
 moe_status moe_forward_mxfp4(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                              const moe_bf16* w_r, const float* bias, const uint8_t* c13, const int8_t* s13,
-                             const int8_t* t13, const uint8_t* c2, const int8_t* s2, const int8_t* t2,
-                             const uint8_t* c13_sh, const int8_t* s13_sh, const int8_t* t13_sh,
-                             const uint8_t* c2_sh, const int8_t* s2_sh, const int8_t* t2_sh, moe_bf16* out,
-                             void* ws, size_t ws_bytes, moe_stream_t stream);
+                             const uint8_t* c2, const int8_t* s2, const uint8_t* c13_sh, const int8_t* s13_sh,
+                             const uint8_t* c2_sh, const int8_t* s2_sh, moe_bf16* out, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
 
 /* Layer forward with the routing given by the caller (topk_ids [T,k] int32 in [0,E),
  * topk_w [T,k] fp32): dispatch, grouped GEMMs and combine only. */

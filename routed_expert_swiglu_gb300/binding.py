@@ -85,7 +85,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward_fp8": ([P, I, V, V, V, V, V, V, V, V, V, V, V, V, V, V, S, V], I),
         "moe_quantize_mxfp4": ([V, I, I, I, V, V, V], I),
         "moe_mxfp4_to_fp8": ([V, V, I, I, I, V, V, V], I),
-        "moe_forward_mxfp4": ([P, I] + [V] * 18 + [S, V], I),
+        "moe_forward_mxfp4": ([P, I] + [V] * 14 + [S, V], I),
     }
     for name, (argt, rest) in sig.items():
         fn = getattr(lib, name)
@@ -219,26 +219,12 @@ def mxfp4_to_fp8(codes, exps, stream=None):
     return q8, e8
 
 
-def mxfp4_tile_exps(codes, exps, stream=None):
-    """The 128 x 128 tile exponents of the FP8 form of MXFP4 weights (moe_mxfp4_to_fp8 without
-    the codes): what moe_forward_mxfp4 takes beside the codes and sub-block exponents."""
-    rows, K = codes.shape[-2], codes.shape[-1] * 2
-    n = 1
-    for v in codes.shape[:-2]:
-        n *= v
-    e8 = torch.empty(tuple(codes.shape[:-2]) + (-(-rows // 128), -(-K // 128)), dtype=torch.int8,
-                     device=codes.device)
-    _check(load().moe_mxfp4_to_fp8(_ptr(codes), _ptr(exps), n, rows, K, None, _ptr(e8), _stream(stream)),
-           "moe_mxfp4_to_fp8")
-    return e8
-
-
 def moe_forward_mxfp4(plan, T, x, token_ids, w_r, bias, w13, w2, w13_sh, w2_sh, out, ws, stream=None):
-    """w13, w2, w13_sh, w2_sh: (codes, sub-block exponents, tile exponents) triples (shared: None
-    without a shared expert)."""
-    def trip(q):
-        return (None, None, None) if q is None else tuple(_ptr(t) for t in q)
-    args = [*trip(w13), *trip(w2), *trip(w13_sh), *trip(w2_sh)]
+    """w13, w2, w13_sh, w2_sh: (codes, sub-block exponents) pairs as quantize_mxfp4 returns them
+    (shared: None without a shared expert)."""
+    def pair(q):
+        return (None, None) if q is None else (_ptr(q[0]), _ptr(q[1]))
+    args = [*pair(w13), *pair(w2), *pair(w13_sh), *pair(w2_sh)]
     _check(load().moe_forward_mxfp4(plan, T, _ptr(x), _ptr(token_ids), _ptr(w_r), _ptr(bias), *args, _ptr(out),
                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_forward_mxfp4")
@@ -361,13 +347,8 @@ class MoELayer:
         """The FP8 form (for forward_fp8) of MXFP4 weights from quantize_mxfp4."""
         return {k: mxfp4_to_fp8(c, e, stream) for k, (c, e) in q4.items()}
 
-    @staticmethod
-    def mxfp4_native(q4, stream=None):
-        """(codes, sub-block exponents, tile exponents) per weight set, for forward_mxfp4."""
-        return {k: (c, e, mxfp4_tile_exps(c, e, stream)) for k, (c, e) in q4.items()}
-
     def forward_mxfp4(self, x, q, token_ids=None, out=None, stream=None):
-        """The layer on native MXFP4 expert weights q (from mxfp4_native)."""
+        """The layer on native MXFP4 expert weights q (from quantize_mxfp4)."""
         T = x.shape[0]
         inp = self.inputs
         if out is None:

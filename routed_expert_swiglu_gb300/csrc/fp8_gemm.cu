@@ -3,8 +3,8 @@
 // per 1 x 32 sub-block, losslessly dequantised to the FP8 form).  Three kernel families:
 //   * fp8mma_gemm_kernel: FP8 codes as the 8-bit MMA's A operand, as stored; the activations as
 //     E4M3 pieces (d and d_ff multiples of 128);
-//   * fp4mma_gemm_kernel: MXFP4 codes turned into the E4M3 bytes of the FP8 form on the chip,
-//     into Tensor Memory, then as fp8mma (same shapes, decode-sized token tiles);
+//   * fp4mma_gemm_kernel: MXFP4 codes as the A operand of the block-scaled MMA, as stored, with
+//     their 1 x 32 sub-block scales applied by the tensor cores; the activations as E4M3 pieces;
 //   * fp8w_gemm_kernel: FP8 codes widened to bf16 into Tensor Memory and multiplied by the bf16
 //     activations (any shape).
 #include "gemm_common.cuh"
@@ -689,47 +689,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ============================================================================ MXFP4 variant
 // Native MXFP4 weights (E2M1 codes, one power-of-two scale 2^s per 1 x 32 sub-block; "DeepSeek-V4
-// MoE", section "FP4 QAT 怎么做到反量化无损": FP4 sub-blocks losslessly dequantised to FP8 E4M3
-// tiles of 128 x 128 for the computation, native FP4 weights at inference).  TMA streams the
-// packed codes (two per byte, 64-byte rows per 128-wide K tile, 64-byte swizzle) with the token
-// rows' E4M3 pieces; groups of four converter warps, one per TMEM lane quadrant, take turns by
-// stage and turn the weight rows into E4M3 bytes of q * 2^(s - E), E the tile's exponent (its
-// largest sub-block exponent - 6, given with the weights), exact since s - E lies in [-8, 6], and
-// store them into a ring of A tiles in Tensor Memory; the 8-bit MMA reads A from there and B (the
-// pieces) from shared memory, and the epilogue is that of the FP8 MMA kernel with 2^E per tile.
-// Four codes become their bytes with one byte permute, which picks the magnitudes from an
-// eight-entry table of E4M3 bytes for the sub-block's s - E; the stored layout keeps the signs
-// where the bytes keep theirs (see moe_quantize_mxfp4), so a mask and an OR add them (about 1.2
-// integer operations per code in all).  Decode-sized token tiles (16 rows).  The integer pipe,
-// not the halved weight stream, bounds it.
+// MoE", section "FP4 QAT 怎么做到反量化无损": FP4 weights with 1 x 32 sub-block scales used
+// natively at inference) on the block-scaled tensor-core MMA (tcgen05.mma kind::mxf8f6f4 with
+// block_scale, one UE8M0 scale per row and per 32 K values of each operand).  TMA streams the
+// stored codes (two per byte) as 16 x 4-bit groups, each unpacked into the low 8 bytes of a 16-byte
+// chunk of shared memory -- the form in which the MMA reads E2M1 -- beside the token rows'
+// E4M3 pieces; the codes reach the tensor cores as they are stored.  The sub-block exponents
+// become the A scales (2^s, UE8M0 s + 127) in Tensor Memory, written per stage by four scale
+// warps; the B scales are the pieces' fixed weights 2^(-4p), so every piece of every stage
+// accumulates into one fp32 accumulator per tile, and the epilogue applies the token rows'
+// exponents 2^e (and the gate weights) once.
+//
+// Scale-factor layout in Tensor Memory, as used here for M = 128 (measured on this part: row m
+// of A takes its scale from lane m, column c0 + m / 32, byte `sfa_id` of the instruction
+// descriptor, c0 the scale address's column; a scale address whose column is not a multiple of
+// 4 raised a misaligned-address fault, so every scale address here is a multiple of 4 columns):
+// the scale warp of lane quadrant q writes its 32 rows' four sub-block scales of a 128-wide K
+// step as one word at column c0 + q, and the four MMAs of the step select bytes 0..3.  The B
+// scales are written uniform (every lane, byte and column of an 8-column region per piece), so
+// their layout does not matter.
 
-// D (+)= A[tmem] * B[smem]^T on 8-bit operands: A's 128 rows in the 128 lanes, K = 32 codes
-// packed four per 32-bit column (8 columns, the lowest k in the lowest byte).
-__device__ __forceinline__ void tc_mma_f8_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t accumulate) {
+// D (+)= (A[smem] . 2^SFA) * (B[smem] . 2^SFB)^T: E2M1 A in the 16-byte-chunk form, E4M3 B, K = 32
+// per instruction, UE8M0 scales read from Tensor Memory at sfa / sfb; issued by one thread.
+__device__ __forceinline__ void tc_mma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
 
-// Store 8 consecutive 32-bit columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
+// Instruction descriptor of kind::mxf8f6f4 with E2M1 A (format 5) and E4M3 B (format 0), fp32
+// accumulator, both K-major, UE8M0 scales (bit 23), M = 128, N = n, B scale byte 0 (bits [4,6)),
+// A scale byte `ida` (bits [29,31)).
+__device__ __forceinline__ uint32_t idesc_mx_e2m1_e4m3(uint32_t n, uint32_t ida) {
+  return (5u << 7)                // A format E2M1, bits [7,10)
+         | ((n >> 3) << 17)       // N >> 3, bits [17,23)
+         | (1u << 23)             // scale format UE8M0
+         | ((128u >> 4) << 24)    // M >> 4, bits [24,29)
+         | (ida << 29);           // A scale byte, bits [29,31)
 }
 
-// Eight stored E2M1 codes (one word: the magnitude index of code k in bits 4k..4k+2, the sign
-// of code j < 4 in bit 8j+7, that of code 4+j in bit 8j+3) -> eight E4M3 bytes (two words, low
-// word first) with the magnitude table lut (bytes 0..7 of lut_lo, lut_hi): one byte permute
-// picks four magnitudes, the signs are already where the bytes keep theirs.
-__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
-  const uint32_t m_lo = __byte_perm(lut_lo, lut_hi, w & 0x7777u);          // magnitudes of codes 0..3
-  const uint32_t m_hi = __byte_perm(lut_lo, lut_hi, (w >> 16) & 0x7777u);  // codes 4..7
-  return make_uint2(m_lo | (w & 0x80808080u), m_hi | ((w << 4) & 0x80808080u));
+// Store one 32-bit column of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
 // The parameter block plus the MXFP4 sub-block exponents [mats, rows, K/32] (int8) of the routed
@@ -739,92 +745,80 @@ struct Fp4Params : GemmParams {
   const int8_t* a_sh_sub;
 };
 
-// Converter groups of the MXFP4 kernel (four warps each).  The conversion is bound by the
-// integer pipe: 2, 3 and 4 groups measured alike (V4-Flash T=64: 0.827 / 0.830 / 0.874 ms); 2
-// leave the epilogue room (96 registers) to sum the pieces exactly as the FP8 kernel does.
-#ifndef MOE_F4_CVT_GROUPS
-#define MOE_F4_CVT_GROUPS 2
-#endif
-
-template <int EPI, int MBLK>
+template <int EPI, int MBLK, int TN_>
 struct F4Shape {
-  static constexpr int TN = 16;
-  static constexpr int BLOCK_K = 128;                   // codes per stage (one FP8 tile of K)
+  static constexpr int TN = TN_;
+  static constexpr int BLOCK_K = 128;                    // codes per stage: one TMA box, four MMAs
   static constexpr int NUM_A = (EPI == EPI_SWIGLU) ? 2 : MBLK;
-  static constexpr int RAW_SLAB = BLOCK_M * BLOCK_K / 2;  // 128 rows x 64 bytes of codes
-  static constexpr int RAW_A = NUM_A * RAW_SLAB;
+  static constexpr int A_SLAB = BLOCK_M * BLOCK_K;       // 128 rows x 128 bytes (codes in 16-byte chunks)
+  static constexpr int A_BYTES = NUM_A * A_SLAB;
   static constexpr int PIECES = (EPI == EPI_SWIGLU) ? 2 : 4;
-  static constexpr int B_PIECE = TN * BLOCK_K;          // 16 token rows x 128 E4M3 codes
-  static constexpr int RAW_STAGE = RAW_A + PIECES * B_PIECE;
-  static constexpr int A_COLS = BLOCK_K / 4;            // TMEM columns of one converted slab
-  static constexpr int CSTAGES = MOE_F4_CVT_GROUPS;     // converted stages in Tensor Memory
-  static constexpr int CVT_GROUPS = CSTAGES;            // group g converts every CSTAGES-th stage
-  static constexpr int NUM_CVT_WARPS = 4 * CVT_GROUPS;
-  static constexpr int THREADS = (2 + NUM_EPI_WARPS + NUM_CVT_WARPS) * 32;
-  static constexpr int A_RING_COLS = CSTAGES * NUM_A * A_COLS;
-  static constexpr int SLOT_COLS = NUM_A * PIECES * TN;
-  static constexpr int SLOTS = ((512 - A_RING_COLS) / SLOT_COLS) > 8 ? 8 : ((512 - A_RING_COLS) / SLOT_COLS);
-  static constexpr int A_COL0 = SLOTS * SLOT_COLS;      // first column of the A ring
-  static constexpr int RSTAGES_FIT = (SMEM_LIMIT - 1024 - 512) / RAW_STAGE;
-  static constexpr int RSTAGES = RSTAGES_FIT > 8 ? 8 : RSTAGES_FIT;
-  static constexpr int SMEM_BYTES = RSTAGES * RAW_STAGE + 1024 + 512;
+  static constexpr int B_PIECE = TN * BLOCK_K;           // TN token rows x 128 E4M3 codes
+  static constexpr int STAGE = A_BYTES + PIECES * B_PIECE;
+  static constexpr int TX_BYTES = A_BYTES / 2 + PIECES * B_PIECE;  // bytes a stage's TMA loads move
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - 512) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 + 512;
+  // Decode-sized tiles (TN <= 32) put the pieces side by side in N: one MMA per slab and K step
+  // covers every piece, each into its own accumulator columns, summed by the epilogue (so the
+  // B scales are all 1).  Wider tiles issue one MMA per piece into one accumulator per slab, the
+  // piece's weight 2^(-4p) applied as its B scale.
+  static constexpr bool PIN = TN <= 32;
+  static constexpr int ACC_COLS = NUM_A * (PIN ? PIECES : 1) * TN;   // one accumulator buffer
+  static constexpr int SFB_REGIONS = PIN ? 1 : PIECES;
+  static constexpr int SFB_COLS = 8;                     // one B-scale region
+  static constexpr int SFA_COLS = STAGES * NUM_A * 4;    // per stage and slab: one column per lane quadrant
+  static constexpr int NUM_BUF = (2 * ACC_COLS + SFB_REGIONS * SFB_COLS + SFA_COLS <= 512) ? 2 : 1;
+  static constexpr int SFB_COL0 = NUM_BUF * ACC_COLS;    // after the accumulator buffers
+  static constexpr int SFA_COL0 = SFB_COL0 + SFB_REGIONS * SFB_COLS;
+  static constexpr int TMEM_COLS = (SFA_COL0 + SFA_COLS <= 256) ? 256 : 512;
+  static constexpr int SF_WARP0 = 2 + NUM_EPI_WARPS;     // four scale warps after the epilogue warps
+  static constexpr int THREADS = (SF_WARP0 + 4) * 32;
   static constexpr int FEATS = (EPI == EPI_SWIGLU) ? BLOCK_M : BLOCK_M * MBLK;
-  static_assert(SLOTS >= 2 && A_COL0 + A_RING_COLS <= 512, "TMEM: partial slots + A ring");
-  static_assert(RSTAGES >= 2, "pipeline needs two raw stages");
-  static_assert(RAW_SLAB % 1024 == 0 && RAW_STAGE % 1024 == 0, "swizzled tiles on 1024 B");
-  static_assert((2 * RSTAGES + 2 * CSTAGES + 2 * SLOTS) * 8 + 8 <= 512, "barrier area");
+  static_assert(TN % 16 == 0 && TN <= 64, "token tile");
+  static_assert(!PIN || PIECES * TN <= 256, "MMA N");
+  static_assert(STAGES >= 2, "pipeline needs two stages");
+  static_assert(A_SLAB % 1024 == 0 && B_PIECE % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles on 1024 B");
+  static_assert(SFB_COL0 % 4 == 0 && SFA_COL0 % 4 == 0, "scale addresses on 4-column boundaries");
+  static_assert(SFA_COL0 + SFA_COLS <= TMEM_COLS, "TMEM: accumulators + scales");
+  static_assert((3 * STAGES + 4) * 8 + 8 <= 512, "barrier area");
   static_assert(EPI == EPI_F32 || MBLK == 1, "SwiGLU variant");
-  static_assert(PIECES == 2 || PIECES == 4, "pieces are summed in pairs");
 };
 
-template <int EPI, int MBLK>
-__global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
+template <int EPI, int MBLK, int TN_>
+__global__ void __launch_bounds__(F4Shape<EPI, MBLK, TN_>::THREADS, 1)
     fp4mma_gemm_kernel(const __grid_constant__ GemmMaps maps, const Fp4Params p) {
-  using S = F4Shape<EPI, MBLK>;
+  using S = F4Shape<EPI, MBLK, TN_>;
   constexpr int TN = S::TN;
-  constexpr int RST = S::RSTAGES;
-  constexpr int CST = S::CSTAGES;
-  constexpr int SL = S::SLOTS;
+  constexpr int ST = S::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint2 s_lut[15];  // E4M3 bytes of the eight E2M1 magnitudes times 2^t, t = -8 .. 6
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* raw = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + RST * S::RAW_STAGE);
-  // bars: full[RST], empty[RST], cfull[CST], cempty[CST], slot_full[SL], slot_empty[SL]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RST + 2 * CST + 2 * SL);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ST * S::STAGE);
+  // bars: full[ST], empty[ST], sfull[ST], accf[2], acce[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * ST + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (RST + s); };
-  auto cfull_bar = [&](int c) { return bar0 + 8u * (2 * RST + c); };
-  auto cempty_bar = [&](int c) { return bar0 + 8u * (2 * RST + CST + c); };
-  auto sfull_bar = [&](int c) { return bar0 + 8u * (2 * RST + 2 * CST + c); };
-  auto sempty_bar = [&](int c) { return bar0 + 8u * (2 * RST + 2 * CST + SL + c); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (ST + s); };
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * ST + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (3 * ST + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (3 * ST + 2 + a); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RST; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sfull_bar(s), 4);  // one arrival per scale warp
     }
-    for (int c = 0; c < CST; ++c) {
-      mbar_init(cfull_bar(c), 4 * 32);  // the four warps of the slot's converter group
-      mbar_init(cempty_bar(c), 1);
-    }
-    for (int c = 0; c < SL; ++c) {
-      mbar_init(sfull_bar(c), 1);
-      mbar_init(sempty_bar(c), NUM_EPI_WARPS);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), NUM_EPI_WARPS);
     }
     *abort_flag = 0;
     fence_barrier_init();
-  }
-  if (threadIdx.x < 15 * 8) {  // the magnitude tables, one byte per thread
-    const int t = threadIdx.x / 8 - 8, idx = threadIdx.x % 8;
-    const float mag = idx < 2 ? 0.5f * (float)idx : ldexpf((idx & 1) ? 1.5f : 1.0f, (idx >> 1) - 1);
-    reinterpret_cast<uint8_t*>(s_lut)[threadIdx.x] =
-        idx == 0 ? 0 : (uint8_t)__nv_cvt_float_to_fp8(ldexpf(mag, t), __NV_SATFINITE, __NV_E4M3);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&maps.a);
@@ -832,13 +826,26 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
     tma_prefetch_desc(&maps.b[0]);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (warp >= S::SF_WARP0) {
+    // B scales: region p holds 2^(-4p) (UE8M0 127 - 4p; a single region of 1 with the pieces
+    // along N), the same in every lane, byte and column of the region
+    const uint32_t tq = tmem_base + (uint32_t((warp & 3) * 32) << 16) + S::SFB_COL0;
+#pragma unroll
+    for (int pc = 0; pc < S::SFB_REGIONS; ++pc)
+#pragma unroll
+      for (int c = 0; c < S::SFB_COLS; ++c) tmem_st1(tq + pc * S::SFB_COLS + c, (127u - 4u * pc) * 0x01010101u);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   const int row_tiles = p.grp != nullptr ? __ldg(&p.grp[p.n_groups_total].z)
                                          : (p.dense_rows + p.sched_tn - 1) / p.sched_tn;
@@ -856,24 +863,25 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
         if (t.rows <= 0) continue;
         const CUtensorMap* ta = t.shared ? &maps.a_sh : &maps.a;
         const int a_row = (t.shared ? 0 : t.g * p.a_rows_per_group) + t.mb * S::FEATS;
-        const uint32_t bytes = S::RAW_A + S::PIECES * t.n_mma * S::BLOCK_K;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
+          const uint32_t sr = smem_u32(smem + stage * S::STAGE);
           const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, bytes);
+          // transaction bytes: the codes as stored (4 bits each; the gaps in shared memory do not
+          // count) and the pieces
+          mbar_arrive_expect_tx(fb, S::TX_BYTES);
           if (EPI == EPI_SWIGLU) {
-            tma_load_3d(sr, ta, fb, kb * (S::BLOCK_K / 2), t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);
+            tma_load_3d(sr, ta, fb, kb * S::BLOCK_K, t.mb * BLOCK_M, t.shared ? 0 : 2 * t.g);  // gate, up
           } else {
-            tma_load_2d(sr, ta, fb, kb * (S::BLOCK_K / 2), a_row);
+            tma_load_2d(sr, ta, fb, kb * S::BLOCK_K, a_row);                                   // MBLK slabs
           }
 #pragma unroll
           for (int pc = 0; pc < S::PIECES; ++pc)
-            tma_load_3d(sr + S::RAW_A + pc * t.n_mma * S::BLOCK_K, &maps.b[0], fb, kb * S::BLOCK_K, pc, t.b_row);
-          if (++stage == RST) {
+            tma_load_3d(sr + S::A_BYTES + pc * S::B_PIECE, &maps.b[0], fb, kb * S::BLOCK_K, pc, t.b_row);
+          if (++stage == ST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -884,217 +892,205 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0, cs = 0, slot = 0;
-      uint32_t phase = 0, cphase = 0, sphase = 0;
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, buf_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const Tile t = decode_tile<TN>(tile, p);
         if (t.rows <= 0) continue;
-        const uint32_t idesc = idesc_e4m3_f32(S::PIECES * t.n_mma);
+        if (!mbar_wait(acce_bar(buf), buf_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + buf * S::ACC_COLS;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
-              !mbar_wait(cfull_bar(cs), cphase, abort_flag, p.err) ||
-              !mbar_wait(sempty_bar(slot), sphase ^ 1u, abort_flag, p.err)) {
+              !mbar_wait(sfull_bar(stage), phase, abort_flag, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sr = smem_u32(raw + stage * S::RAW_STAGE);
-          const uint32_t d0 = tmem_base + slot * S::SLOT_COLS;
-          const uint32_t ta = tmem_base + S::A_COL0 + cs * (S::NUM_A * S::A_COLS);
+          const uint32_t sr = smem_u32(smem + stage * S::STAGE);
+          const uint32_t sfa0 = tmem_base + S::SFA_COL0 + stage * S::NUM_A * 4;
 #pragma unroll
           for (int kk = 0; kk < S::BLOCK_K / 32; ++kk) {
-            const uint64_t db = smem_desc_sw(sr + S::RAW_A, 128) + 2 * kk;
 #pragma unroll
-            for (int a = 0; a < S::NUM_A; ++a)
-              tc_mma_f8_ta(d0 + a * S::PIECES * TN, ta + a * S::A_COLS + kk * 8, db, idesc, kk ? 1u : 0u);
+            for (int a = 0; a < S::NUM_A; ++a) {
+              const uint64_t ad = smem_desc_sw(sr + a * S::A_SLAB, 128) + 2 * kk;
+              if (S::PIN) {  // all pieces (PIECES * TN rows of B) into piece-wise accumulator columns
+                const uint64_t bd = smem_desc_sw(sr + S::A_BYTES, 128) + 2 * kk;
+                tc_mma_mx(d0 + a * S::PIECES * TN, ad, bd, idesc_mx_e2m1_e4m3(S::PIECES * TN, kk), sfa0 + a * 4,
+                          tmem_base + S::SFB_COL0, (kb | kk) ? 1u : 0u);
+              } else {
+#pragma unroll
+                for (int pc = 0; pc < S::PIECES; ++pc) {
+                  const uint64_t bd = smem_desc_sw(sr + S::A_BYTES + pc * S::B_PIECE, 128) + 2 * kk;
+                  tc_mma_mx(d0 + a * TN, ad, bd, idesc_mx_e2m1_e4m3(t.n_mma, kk), sfa0 + a * 4,
+                            tmem_base + S::SFB_COL0 + pc * S::SFB_COLS, (kb | kk | pc) ? 1u : 0u);
+                }
+              }
+            }
           }
           tc_commit(empty_bar(stage));
-          tc_commit(cempty_bar(cs));
-          tc_commit(sfull_bar(slot));
-          if (++stage == RST) {
+          if (++stage == ST) {
             stage = 0;
             phase ^= 1u;
           }
-          if (++cs == CST) {
-            cs = 0;
-            cphase ^= 1u;
-          }
-          if (++slot == SL) {
-            slot = 0;
-            sphase ^= 1u;
-          }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(buf));
+        if (++buf == S::NUM_BUF) {
+          buf = 0;
+          buf_phase ^= 1u;
         }
       }
     }
     __syncwarp();
-  } else if (warp < 2 + NUM_EPI_WARPS) {
+  } else if (warp < S::SF_WARP0) {
     // ------------------------------------------------------------------ epilogue
-    // Warps of half 0 hold the 16 token columns (half 1 has none with 16-row tiles but keeps
-    // the slot protocol).
-    const int ew = warp - 2;
+    // Warp w reads TMEM lane quadrant w % 4 (weight rows 32 (w % 4) + lane) and the 16-column
+    // chunks of its half; each column (a token row) is scaled by 2^e of the row's pieces (and,
+    // in the down projection, by the row's gate weight).
     const int quad = warp & 3;
-    const int half = ew >> 2;
-    int slot = 0;
-    uint32_t sphase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+    const int half = (warp - 2) >> 2;
+    int buf = 0;
+    uint32_t buf_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<TN>(tile, p);
       if (t.rows <= 0) continue;
-      const bool mine = half == 0;
-      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
-      int erow[S::NUM_A];
+      if (!mbar_wait(accf_bar(buf), buf_phase, abort_flag, p.err)) break;
+      tc_fence_after();
+      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16) + buf * S::ACC_COLS;
+      const int nchunk = (t.rows + 15) >> 4;
+      for (int ci = half; ci < nchunk; ci += 2) {
+        const int c0 = ci * 16;
+        const int nr = min(16, t.rows - c0);
+        const bool rvalid = lane < nr;
+        float cs_l = rvalid ? __int_as_float((127 + __ldg(p.b_exp + t.b_row + c0 + lane)) << 23) : 0.0f;
+        if (EPI == EPI_F32 && p.row_scale != nullptr && !t.shared && rvalid)
+          cs_l *= __ldg(p.row_scale + t.out_row + c0 + lane);
+        // slab a's 16 columns at c0, the pieces summed with weights 2^(-4p) where they lie along N
+        auto load_slab = [&](int a, float(&v)[16]) {
+          if (S::PIN) {
+            uint32_t r[S::PIECES][16];
 #pragma unroll
-      for (int a = 0; a < S::NUM_A; ++a) {
-        const int base = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M : t.mb * S::FEATS + a * BLOCK_M;
-        erow[a] = min(base >> 7, p.exp_nr - 1) * p.exp_nk;
-      }
-      float acc[S::NUM_A][16];
+            for (int pc = 0; pc < S::PIECES; ++pc) tmem_ld16(tq + (a * S::PIECES + pc) * TN + c0, r[pc]);
+            tmem_ld_wait();
 #pragma unroll
-      for (int a = 0; a < S::NUM_A; ++a)
+            for (int pc = 0; pc < S::PIECES; ++pc) reg_fence16(r[pc]);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[a][j] = 0.0f;
-      int e_cur[S::NUM_A];
+            for (int j = 0; j < 16; ++j) {
+              float x = fmaf(__uint_as_float(r[1][j]), 0.0625f, __uint_as_float(r[0][j]));
+              if (S::PIECES == 4)
+                x = fmaf(fmaf(__uint_as_float(r[S::PIECES - 1][j]), 0.0625f, __uint_as_float(r[S::PIECES - 2][j])),
+                         0.00390625f, x);
+              v[j] = x;
+            }
+          } else {
+            uint32_t r[16];
+            tmem_ld16(tq + a * TN + c0, r);
+            tmem_ld_wait();
+            reg_fence16(r);
 #pragma unroll
-      for (int a = 0; a < S::NUM_A; ++a) e_cur[a] = __ldg(ex + erow[a]);
-      const uint32_t tq = tmem_base + (uint32_t(quad * 32) << 16);
-      for (int kb = 0; kb < KB; ++kb) {
-        int e_nxt[S::NUM_A];
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          }
+        };
+        float cs[16];  // the columns' scales
 #pragma unroll
-        for (int a = 0; a < S::NUM_A; ++a) e_nxt[a] = (kb + 1 < KB) ? __ldg(ex + erow[a] + kb + 1) : 0;
-        if (!mbar_wait(sfull_bar(slot), sphase, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (mine) {
-          const uint32_t ts = tq + slot * S::SLOT_COLS;
+        for (int j = 0; j < 16; ++j) cs[j] = __shfl_sync(0xffffffffu, cs_l, j);
+        const bool skip = p.out_rows > 0 && (bad_index(t.out_row + c0, p.out_rows, p.err) ||
+                                             bad_index(t.out_row + c0 + nr - 1, p.out_rows, p.err));
+        float* out = static_cast<float*>(p.out) + (size_t)(t.out_row + c0) * p.out_ld;
+        if (EPI == EPI_SWIGLU) {
+          float g[16], u[16];
+          load_slab(0, g);
+          load_slab(1, u);
+          const int feat = t.mb * BLOCK_M + quad * 32 + lane;
+          if (!skip && feat < p.out_features) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (j < nr) {
+                const float gj = g[j] * cs[j], uj = u[j] * cs[j];
+                out[(size_t)j * p.out_ld + feat] = __fdividef(gj, 1.0f + __expf(-gj)) * uj;
+              }
+            }
+          }
+        } else {
 #pragma unroll
           for (int a = 0; a < S::NUM_A; ++a) {
-            const float sc = __int_as_float((e_cur[a] + 127) << 23);  // 2^E, E in [-126, 121]
-#pragma unroll
-            for (int pp = 0; pp < S::PIECES; pp += 2) {  // two pieces per wait, summed as in the FP8 kernel
-              const float scp = sc * (pp == 0 ? 1.0f : 0.00390625f);  // 2^E * 2^(-4 pp), exact
-              uint32_t r0[2][16];
-#pragma unroll
-              for (int q = 0; q < 2; ++q) tmem_ld16(ts + a * S::PIECES * TN + (pp + q) * t.n_mma, r0[q]);
-              tmem_ld_wait();
-              reg_fence16(r0[0]);
-              reg_fence16(r0[1]);
+            float v[16];
+            load_slab(a, v);
+            const int feat = t.mb * S::FEATS + a * BLOCK_M + quad * 32 + lane;
+            if (!skip && feat < p.out_features) {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                acc[a][j] = fmaf(fmaf(__uint_as_float(r0[1][j]), 0.0625f, __uint_as_float(r0[0][j])), scp, acc[a][j]);
+                if (j < nr) out[(size_t)j * p.out_ld + feat] = v[j] * cs[j];
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sempty_bar(slot));
-#pragma unroll
-        for (int a = 0; a < S::NUM_A; ++a) e_cur[a] = e_nxt[a];
-        if (++slot == SL) {
-          slot = 0;
-          sphase ^= 1u;
-        }
       }
-      if (!ok || !mine) continue;
-      const int cols = min(16, t.rows);
-      const bool rvalid = lane < t.rows;
-      const int er = rvalid ? __ldg(p.b_exp + t.b_row + lane) : 0;
-      float cs_l = __int_as_float((127 + er) << 23);  // 2^e_r, e_r in [-126, 120]
-      if (EPI == EPI_F32 && p.row_scale != nullptr && !t.shared && rvalid) cs_l *= __ldg(p.row_scale + t.out_row + lane);
-      float* out = static_cast<float*>(p.out) + (size_t)t.out_row * p.out_ld;
-      if (EPI == EPI_SWIGLU) {
-        const int feat = t.mb * BLOCK_M + quad * 32 + lane;
-        const bool fvalid = feat < p.out_features;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float cs = __shfl_sync(0xffffffffu, cs_l, j);
-          if (j < cols && fvalid) {
-            const float g = acc[0][j] * cs, u = acc[1][j] * cs;
-            out[(size_t)j * p.out_ld + feat] = __fdividef(g, 1.0f + __expf(-g)) * u;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float cs = __shfl_sync(0xffffffffu, cs_l, j);
-#pragma unroll
-          for (int a = 0; a < S::NUM_A; ++a) {
-            const int feat = t.mb * S::FEATS + a * BLOCK_M + quad * 32 + lane;
-            if (j < cols && feat < p.out_features) out[(size_t)j * p.out_ld + feat] = acc[a][j] * cs;
-          }
-        }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+      if (++buf == S::NUM_BUF) {
+        buf = 0;
+        buf_phase ^= 1u;
       }
     }
   } else {
-    // ------------------------------------------------------------------ E2M1 -> E4M3 converters
-    // Group g converts the stages n with n % CVT_GROUPS == g into A slot g; warp w owns TMEM lane
-    // quadrant w % 4, i.e. weight rows r = 32 (w % 4) + lane of every slab: the thread reads the
-    // row's 64 code bytes (four 16-byte chunks, chunk c of row r at c ^ ((r >> 1) & 3), the
-    // 64-byte swizzle TMA wrote), i.e. four sub-blocks of 32 codes, and stores 32 columns of
-    // E4M3 bytes per slab.
+    // ------------------------------------------------------------------ A-scale writers
+    // Warp w owns TMEM lane quadrant q = w % 4, i.e. weight rows r = 32 q + lane of every slab.
+    // For each stage the thread loads the row's four sub-block exponents s of the stage's 128 K
+    // values (one word, byte j = sub-block j), turns them into UE8M0 bytes s + 127 (s below -127,
+    // values under 2^-127 * 6, taken as -127) and stores the word at column q of the stage's
+    // slot of each slab, once the stage's previous MMAs have completed (the stage's empty barrier).
     const int quad = warp & 3;
-    const int group = (warp - 2 - NUM_EPI_WARPS) >> 2;
     const int r = quad * 32 + lane;
-    const uint32_t ta = tmem_base + (uint32_t(quad * 32) << 16) + S::A_COL0 + group * (S::NUM_A * S::A_COLS);
     const int kb32 = p.K / 32;  // sub-blocks per weight row
-    uint32_t n = 0, mine = 0;
+    int stage = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<TN>(tile, p);
       if (t.rows <= 0) continue;
-      const int8_t* ex = t.shared ? p.a_sh_exp : p.a_exp + (size_t)t.g * p.exp_nr * p.exp_nk;
       const int8_t* sub = t.shared ? p.a_sh_sub : p.a_sub + (size_t)t.g * p.a_rows_per_group * kb32;
-      int srow[S::NUM_A], erow[S::NUM_A];
+      const uint32_t* srow[S::NUM_A];
 #pragma unroll
       for (int a = 0; a < S::NUM_A; ++a) {
         const int base = (EPI == EPI_SWIGLU) ? a * p.a_up_offset + t.mb * BLOCK_M : t.mb * S::FEATS + a * BLOCK_M;
         const int row = min(base + r, p.a_rows_per_group - 1);  // rows past the matrix: any valid row
-        srow[a] = row * kb32;
-        erow[a] = min(base >> 7, p.exp_nr - 1) * p.exp_nk;
+        srow[a] = reinterpret_cast<const uint32_t*>(sub + (size_t)row * kb32);
       }
-      for (int kb = 0; kb < KB; ++kb, ++n) {
-        if ((int)(n % S::CVT_GROUPS) != group) continue;
-        // this stage's sub-block exponents (four bytes per slab) and tile exponents, loaded
-        // before the waits
-        uint32_t s4[S::NUM_A];
-        int E[S::NUM_A];
+      // the rows' exponents into L2 at the tile's start, then each stage's word loaded one stage
+      // ahead, so that no exponent load sits in a stage's critical path
+      uint32_t nxt[S::NUM_A];
+#pragma unroll
+      for (int a = 0; a < S::NUM_A; ++a) {
+        for (int o = 0; o < kb32; o += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const int8_t*>(srow[a]) + o));
+        nxt[a] = __ldg(srow[a]);
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        uint32_t w[S::NUM_A];
 #pragma unroll
         for (int a = 0; a < S::NUM_A; ++a) {
-          s4[a] = __ldg(reinterpret_cast<const uint32_t*>(sub + srow[a] + kb * 4));
-          E[a] = __ldg(ex + erow[a] + kb);
+          w[a] = __vadd4(__vmaxs4(nxt[a], 0x81818181u), 0x7F7F7F7Fu);
+          if (kb + 1 < KB) nxt[a] = __ldg(srow[a] + kb + 1);
         }
-        const int stage = (int)(n % RST);
-        const uint32_t phase = (n / RST) & 1u;
-        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err) ||
-            !mbar_wait(cempty_bar(group), (mine & 1u) ^ 1u, abort_flag, p.err)) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        ++mine;
         tc_fence_after();
-        const uint8_t* src = raw + stage * S::RAW_STAGE;
+        const uint32_t ts = tmem_base + (uint32_t(quad * 32) << 16) + S::SFA_COL0 + stage * S::NUM_A * 4 + quad;
 #pragma unroll
-        for (int a = 0; a < S::NUM_A; ++a) {
-          const uint8_t* row = src + a * S::RAW_SLAB + r * 64;
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {  // sub-block b: 32 codes -> 8 columns
-            int tix = (int)(int8_t)(s4[a] >> (8 * b)) - E[a] + 8;  // s - E + 8, in [0, 14]
-            tix = min(max(tix, 0), 14);
-            const uint2 lut = s_lut[tix];
-            const uint4 q = *reinterpret_cast<const uint4*>(row + ((b ^ ((r >> 1) & 3)) << 4));
-            const uint2 v0 = e2m1x8_to_e4m3x8(q.x, lut.x, lut.y);
-            const uint2 v1 = e2m1x8_to_e4m3x8(q.y, lut.x, lut.y);
-            const uint2 v2 = e2m1x8_to_e4m3x8(q.z, lut.x, lut.y);
-            const uint2 v3 = e2m1x8_to_e4m3x8(q.w, lut.x, lut.y);
-            const uint32_t o[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
-            tmem_st8(ta + a * S::A_COLS + b * 8, o);
-          }
-        }
+        for (int a = 0; a < S::NUM_A; ++a) tmem_st1(ts + a * 4, w[a]);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(cfull_bar(group));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfull_bar(stage));
+        if (++stage == ST) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   }
@@ -1103,7 +1099,7 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK>::THREADS, 1)
   sync_and_quiesce(abort_flag);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
   }
 }
 
@@ -1584,6 +1580,36 @@ static bool make_tmap_pieces(CUtensorMap* m, const void* ptr, int64_t rows, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP4 codes, two E2M1 codes per byte (code 2i in the low nibble of byte i), row-major [rows,
+// K]: each group of 16 codes (8 bytes) lands in the low half of a 16-byte chunk of shared memory
+// (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B), the form the block-scaled MMA reads; boxes of 128
+// codes (one 128-byte row of shared memory) x box_rows rows, 128-byte swizzle.  The gate/up view
+// is 3-D (K, d_ff, 2*groups) with boxes (128, 128, 2).  The type wants K a multiple of 128,
+// row strides a multiple of 32 bytes and a 32-byte aligned base.
+static bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_tmap_e2m1_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t K) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
+  cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)(d_ff * K / 2)};
+  cuuint32_t box[3] = {128, (cuuint32_t)BLOCK_M, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI, int TN, int MBLK, bool HILO>
 static cudaError_t launch_fp8_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
   using Sh = Fp8Shape<EPI, TN, MBLK, HILO>;
@@ -1667,43 +1693,40 @@ static cudaError_t launch_fp8mma_variant(const GemmLaunch& L, GemmParams p, cuda
   return cudaGetLastError();
 }
 
-template <int EPI, int MBLK>
+template <int EPI, int MBLK, int TN>
 static cudaError_t launch_fp4mma_variant(const GemmLaunch& L, GemmParams base, cudaStream_t s) {
-  using Sh = F4Shape<EPI, MBLK>;
+  using Sh = F4Shape<EPI, MBLK, TN>;
   static_assert(Sh::SMEM_BYTES <= SMEM_LIMIT, "dynamic shared memory per block");
-  if (base.sched_tn != Sh::TN || L.K % Sh::BLOCK_K != 0 || base.ksplit != 1) return cudaErrorInvalidValue;
-  if (L.a_exp == nullptr || L.a_sub == nullptr || L.b_exp == nullptr) return cudaErrorInvalidValue;
-  if (L.a_sh_ptr != nullptr && (L.a_sh_exp == nullptr || L.a_sh_sub == nullptr)) return cudaErrorInvalidValue;
-  if (EPI == EPI_SWIGLU && L.a_up_offset % 128 != 0) return cudaErrorInvalidValue;  // slabs on scale tiles
+  if (base.sched_tn % TN != 0 || L.K % Sh::BLOCK_K != 0 || base.ksplit != 1) return cudaErrorInvalidValue;
+  if (L.a_sub == nullptr || L.b_exp == nullptr) return cudaErrorInvalidValue;
+  if (L.a_sh_ptr != nullptr && L.a_sh_sub == nullptr) return cudaErrorInvalidValue;
+  if (EPI == EPI_SWIGLU && L.a_up_offset % 128 != 0) return cudaErrorInvalidValue;  // slabs on 128-row boundaries
+  if (reinterpret_cast<uintptr_t>(L.a_ptr) % 32 != 0 || reinterpret_cast<uintptr_t>(L.a_sh_ptr) % 32 != 0)
+    return cudaErrorInvalidValue;  // the 4-bit tensor maps want 32-byte aligned codes
   GemmMaps m;
   memset(&m, 0, sizeof(m));
-  const int64_t kc = L.K / 2;  // code bytes per weight row
   if (EPI == EPI_SWIGLU) {
     const int64_t f = L.a_up_offset;
-    if (!make_tmap_u8_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, kc, 64)) return cudaErrorInvalidValue;
-    if (L.a_sh_ptr != nullptr && !make_tmap_u8_gateup(&m.a_sh, L.a_sh_ptr, 1, f, kc, 64))
-      return cudaErrorInvalidValue;
+    if (!make_tmap_e2m1_gateup(&m.a, L.a_ptr, L.a_rows / (2 * f), f, L.K)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_e2m1_gateup(&m.a_sh, L.a_sh_ptr, 1, f, L.K)) return cudaErrorInvalidValue;
   } else {
-    if (!make_tmap_u8(&m.a, L.a_ptr, L.a_rows, kc, BLOCK_M * MBLK, 64)) return cudaErrorInvalidValue;
-    if (L.a_sh_ptr != nullptr && !make_tmap_u8(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, kc, BLOCK_M * MBLK, 64))
+    if (!make_tmap_e2m1(&m.a, L.a_ptr, L.a_rows, L.K, BLOCK_M * MBLK)) return cudaErrorInvalidValue;
+    if (L.a_sh_ptr != nullptr && !make_tmap_e2m1(&m.a_sh, L.a_sh_ptr, L.a_sh_rows, L.K, BLOCK_M * MBLK))
       return cudaErrorInvalidValue;
   }
   if (L.a_sh_ptr == nullptr) m.a_sh = m.a;
-  if (!make_tmap_pieces(&m.b[0], L.b_ptr, L.b_rows, Sh::PIECES, L.K, Sh::TN)) return cudaErrorInvalidValue;
+  if (!make_tmap_pieces(&m.b[0], L.b_ptr, L.b_rows, Sh::PIECES, L.K, TN)) return cudaErrorInvalidValue;
   Fp4Params p;
   static_cast<GemmParams&>(p) = base;
-  p.a_exp = L.a_exp;
-  p.a_sh_exp = L.a_sh_exp != nullptr ? L.a_sh_exp : L.a_exp;
-  p.exp_nr = (L.a_rows_per_group + 127) / 128;
-  p.exp_nk = (L.K + 127) / 128;
   p.b_exp = L.b_exp;
   p.a_sub = L.a_sub;
   p.a_sh_sub = L.a_sh_sub != nullptr ? L.a_sh_sub : L.a_sub;
-  auto kern = fp4mma_gemm_kernel<EPI, MBLK>;
+  auto kern = fp4mma_gemm_kernel<EPI, MBLK, TN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   int grid = L.num_sms;
-  if (L.max_tiles < grid) grid = L.max_tiles;
+  const int tiles = L.max_tiles * (base.sched_tn / TN);
+  if (tiles < grid) grid = tiles;
   if (grid < 1) grid = 1;
   kern<<<grid, Sh::THREADS, Sh::SMEM_BYTES, s>>>(m, p);
   return cudaGetLastError();
@@ -1789,9 +1812,14 @@ cudaError_t launch_fp8_gemm(const GemmLaunch& L, GemmParams p, int kernel_tn, cu
     return cudaErrorInvalidValue;
   }
   if (L.q8 == 3) {
-    // native MXFP4 codes, converted to E4M3 in Tensor Memory, 16-row token tiles
-    if (L.epi == EPI_SWIGLU && kernel_tn == 16) return launch_fp4mma_variant<EPI_SWIGLU, 1>(L, p, s);
-    if (L.epi != EPI_SWIGLU && kernel_tn == 16 && L.mblk == 2) return launch_fp4mma_variant<EPI_F32, 2>(L, p, s);
+    // native MXFP4 codes on the block-scaled MMA, E4M3-piece activations, 16-, 32- or 64-row
+    // token tiles (the down projection's 32- and 64-row tiles on one 128-feature slab)
+    if (L.epi == EPI_SWIGLU && kernel_tn == 16) return launch_fp4mma_variant<EPI_SWIGLU, 1, 16>(L, p, s);
+    if (L.epi == EPI_SWIGLU && kernel_tn == 32) return launch_fp4mma_variant<EPI_SWIGLU, 1, 32>(L, p, s);
+    if (L.epi == EPI_SWIGLU && kernel_tn == 64) return launch_fp4mma_variant<EPI_SWIGLU, 1, 64>(L, p, s);
+    if (L.epi != EPI_SWIGLU && kernel_tn == 16 && L.mblk == 2) return launch_fp4mma_variant<EPI_F32, 2, 16>(L, p, s);
+    if (L.epi != EPI_SWIGLU && kernel_tn == 32 && L.mblk == 1) return launch_fp4mma_variant<EPI_F32, 1, 32>(L, p, s);
+    if (L.epi != EPI_SWIGLU && kernel_tn == 64 && L.mblk == 1) return launch_fp4mma_variant<EPI_F32, 1, 64>(L, p, s);
     return cudaErrorInvalidValue;
   }
   if (L.q8 == 2) {

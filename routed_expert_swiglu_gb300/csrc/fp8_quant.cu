@@ -200,10 +200,8 @@ cudaError_t launch_split_rows_e4m3(const void* src, bool bf16_src, const int32_t
 // the sub-block scales inside a tile stay within the FP8 exponent headroom).
 //
 // E2M1 code = sign << 3 | magnitude index, magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.  Storage:
-// eight consecutive codes per 32-bit word (little endian), the magnitude index of code k in
-// bits 4k..4k+2, the sign of code j < 4 in bit 8j+7 and that of code 4+j in bit 8j+3 -- where an
-// E4M3 byte keeps its sign, directly for codes 0..3 and after a 4-bit shift for codes 4..7.
-// Sub-block exponent: the smallest s with
+// two consecutive codes per byte, code 2i in the low nibble of byte i of the row (the order in
+// which the block-scaled MMA reads packed E2M1).  Sub-block exponent: the smallest s with
 // amax <= 6 * 2^s (frexp: amax = m * 2^x, s = x - 3 if m <= 0.75 else x - 2), at least -114,
 // then raised to (the largest s of its 128 x 128 tile) - 14; an all-zero sub-block takes the
 // tile's largest s (-114 in an all-zero tile), so that E below is at least -120.  q * 2^t is an E4M3 value for every magnitude q iff -8 <= t <= 6, so with the
@@ -291,7 +289,7 @@ __global__ void __launch_bounds__(256) quantize_mxfp4_kernel(const __nv_bfloat16
         const float val = ldexpf(__uint_as_float(bits), -e);  // exact power-of-two scaling
         const uint32_t idx = e2m1_index(fabsf(val));
         const uint32_t neg = (val < 0.0f && idx > 0) ? 1u : 0u;
-        word |= (idx << (4 * j)) | (neg << (j < 4 ? 8 * j + 7 : 8 * (j - 4) + 3));
+        word |= (idx | (neg << 3)) << (4 * j);
       }
       out[q] = word;
     }
@@ -352,7 +350,7 @@ __global__ void __launch_bounds__(256) mxfp4_to_fp8_kernel(const uint8_t* __rest
         for (int j = 0; j < 4; ++j) {
           const int k = 4 * h + j;  // code k of the word
           const uint32_t idx = (cw[q] >> (4 * k)) & 7u;
-          const uint32_t neg = (cw[q] >> (h == 0 ? 8 * j + 7 : 8 * j + 3)) & 1u;
+          const uint32_t neg = (cw[q] >> (4 * k + 3)) & 1u;
           const float mag = ldexpf(e2m1_magnitude(idx), t);
           uint32_t b8 = (uint32_t)__nv_cvt_float_to_fp8(neg ? -mag : mag, __NV_SATFINITE, __NV_E4M3);
           if ((b8 & 0x7Fu) == 0) b8 = 0;

@@ -263,8 +263,8 @@ bool fp8_mma_shapes(const moe_config& c) {
 
 // Dispatch + grouped GEMMs + combine, from routing in the workspace or the caller's buffers.
 // FP8 (E4M3) expert weights: codes and 128 x 128 tile exponents (see moe_quantize_fp8).  With
-// the sub-block exponents s* set, MXFP4 weights instead: packed E2M1 codes, 1 x 32 sub-block
-// exponents and the tile exponents of their FP8 form (see moe_quantize_mxfp4).
+// the sub-block exponents s* set, MXFP4 weights instead: packed E2M1 codes and their 1 x 32
+// sub-block exponents (see moe_quantize_mxfp4); the tile exponents are then unused.
 struct Fp8Weights {
   const uint8_t* q13; const int8_t* e13; const uint8_t* q2; const int8_t* e2;
   const uint8_t* q13_sh; const int8_t* e13_sh; const uint8_t* q2_sh; const int8_t* e2_sh;
@@ -286,13 +286,13 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   pm.E = E;
   pm.n_shared = sh;
   // FP8 weights: a schedule of the FP8 kernels' own row tiles (the widening kernels: 64 rows)
-  const bool f4 = q8 != nullptr && q8->s13 != nullptr;  // native MXFP4 (16-row token tiles)
+  const bool f4 = q8 != nullptr && q8->s13 != nullptr;  // native MXFP4 (block-scaled MMA)
   if (f4 && !fp8_mma_shapes(c)) return MOE_ERR_UNSUPPORTED;
   // FP8 weights at prefill: codes widened to bf16 in shared memory on the CTA-pair kernels, bf16
   // activations (the dispatched rows and the (hi, lo) pair), the bf16 path's schedule
   const bool f8pair = q8 != nullptr && !f4 && !is_decode(T);
   const bool f8mma = q8 != nullptr && !f8pair && fp8_mma_shapes(c);
-  const int sched_tn = (q8 == nullptr || f8pair) ? L.TN : (f4 ? 16 : f8mma ? fp8_token_tile(T, c.top_k, E) : 64);
+  const int sched_tn = (q8 == nullptr || f8pair) ? L.TN : f8mma ? fp8_token_tile(T, c.top_k, E) : 64;
   pm.TN = sched_tn;
   pm.nblk = L.nblk;
   pm.blockhist = at<int32_t>(ws, L.blockhist);
@@ -419,7 +419,9 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
     g2.pair = f8pair;
     g2.TN = sched_tn;
     g2.kernel_tn = sched_tn;
-    g2.mblk = (f8mma && sched_tn == 64) ? 1 : 2;  // four 64-row pieces already fill N = 256; a pair 256
+    // four 64-row pieces already fill N = 256 (MXFP4: 32-row tiles too, whose four pieces then sit
+    // side by side in N); a pair 256
+    g2.mblk = (f8mma && (sched_tn == 64 || (f4 && sched_tn == 32))) ? 1 : 2;
     g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
     g2.max_tiles = L.max_rt * g2.num_mblocks;
     if (f8mma) {
@@ -612,23 +614,19 @@ moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const i
 
 moe_status moe_forward_mxfp4(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                              const moe_bf16* w_r, const float* bias, const uint8_t* c13, const int8_t* s13,
-                             const int8_t* t13, const uint8_t* c2, const int8_t* s2, const int8_t* t2,
-                             const uint8_t* c13_sh, const int8_t* s13_sh, const int8_t* t13_sh, const uint8_t* c2_sh,
-                             const int8_t* s2_sh, const int8_t* t2_sh, moe_bf16* out, void* ws, size_t ws_bytes,
+                             const uint8_t* c2, const int8_t* s2, const uint8_t* c13_sh, const int8_t* s13_sh,
+                             const uint8_t* c2_sh, const int8_t* s2_sh, moe_bf16* out, void* ws, size_t ws_bytes,
                              moe_stream_t stream) {
   MOE_TRY(check_common(plan, T, ws, ws_bytes));
   if (T == 0) return MOE_OK;
   if (!fp8_mma_shapes(plan->cfg)) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_route_ptrs(plan, x, token_ids, w_r, bias));
-  MOE_TRY(need16(c13));
-  MOE_TRY(need16(c2));
-  if (s13 == nullptr || t13 == nullptr || s2 == nullptr || t2 == nullptr) return MOE_ERR_INVALID_ARG;
-  if (!aligned(s13, 4) || !aligned(s2, 4)) return MOE_ERR_ALIGNMENT;
+  if (c13 == nullptr || c2 == nullptr || s13 == nullptr || s2 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(c13, 32) || !aligned(c2, 32) || !aligned(s13, 4) || !aligned(s2, 4)) return MOE_ERR_ALIGNMENT;
   if (plan->cfg.n_shared) {
-    MOE_TRY(need16(c13_sh));
-    MOE_TRY(need16(c2_sh));
-    if (s13_sh == nullptr || t13_sh == nullptr || s2_sh == nullptr || t2_sh == nullptr) return MOE_ERR_INVALID_ARG;
-    if (!aligned(s13_sh, 4) || !aligned(s2_sh, 4)) return MOE_ERR_ALIGNMENT;
+    if (c13_sh == nullptr || c2_sh == nullptr || s13_sh == nullptr || s2_sh == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned(c13_sh, 32) || !aligned(c2_sh, 32) || !aligned(s13_sh, 4) || !aligned(s2_sh, 4))
+      return MOE_ERR_ALIGNMENT;
   }
   MOE_TRY(need16(out));
   int sms = 0;
@@ -640,7 +638,7 @@ moe_status moe_forward_mxfp4(moe_plan* plan, int32_t T, const moe_bf16* x, const
   int32_t* ids = at<int32_t>(ws, L.topk_ids);
   float* w = at<float>(ws, L.topk_w);
   MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
-  const Fp8Weights qw = {c13, t13, c2, t2, c13_sh, t13_sh, c2_sh, t2_sh, s13, s2, s13_sh, s2_sh};
+  const Fp8Weights qw = {c13, nullptr, c2, nullptr, c13_sh, nullptr, c2_sh, nullptr, s13, s2, s13_sh, s2_sh};
   return run_experts(plan, T, x, ids, w, nullptr, nullptr, nullptr, nullptr, out, ws, sms, s, &qw);
 }
 

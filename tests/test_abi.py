@@ -118,7 +118,7 @@ def test_weight_format_validation_without_gpu(lib):
     assert lib.moe_quantize_mxfp4(p16, 1, 128, 128, ctypes.c_void_p(base + 8), p16, nul) == 3
     assert lib.moe_quantize_fp8(p16, 1, 0, 128, p16, p16, nul) == 1
     assert lib.moe_quantize_fp8(ctypes.c_void_p(base + 1), 1, 128, 128, p16, p16, nul) == 3
-    # conversion: tile exponents required, codes optional, K a multiple of 32
+    # conversion: tile exponents required, FP8 codes optional, K a multiple of 32
     assert lib.moe_mxfp4_to_fp8(p16, p16, 1, 128, 128, p16, nul, nul) == 1
     assert lib.moe_mxfp4_to_fp8(p16, p16, 1, 128, 96 + 8, p16, p16, nul) == 1
     assert lib.moe_mxfp4_to_fp8(p16, p16, 1, 128, 128, ctypes.c_void_p(base + 4), p16, nul) == 3
@@ -127,16 +127,19 @@ def test_weight_format_validation_without_gpu(lib):
     need = lib.moe_workspace_bytes(plan, 64)
     ws_buf = ctypes.create_string_buffer(need + 4096)
     ws = ctypes.c_void_p((ctypes.addressof(ws_buf) + 255) // 256 * 256)
-    w = [p16] * 12
+    w = [p16] * 8                                       # (codes, sub-block exponents) x 4; base is 256-aligned
     assert lib.moe_forward_mxfp4(plan, 65, p16, nul, p16, nul, *w, p16, ws, need, nul) == 1
     bad = list(w)
-    bad[2] = nul                                        # t13
+    bad[1] = nul                                        # s13
     assert lib.moe_forward_mxfp4(plan, 64, p16, nul, p16, nul, *bad, p16, ws, need, nul) == 1
     bad = list(w)
     bad[1] = ctypes.c_void_p(base + 2)                  # s13 not 4-byte aligned
     assert lib.moe_forward_mxfp4(plan, 64, p16, nul, p16, nul, *bad, p16, ws, need, nul) == 3
     bad = list(w)
-    bad[6] = nul                                        # shared codes of a layer with a shared expert
+    bad[2] = ctypes.c_void_p(base + 16)                 # c2 16-byte but not 32-byte aligned
+    assert lib.moe_forward_mxfp4(plan, 64, p16, nul, p16, nul, *bad, p16, ws, need, nul) == 3
+    bad = list(w)
+    bad[4] = nul                                        # shared codes of a layer with a shared expert
     assert lib.moe_forward_mxfp4(plan, 64, p16, nul, p16, nul, *bad, p16, ws, need, nul) == 1
     assert lib.moe_forward_fp8(plan, 64, p16, nul, p16, nul, p16, nul, p16, p16, p16, p16, p16, p16, p16, ws,
                                need, nul) == 1         # e13 null
