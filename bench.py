@@ -5,11 +5,10 @@
 One step = one whole layer forward (router GEMM, top-k, dispatch, gate/up grouped GEMM, down
 grouped GEMM, combine) over one batch of T synthetic tokens whose inputs are resident in HBM.
 Default workload: the DeepSeek-V4-Flash-shaped layer at T=8192 (prefill), also with FP8 expert
-weights ("fp8_weights"); the same line carries the same layer with Zipf-skewed routing under
+weights ("fp8_weights") and MXFP4 expert weights ("mxfp4_weights"); the same line carries the same layer with Zipf-skewed routing under
 "skewed", and a T=64 (decode) measurement under "decode", with the same layer on FP8 expert
 weights ("fp8_weights") and on MXFP4 expert weights ("mxfp4_weights": the one-time conversion to
-the FP8 form, the forward on the converted tiles, and the native forward that streams the 4-bit
-codes).
+the FP8 form, the forward on the converted tiles, and the native forward on the 4-bit codes).
 Multi-GPU runs are independent replicas (one process per GPU, each with its own token batch; no
 collective on the data path).
 
@@ -386,10 +385,12 @@ def run_ours(args, world, rank, local):
     roof_s = cost.roofline_seconds(layer_flops, layer_bytes, float(peaks["bf16_tflops_sustained"]), hbm_peak)
     gemm_ms = stage_ms[STAGES.index("gate_up_gemm")] + stage_ms[STAGES.index("down_gemm")]
     e2e_ms, h2d, d2h = measure_e2e(layer, inp, w, args.steps, args.warmup, world)
-    prefill_fp8 = None
+    prefill_fp8 = prefill_mxfp4 = None
     if not args.no_fp8:
         prefill_fp8 = measure_fp8(layer, inp, w, max(args.steps // 2, 5), args.warmup, active, ms_per_step,
                                   hbm_peak, world)
+        prefill_mxfp4 = measure_mxfp4(layer, inp, w, max(args.steps // 2, 5), args.warmup,
+                                      prefill_fp8["ms_per_step"], ms_per_step, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inp, min(args.cpu_tokens, w.T))
@@ -469,6 +470,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "fp8_weights": prefill_fp8,
+        "mxfp4_weights": prefill_mxfp4,
         "decode": decode,
         "skewed": skewed,
         "cpu_baseline": cpu,
@@ -581,7 +583,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=240,
                     help="tokens per step of the reference arm (the oracle; about 3 s per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8- and MXFP4-weight decode measurements")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8- and MXFP4-weight measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["moe_api.cu", "grouped_gemm.cu", "fp8_gemm.cu", "routing.cu", "permute.cu", "combine.cu", "permute_noalloc.cu",
+SOURCES = ["moe_api.cu", "grouped_gemm.cu", "fp8_gemm.cu", "bs_pair_gemm.cu", "routing.cu", "permute.cu", "combine.cu", "permute_noalloc.cu",
            "bias_update.cu", "fp8_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -472,6 +472,35 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t tmem_d, uint64_t adesc, uin
       : "memory");
 }
 
+// D (+)= (A[smem] . 2^SFA) * (B[smem] . 2^SFB)^T: E2M1 A in the 16-byte-chunk form, E4M3 B, K = 32
+// per instruction, UE8M0 scales read from Tensor Memory at sfa / sfb; issued by one thread.
+__device__ __forceinline__ void tc_mma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E2M1 A (format 5) and E4M3 B (format 0), fp32
+// accumulator, both K-major, UE8M0 scales (bit 23), M = 128, N = n, B scale byte 0 (bits [4,6)),
+// A scale byte `ida` (bits [29,31)).
+__device__ __forceinline__ uint32_t idesc_mx_e2m1_e4m3(uint32_t n, uint32_t ida) {
+  return (5u << 7)                // A format E2M1, bits [7,10)
+         | ((n >> 3) << 17)       // N >> 3, bits [17,23)
+         | (1u << 23)             // scale format UE8M0
+         | ((128u >> 4) << 24)    // M >> 4, bits [24,29)
+         | (ida << 29);           // A scale byte, bits [29,31)
+}
+
+// Store one 32-bit column of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
 // Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask` when all tcgen05
 // operations issued so far by this thread complete.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {

@@ -709,41 +709,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // scales are written uniform (every lane, byte and column of an 8-column region per piece), so
 // their layout does not matter.
 
-// D (+)= (A[smem] . 2^SFA) * (B[smem] . 2^SFB)^T: E2M1 A in the 16-byte-chunk form, E4M3 B, K = 32
-// per instruction, UE8M0 scales read from Tensor Memory at sfa / sfb; issued by one thread.
-__device__ __forceinline__ void tc_mma_mx(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-          tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-      : "memory");
-}
-
-// Instruction descriptor of kind::mxf8f6f4 with E2M1 A (format 5) and E4M3 B (format 0), fp32
-// accumulator, both K-major, UE8M0 scales (bit 23), M = 128, N = n, B scale byte 0 (bits [4,6)),
-// A scale byte `ida` (bits [29,31)).
-__device__ __forceinline__ uint32_t idesc_mx_e2m1_e4m3(uint32_t n, uint32_t ida) {
-  return (5u << 7)                // A format E2M1, bits [7,10)
-         | ((n >> 3) << 17)       // N >> 3, bits [17,23)
-         | (1u << 23)             // scale format UE8M0
-         | ((128u >> 4) << 24)    // M >> 4, bits [24,29)
-         | (ida << 29);           // A scale byte, bits [29,31)
-}
-
-// Store one 32-bit column of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-
 // The parameter block plus the MXFP4 sub-block exponents [mats, rows, K/32] (int8) of the routed
 // and the shared weights.
 struct Fp4Params : GemmParams {
   const int8_t* a_sub;
   const int8_t* a_sh_sub;
 };
+
+// Stages whose A scales a scale writer loads at once (see the writers' loop).
+constexpr int F4_SF_CHUNK = 8;
 
 template <int EPI, int MBLK, int TN_>
 struct F4Shape {
@@ -1059,37 +1033,35 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK, TN_>::THREADS, 1)
         const int row = min(base + r, p.a_rows_per_group - 1);  // rows past the matrix: any valid row
         srow[a] = reinterpret_cast<const uint32_t*>(sub + (size_t)row * kb32);
       }
-      // the rows' exponents into L2 at the tile's start, then each stage's word loaded one stage
-      // ahead, so that no exponent load sits in a stage's critical path
-      uint32_t nxt[S::NUM_A];
+      // The words of F4_SF_CHUNK stages are loaded together and used before the first of those
+      // stages reports: the report (an arrive with release semantics) then never waits for a load
+      // still in flight, which would put a global-memory latency into every stage.
+      for (int kb0 = 0; ok && kb0 < KB; kb0 += F4_SF_CHUNK) {
+        uint32_t w[F4_SF_CHUNK][S::NUM_A];
 #pragma unroll
-      for (int a = 0; a < S::NUM_A; ++a) {
-        for (int o = 0; o < kb32; o += 128)
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const int8_t*>(srow[a]) + o));
-        nxt[a] = __ldg(srow[a]);
-      }
-      for (int kb = 0; kb < KB; ++kb) {
-        uint32_t w[S::NUM_A];
+        for (int j = 0; j < F4_SF_CHUNK; ++j)
 #pragma unroll
-        for (int a = 0; a < S::NUM_A; ++a) {
-          w[a] = __vadd4(__vmaxs4(nxt[a], 0x81818181u), 0x7F7F7F7Fu);
-          if (kb + 1 < KB) nxt[a] = __ldg(srow[a] + kb + 1);
-        }
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t ts = tmem_base + (uint32_t(quad * 32) << 16) + S::SFA_COL0 + stage * S::NUM_A * 4 + quad;
+          for (int a = 0; a < S::NUM_A; ++a)
+            w[j][a] = (kb0 + j < KB) ? __vadd4(__vmaxs4(__ldg(srow[a] + kb0 + j), 0x81818181u), 0x7F7F7F7Fu) : 0u;
 #pragma unroll
-        for (int a = 0; a < S::NUM_A; ++a) tmem_st1(ts + a * 4, w[a]);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sfull_bar(stage));
-        if (++stage == ST) {
-          stage = 0;
-          phase ^= 1u;
+        for (int j = 0; j < F4_SF_CHUNK; ++j) {
+          if (kb0 + j >= KB) break;
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ts = tmem_base + (uint32_t(quad * 32) << 16) + S::SFA_COL0 + stage * S::NUM_A * 4 + quad;
+#pragma unroll
+          for (int a = 0; a < S::NUM_A; ++a) tmem_st1(ts + a * 4, w[j][a]);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sfull_bar(stage));
+          if (++stage == ST) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
@@ -1537,79 +1509,6 @@ __global__ void __launch_bounds__(Fp8PairShape<EPI, HILO>::THREADS, 1)
 
 // ----------------------------------------------------------------------------- host side
 
-// E4M3 weight codes: 2-D uint8 [rows, cols] with boxes of box_k codes x box_rows rows, and the
-// gate/up 3-D view (cols, d_ff, 2*groups) with boxes (box_k, 128, 2).  box_k = 64: 64-byte
-// swizzle, so that the converter warps' row-wise 16-byte reads spread over all banks; box_k =
-// 128: 128-byte swizzle, the K-major layout the 8-bit MMA reads.
-static bool make_tmap_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows, int box_k = 64) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols};
-  cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-static bool make_tmap_u8_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t cols,
-                                int box_k = 64, int box_rows = BLOCK_M) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
-  cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(d_ff * cols)};
-  cuuint32_t box[3] = {(cuuint32_t)box_k, (cuuint32_t)box_rows, 2};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// E4M3 activation pieces [rows, pieces, K]: 3-D view (K, pieces, rows) with boxes of
-// (128, 1, box_rows), i.e. box_rows rows of 128 codes of one piece, 128-byte swizzle.
-static bool make_tmap_pieces(CUtensorMap* m, const void* ptr, int64_t rows, int pieces, int64_t K, int box_rows) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)pieces, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)(pieces * K)};
-  cuuint32_t box[3] = {128, 1, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// MXFP4 codes, two E2M1 codes per byte (code 2i in the low nibble of byte i), row-major [rows,
-// K]: each group of 16 codes (8 bytes) lands in the low half of a 16-byte chunk of shared memory
-// (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B), the form the block-scaled MMA reads; boxes of 128
-// codes (one 128-byte row of shared memory) x box_rows rows, 128-byte swizzle.  The gate/up view
-// is 3-D (K, d_ff, 2*groups) with boxes (128, 128, 2).  The type wants K a multiple of 128,
-// row strides a multiple of 32 bytes and a 32-byte aligned base.
-static bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-static bool make_tmap_e2m1_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t K) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
-  cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)(d_ff * K / 2)};
-  cuuint32_t box[3] = {128, (cuuint32_t)BLOCK_M, 2};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int EPI, int TN, int MBLK, bool HILO>
 static cudaError_t launch_fp8_variant(const GemmLaunch& L, GemmParams p, cudaStream_t s) {
   using Sh = Fp8Shape<EPI, TN, MBLK, HILO>;
@@ -1804,6 +1703,7 @@ static cudaError_t launch_fp8w_pair_variant(const GemmLaunch& L, GemmParams p, c
 }
 
 cudaError_t launch_fp8_gemm(const GemmLaunch& L, GemmParams p, int kernel_tn, cudaStream_t s) {
+  if ((L.q8 == 2 || L.q8 == 3) && L.pair) return launch_bs_pair_gemm(L, p, s);  // prefill, block-scaled
   if (L.q8 == 1 && L.pair) {
     // prefill: codes widened to bf16 in shared memory, CTA-pair bf16 MMA, 256-row token tiles
     if (L.epi == EPI_SWIGLU && kernel_tn == 256) return launch_fp8w_pair_variant<EPI_SWIGLU, false>(L, p, s);

@@ -181,8 +181,86 @@ inline bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int64_t col
   return r == CUDA_SUCCESS;
 }
 
+// E4M3 weight codes: 2-D uint8 [rows, cols] with boxes of box_k codes x box_rows rows, and the
+// gate/up 3-D view (cols, d_ff, 2*groups) with boxes (box_k, 128, 2).  box_k = 64: 64-byte
+// swizzle, so that the converter warps' row-wise 16-byte reads spread over all banks; box_k =
+// 128: 128-byte swizzle, the K-major layout the 8-bit MMA reads.
+inline bool make_tmap_u8(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows, int box_k = 64) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool make_tmap_u8_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t cols,
+                                int box_k = 64, int box_rows = BLOCK_M) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
+  cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(d_ff * cols)};
+  cuuint32_t box[3] = {(cuuint32_t)box_k, (cuuint32_t)box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, box_k == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// E4M3 activation pieces [rows, pieces, K]: 3-D view (K, pieces, rows) with boxes of
+// (128, 1, box_rows), i.e. box_rows rows of 128 codes of one piece, 128-byte swizzle.
+inline bool make_tmap_pieces(CUtensorMap* m, const void* ptr, int64_t rows, int pieces, int64_t K, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)pieces, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)K, (cuuint64_t)(pieces * K)};
+  cuuint32_t box[3] = {128, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MXFP4 codes, two E2M1 codes per byte (code 2i in the low nibble of byte i), row-major [rows,
+// K]: each group of 16 codes (8 bytes) lands in the low half of a 16-byte chunk of shared memory
+// (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B), the form the block-scaled MMA reads; boxes of 128
+// codes (one 128-byte row of shared memory) x box_rows rows, 128-byte swizzle.  The gate/up view
+// is 3-D (K, d_ff, 2*groups) with boxes (128, 128, 2).  The type wants K a multiple of 128,
+// row strides a multiple of 32 bytes and a 32-byte aligned base.
+inline bool make_tmap_e2m1(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool make_tmap_e2m1_gateup(CUtensorMap* m, const void* ptr, int64_t groups, int64_t d_ff, int64_t K,
+                                  int box_rows = BLOCK_M) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)d_ff, (cuuint64_t)(2 * groups)};
+  cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)(d_ff * K / 2)};
+  cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The FP8-weight grouped GEMMs (fp8_gemm.cu) for a launch with L.q8 set: 1 = codes widened to
 // bf16 in Tensor Memory, 2 = codes straight into the 8-bit MMA with E4M3-piece activations.
 cudaError_t launch_fp8_gemm(const GemmLaunch& L, GemmParams p, int kernel_tn, cudaStream_t s);
+
+// The block-scaled CTA-pair GEMMs (bs_pair_gemm.cu) for FP8 (q8 = 2) or MXFP4 (q8 = 3) weights at
+// prefill: codes and their scales into the 2-SM block-scaled MMA, E4M3-piece activations.
+cudaError_t launch_bs_pair_gemm(const GemmLaunch& L, GemmParams p, cudaStream_t s);
 
 }  // namespace moe

@@ -50,6 +50,10 @@ inline int token_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
 // Token-tile width of the router GEMM.
 inline int router_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
 
+// Token rows per tile of the block-scaled CTA-pair kernels (FP8 / MXFP4 weights at prefill):
+// the most that leaves Tensor Memory room for the scales beside two accumulator buffers.
+constexpr int BS_PAIR_TN = 224;
+
 // Row-tile width of the FP8-weight GEMMs' schedule, from the mean rows per routed expert
 // T k / E: 16 up to 8 rows, 32 up to 24, else 64.  Narrow tiles leave more of each pipeline
 // stage to the weight codes; a tile narrower than an expert's rows streams its weights again.

@@ -288,11 +288,17 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   // FP8 weights: a schedule of the FP8 kernels' own row tiles (the widening kernels: 64 rows)
   const bool f4 = q8 != nullptr && q8->s13 != nullptr;  // native MXFP4 (block-scaled MMA)
   if (f4 && !fp8_mma_shapes(c)) return MOE_ERR_UNSUPPORTED;
-  // FP8 weights at prefill: codes widened to bf16 in shared memory on the CTA-pair kernels, bf16
-  // activations (the dispatched rows and the (hi, lo) pair), the bf16 path's schedule
-  const bool f8pair = q8 != nullptr && !f4 && !is_decode(T);
+  // FP8 / MXFP4 weights at prefill: the block-scaled CTA-pair kernels (codes and scales into the
+  // 2-SM MMA, E4M3-piece activations, 224-row token tiles); FP8 shapes they do not take (d or
+  // d_ff not a multiple of 128): codes widened to bf16 in shared memory on the CTA-pair kernels,
+  // bf16 activations (the dispatched rows and the (hi, lo) pair), the bf16 path's schedule
+  const bool bs_pair = q8 != nullptr && !is_decode(T) && fp8_mma_shapes(c);
+  const bool f8pair = q8 != nullptr && !f4 && !is_decode(T) && !fp8_mma_shapes(c);
   const bool f8mma = q8 != nullptr && !f8pair && fp8_mma_shapes(c);
-  const int sched_tn = (q8 == nullptr || f8pair) ? L.TN : f8mma ? fp8_token_tile(T, c.top_k, E) : 64;
+  const int sched_tn = (q8 == nullptr || f8pair) ? L.TN
+                       : bs_pair                 ? BS_PAIR_TN
+                       : f8mma                   ? fp8_token_tile(T, c.top_k, E)
+                                                 : 64;
   pm.TN = sched_tn;
   pm.nblk = L.nblk;
   pm.blockhist = at<int32_t>(ws, L.blockhist);
@@ -355,7 +361,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
     g1.a_exp = q8->e13;
     g1.a_sh_ptr = sh ? q8->q13_sh : nullptr;
     g1.a_sh_exp = sh ? q8->e13_sh : nullptr;
-    g1.pair = f8pair;
+    g1.pair = f8pair || bs_pair;
     g1.TN = sched_tn;
     g1.kernel_tn = sched_tn;
     if (f8mma) {
@@ -416,12 +422,12 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
     g2.a_exp = q8->e2;
     g2.a_sh_ptr = sh ? q8->q2_sh : nullptr;
     g2.a_sh_exp = sh ? q8->e2_sh : nullptr;
-    g2.pair = f8pair;
+    g2.pair = f8pair || bs_pair;
     g2.TN = sched_tn;
     g2.kernel_tn = sched_tn;
     // four 64-row pieces already fill N = 256 (MXFP4: 32-row tiles too, whose four pieces then sit
     // side by side in N); a pair 256
-    g2.mblk = (f8mma && (sched_tn == 64 || (f4 && sched_tn == 32))) ? 1 : 2;
+    g2.mblk = (f8mma && !bs_pair && (sched_tn == 64 || (f4 && sched_tn == 32))) ? 1 : 2;
     g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
     g2.max_tiles = L.max_rt * g2.num_mblocks;
     if (f8mma) {

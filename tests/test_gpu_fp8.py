@@ -70,9 +70,11 @@ def small(w, T, **kw):
     return dataclasses.replace(w, T=T, name=f"{w.name.rsplit('_T', 1)[0]}_T{T}", **kw)
 
 
-# Batches above 64 tokens (prefill) run the CTA-pair kernels that widen the codes to bf16 in shared
-# memory (any d, d_ff multiple of 64); decode batches the direct 8-bit MMA (d, d_ff multiples of
-# 128) or, for other shapes, the single-CTA widening kernels.
+# Batches above 64 tokens (prefill) run the block-scaled CTA-pair kernels (codes and tile scales
+# into the 2-SM MMA, E4M3-piece activations; d, d_ff multiples of 128: v3_T96, tall_T1500 with
+# two 224-row tiles per expert, edges_T80) or, for other shapes, the CTA-pair kernels that widen
+# the codes to bf16 in shared memory (toy_T333, ragged_T150); decode batches the direct 8-bit MMA
+# (d, d_ff multiples of 128) or, for other shapes, the single-CTA widening kernels.
 CASES = [
     W.TOY,                                                                  # decode kernels
     small(W.TOY, 333),                                                      # prefill: CTA-pair widening
@@ -86,7 +88,7 @@ CASES = [
     small(W.V4FLASH_T64, 64, E=16),                                         # V4-Flash dims, 16 experts
     small(W.V4PRO_HASH_T16384, 40, E=24, d=1024, d_ff=384),
     # direct-MMA path with 16-row tiles (2 mean rows per expert; the shared expert's 64 rows span
-    # four tiles), and a prefill batch with several 256-row tiles per expert
+    # four tiles), and a prefill batch with two 224-row tiles per expert (the second ragged)
     W.Workload("wide_T64", T=64, d=512, d_ff=256, E=64, k=2, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
                use_bias=True),
     W.Workload("tall_T1500", T=1500, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX),

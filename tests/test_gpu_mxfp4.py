@@ -140,10 +140,13 @@ NATIVE = [
     W.Workload("noshared_T40", T=40, d=384, d_ff=384, E=12, k=3, n_shared=0, score=W.SCORE_SOFTMAX),
     W.Workload("v4flash_E16_T64", T=64, d=4096, d_ff=2048, E=16, k=6, n_shared=1, score=W.SCORE_SQRT_SOFTPLUS,
                use_bias=True),
-    # a prefill-sized batch: about 75 rows per expert, two 64-row tiles each, ragged last tiles
+    # decode with 64-row token tiles (32 rows per expert on average)
+    W.Workload("deep_T64", T=64, d=256, d_ff=384, E=4, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
+    # prefill batches: the block-scaled CTA-pair kernels (224-row token tiles), one ragged tile per
+    # expert, and two per expert (about 256 rows each; d = 384: the down projection's second
+    # 256-feature block lies half past the matrix)
     W.Workload("tall_T300", T=300, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
-    # 32-row token tiles (9 to 24 rows per expert on average), K of four 128-wide steps
-    W.Workload("mid32_T96", T=96, d=512, d_ff=384, E=16, k=3, n_shared=1, score=W.SCORE_SIGMOID, use_bias=True),
+    W.Workload("tall_T512", T=512, d=384, d_ff=256, E=8, k=4, n_shared=1, score=W.SCORE_SIGMOID, use_bias=True),
 ]
 
 
@@ -180,8 +183,11 @@ def test_native_mxfp4_layer_vs_oracle(w):
 
 
 @pytest.mark.slow
-def test_native_mxfp4_full_size_layer():
-    run_native(W.V4FLASH_T64, seed=0, sample=2)
+@pytest.mark.parametrize("w,sample", [(W.V4FLASH_T64, 2), (W.V4FLASH_T8192, 6)], ids=lambda v: getattr(v, "name", str(v)))
+def test_native_mxfp4_full_size_layer(w, sample):
+    """Full size in the launch configurations the benchmark times: the decode kernels at T=64,
+    the block-scaled CTA-pair kernels at T=8192."""
+    run_native(w, seed=0, sample=sample)
 
 
 def test_native_mxfp4_needs_128_multiples():
