@@ -445,3 +445,30 @@ def test_a_single_bf16_activation_misses_the_output_tolerance():
     elem = lambda y: (np.abs(y - ref) / (np.abs(ref) + 1e-2)).max()  # noqa: E731
     assert elem(oracle.round_to_bf16(oracle.forward(x, ids, wts, fetch, sh, cast_h=True))) > 0.1
     assert elem(oracle.round_to_bf16(ref)) < 5e-3
+
+
+def test_bf16_expert_outputs_miss_the_output_tolerance():
+    """Why the down projection writes its weighted expert outputs O in fp32: on the same
+    V4-Flash-shaped layer, rounding each weighted expert output to bf16 before the slot sum (the
+    pages' combine, "Mixture of Experts: router, token dispatch, grouped GEMM", Token Combine, sums
+    them unrounded) moves outputs where the slots cancel far beyond the 2e-2 bound, while fp32 O
+    (exact here) with only the bf16 rounding of y meets it."""
+    import dataclasses
+    from oracle import moe_oracle as M
+    from routed_expert_swiglu_gb300 import inputs, workloads as W
+    w = dataclasses.replace(W.V4FLASH_T8192, T=64, E=8, name="v4flash_E8_T64")
+    inp = inputs.make_layer_inputs(w, seed=0, device="cpu")
+    f64 = lambda t: t.double().numpy()  # noqa: E731
+    x = f64(inp.x)
+    ids, wts, _ = oracle.route(oracle.router_logits(x, f64(inp.w_r)), w.k, w.score, bias=f64(inp.bias))
+    fetch = lambda e: (f64(inp.w13[e]), f64(inp.w2[e]))  # noqa: E731
+    sh = (f64(inp.w13_sh), f64(inp.w2_sh))
+    ref = oracle.forward(x, ids, wts, fetch, sh)
+    y = oracle.round_to_bf16(M.swiglu_expert(x, sh[0], sh[1], False))
+    for j in range(w.k):
+        for e in np.unique(ids[:, j]):
+            r = np.nonzero(ids[:, j] == e)[0]
+            y[r] += oracle.round_to_bf16(M.swiglu_expert(x[r], *fetch(int(e)), False) * wts[r, j:j + 1])
+    elem = lambda v: (np.abs(v - ref) / (np.abs(ref) + 1e-2)).max()  # noqa: E731
+    assert elem(oracle.round_to_bf16(y)) > 0.1
+    assert elem(oracle.round_to_bf16(ref)) < 5e-3
