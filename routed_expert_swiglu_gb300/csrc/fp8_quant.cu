@@ -172,6 +172,100 @@ __global__ void __launch_bounds__(SPLIT_THREADS) split_rows_e4m3_kernel(const vo
   }
 }
 
+// The same two-piece split of bf16 rows, token-major for the dispatch: CTA t splits x row t once
+// and writes its pieces and exponent to every dispatched row that holds it -- the k routed rows
+// inv[t*k + j] and, with a shared expert, row N + t -- so each x row is read and split once
+// instead of once per slot.
+__global__ void __launch_bounds__(SPLIT_THREADS) split_tokens_e4m3_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                          const int32_t* __restrict__ inv, int k,
+                                                                          int N, int n_shared, int K,
+                                                                          uint8_t* __restrict__ dst,
+                                                                          int32_t* __restrict__ exps, int* err) {
+  extern __shared__ float srow[];
+  __shared__ float s_max[SPLIT_THREADS / 32];
+  __shared__ int s_e;
+  __shared__ int s_rows[MAX_TOPK + 1];
+  const int t = blockIdx.x;
+  const int nrows = k + n_shared;
+  if (threadIdx.x < nrows) {
+    int r = threadIdx.x < k ? __ldg(inv + (size_t)t * k + threadIdx.x) : N + t;
+    if (bad_index(r, (long long)N + (long long)n_shared * gridDim.x, err)) r = -1;
+    s_rows[threadIdx.x] = r;
+  }
+  float m = 0.0f;
+  const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)t * K);
+  for (int i = threadIdx.x; i < K / 8; i += SPLIT_THREADS) {
+    const uint4 v = __ldcs(s + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      srow[8 * i + 2 * j] = lo;
+      srow[8 * i + 2 * j + 1] = hi;
+      m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float amax = 0.0f;
+    for (int i = 0; i < SPLIT_THREADS / 32; ++i) amax = fmaxf(amax, s_max[i]);
+    int e = 0;
+    if (amax > 0.0f) {
+      int xe;
+      const float mant = frexpf(amax, &xe);
+      e = max((mant <= 0.875f) ? xe - 9 : xe - 8, -126);
+    }
+    s_e = e;
+  }
+  __syncthreads();
+  if (threadIdx.x < nrows && s_rows[threadIdx.x] >= 0) exps[s_rows[threadIdx.x]] = s_e;
+  const float sc = __int_as_float((127 - s_e) << 23);  // 2^-e (e in [-126, 120])
+  for (int i = threadIdx.x; i < K / 4; i += SPLIT_THREADS) {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = srow[4 * i + j] * sc;
+    uint32_t code[2];
+#pragma unroll
+    for (int pc = 0; pc < 2; ++pc) {
+      const __nv_fp8x2_storage_t c01 = __nv_cvt_float2_to_fp8x2(make_float2(v[0], v[1]), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t c23 = __nv_cvt_float2_to_fp8x2(make_float2(v[2], v[3]), __NV_SATFINITE, __NV_E4M3);
+      code[pc] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+      if (pc == 0) {
+        const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(c01, __NV_E4M3);
+        const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(c23, __NV_E4M3);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        v[0] = (v[0] - f01.x) * 16.0f;  // what piece 0 leaves, times 16 (exact, as above)
+        v[1] = (v[1] - f01.y) * 16.0f;
+        v[2] = (v[2] - f23.x) * 16.0f;
+        v[3] = (v[3] - f23.y) * 16.0f;
+      }
+    }
+    for (int j = 0; j < nrows; ++j) {
+      const int r = s_rows[j];
+      if (r < 0) continue;
+      uint32_t* out = reinterpret_cast<uint32_t*>(dst + (size_t)r * 2 * K);
+      __stcs(out + i, code[0]);
+      __stcs(out + K / 4 + i, code[1]);
+    }
+  }
+}
+
+cudaError_t launch_split_tokens_e4m3(const void* x, const int32_t* inv, int T, int k, int N, int n_shared, int K,
+                                     uint8_t* dst, int32_t* exps, int* err, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (K % 8 != 0 || (size_t)K * 4 > SPLIT_SMEM_MAX || k > MAX_TOPK || inv == nullptr) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(split_tokens_e4m3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SPLIT_SMEM_MAX);
+  if (e != cudaSuccess) return e;
+  split_tokens_e4m3_kernel<<<T, SPLIT_THREADS, (size_t)K * 4, s>>>(static_cast<const __nv_bfloat16*>(x), inv, k, N,
+                                                                   n_shared, K, dst, exps, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_split_rows_e4m3(const void* src, bool bf16_src, const int32_t* gather, int n_gather, int rows,
                                    int K, int pieces, uint8_t* dst, int32_t* exps, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;

@@ -54,6 +54,10 @@ inline int router_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
 // the most that leaves Tensor Memory room for the scales beside two accumulator buffers.
 constexpr int BS_PAIR_TN = 224;
 
+// From this batch size the E4M3 pieces of x are made token-major (one split per x row, written
+// to all its dispatched rows); below it one CTA per dispatched row gives more parallelism.
+constexpr int SPLIT_TOKEN_MAJOR_MIN_T = 1024;
+
 // Row-tile width of the FP8-weight GEMMs' schedule, from the mean rows per routed expert
 // T k / E: 16 up to 8 rows, 32 up to 24, else 64.  Narrow tiles leave more of each pipeline
 // stage to the weight codes; a tile narrower than an expert's rows streams its weights again.
@@ -150,6 +154,10 @@ int permute_launch_count(bool gather);
 // or fp32 rows (4 pieces, in place allowed).  K * 4 <= SPLIT_SMEM_MAX.
 cudaError_t launch_split_rows_e4m3(const void* src, bool bf16_src, const int32_t* gather, int n_gather, int rows,
                                    int K, int pieces, uint8_t* dst, int32_t* exps, cudaStream_t s);
+// The two-piece split of x for the dispatch, token-major: token t's pieces and exponent go to
+// rows inv[t*k + j] and, with a shared expert, row N + t.
+cudaError_t launch_split_tokens_e4m3(const void* x, const int32_t* inv, int T, int k, int N, int n_shared, int K,
+                                     uint8_t* dst, int32_t* exps, int* err, cudaStream_t s);
 
 struct CombineLaunch {
   const float* o; const int32_t* inv; int T, k, d, N, n_shared; void* out;

@@ -323,8 +323,12 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   const int64_t rows_h = (int64_t)L.N + (int64_t)sh * T;
   if (f8mma) {
     LaunchRange r("moe.split_rows_e4m3");
-    MOE_CUDA(launch_split_rows_e4m3(x, true, pm.perm_tok, L.N, (int)rows_h, d, 2, at<uint8_t>(ws, L.xd),
-                                    at<int32_t>(ws, L.xexp), s));
+    if (T >= SPLIT_TOKEN_MAJOR_MIN_T)  // each x row split once, written to its k (+1) rows
+      MOE_CUDA(launch_split_tokens_e4m3(x, pm.inv, T, c.top_k, L.N, sh, d, at<uint8_t>(ws, L.xd),
+                                        at<int32_t>(ws, L.xexp), err, s));
+    else
+      MOE_CUDA(launch_split_rows_e4m3(x, true, pm.perm_tok, L.N, (int)rows_h, d, 2, at<uint8_t>(ws, L.xd),
+                                      at<int32_t>(ws, L.xexp), s));
   }
   record(p, ST_DISPATCH, s);
 
