@@ -324,6 +324,11 @@ __global__ void __launch_bounds__(BsPairShape<EPI, F4>::THREADS, 1)
     const int xch = half * 2 + (quad & 1);  // SwiGLU: exchange channel of this gate/up warp pair
     int buf = 0;
     uint32_t buf_phase = 0;
+#if MOE_TEST_UNSET_WAIT
+    // test build: wait on a phase nothing completes (only the epilogue warps arrive on it, the
+    // even CTA's), so the wait runs out and both CTAs take their abort path
+    mbar_wait(acce_bar(0), 0, abort_flag, p.err);
+#endif
     uint32_t xiter = 0;                      // SwiGLU: chunks exchanged so far on this channel
     bool ok = true;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);

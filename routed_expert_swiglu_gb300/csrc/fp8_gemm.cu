@@ -927,6 +927,11 @@ __global__ void __launch_bounds__(F4Shape<EPI, MBLK, TN_>::THREADS, 1)
     const int half = (warp - 2) >> 2;
     int buf = 0;
     uint32_t buf_phase = 0;
+#if MOE_TEST_UNSET_WAIT
+    // test build: wait on a phase nothing completes (only these warps arrive on it), so the
+    // wait runs out and the kernel takes its abort path
+    mbar_wait(acce_bar(0), 0, abort_flag, p.err);
+#endif
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<TN>(tile, p);
       if (t.rows <= 0) continue;

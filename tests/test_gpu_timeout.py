@@ -1,8 +1,9 @@
 """Bounded pipeline waits, exercised without faulting or hanging the GPU.
 
 A test build of the library (MOE_TEST_UNSET_WAIT=1, MOE_WAIT_LIMIT_NS = 1 ms) makes the epilogue
-warps of every bf16 grouped-GEMM launch (router GEMM, single-CTA and CTA-pair expert GEMMs) first
-wait on a barrier phase that nothing completes.  Each such launch must give up after the limit,
+warps of every grouped-GEMM launch (router GEMM, single-CTA and CTA-pair bf16 expert GEMMs, the
+block-scaled MXFP4 decode GEMMs and the block-scaled CTA-pair FP8 / MXFP4 GEMMs) first wait on a
+barrier phase that nothing completes.  Each such launch must give up after the limit,
 stop its roles, wait out the quiet period in which the copies and MMAs issued before the abort
 land, release its Tensor Memory, and report MOE_ERR_TIMEOUT through moe_check_status.  The test
 build runs in a child process; afterwards this process runs the normal library on the same GPU
@@ -34,6 +35,16 @@ for w in (W.TOY, W.TOY.with_T(333), W.TOY.with_T(1)):
     layer.forward(inp.x)
     print("status", w.name, layer.check_status(), flush=True)
     layer.close()
+# weight formats on the block-scaled kernels (d, d_ff multiples of 128): decode and prefill sizes
+f = W.Workload("fmt_T32", T=32, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX)
+for w in (f, f.with_T(300)):
+    inp = inputs.make_layer_inputs(w, seed=0, device="cuda:0")
+    layer = binding.MoELayer(w, inp)
+    layer.forward_fp8(inp.x, layer.quantize_fp8())
+    print("status", w.name + "_fp8", layer.check_status(), flush=True)
+    layer.forward_mxfp4(inp.x, layer.quantize_mxfp4())
+    print("status", w.name + "_mxfp4", layer.check_status(), flush=True)
+    layer.close()
 """
 
 
@@ -54,7 +65,7 @@ def test_a_wait_that_runs_out_reports_timeout_and_leaves_the_gpu_usable():
                          timeout=600, cwd=ROOT)
     assert out.returncode == 0, out.stderr[-3000:]
     got = [ln.split() for ln in out.stdout.splitlines() if ln.startswith("status")]
-    assert len(got) == 3, out.stdout
+    assert len(got) == 7, out.stdout
     for _, name, st in got:
         assert int(st) == MOE_ERR_TIMEOUT, f"{name}: status {st}, expected MOE_ERR_TIMEOUT"
     # the normal library on the same GPU afterwards
