@@ -1,6 +1,7 @@
 """The debug-bounds build (MOE_DEBUG_BOUNDS=1): internal row indices of the dispatch (scatter
-rows, gathered token rows, token-major destination rows), the grouped GEMMs' output rows and the
-combine's rows are checked before use, and a failed check is reported as MOE_ERR_INTERNAL
+rows, gathered token rows, token-major destination rows, the rows the E4M3 pieces of x are
+written to), the grouped GEMMs' output rows (bf16, FP8 and MXFP4 weights) and the combine's rows
+are checked before use, and a failed check is reported as MOE_ERR_INTERNAL
 instead of addressing memory out of range.  On valid inputs no check may fire and the layer's
 output must equal the default build's bit for bit (the checks only guard accesses).  The build
 runs in a child process; this process runs the default library on the same inputs."""
@@ -17,7 +18,11 @@ from routed_expert_swiglu_gb300 import binding, build, inputs, workloads as W
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-CASES = ["toy_T64", "toy_T333", "v4flash_T300", "v3_T200"]
+# bf16 layers, and a layer with d, d_ff multiples of 128 on FP8 and MXFP4 weights: decode kernels
+# (T = 40), the block-scaled CTA-pair kernels (T = 300), and the token-major split of x (T = 1100)
+CASES = ["toy_T64", "toy_T333", "v4flash_T300", "v3_T200", "fmt_T40:fp8", "fmt_T300:fp8", "fmt_T1100:fp8",
+         "fmt_T40:mxfp4", "fmt_T300:mxfp4"]
+FMT = W.Workload("fmt_T40", T=40, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX)
 
 CHILD = """
 import sys
@@ -37,17 +42,23 @@ np.savez({npz!r}, **out)
 
 
 def workload(name):
-    base, T = name.rsplit("_T", 1)
-    w = {"toy": W.TOY, "v4flash": W.V4FLASH_T8192, "v3": W.V3_T4096}[base]
+    base, T = name.split(":")[0].rsplit("_T", 1)
+    w = {"toy": W.TOY, "v4flash": W.V4FLASH_T8192, "v3": W.V3_T4096, "fmt": FMT}[base]
     return w.with_T(int(T))
 
 
 def run_case(name):
     """The layer's forward on seeded inputs: (output as int16 bit patterns, status)."""
     w = workload(name)
+    fmt = name.split(":")[1] if ":" in name else "bf16"
     inp = inputs.make_layer_inputs(w, seed=11, device=DEV)
     layer = binding.MoELayer(w, inp)
-    y = layer.forward(inp.x, inp.token_ids)
+    if fmt == "fp8":
+        y = layer.forward_fp8(inp.x, layer.quantize_fp8(), inp.token_ids)
+    elif fmt == "mxfp4":
+        y = layer.forward_mxfp4(inp.x, layer.quantize_mxfp4(), inp.token_ids)
+    else:
+        y = layer.forward(inp.x, inp.token_ids)
     st = layer.check_status()
     bits = y.view(torch.int16).cpu().numpy()
     layer.close()
