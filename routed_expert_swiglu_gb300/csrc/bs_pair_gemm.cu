@@ -15,8 +15,9 @@
 // from HBM and want more of their stream in flight).  Roles (480 threads per CTA): warp 0 TMA
 // producer of the codes, warp 14 of the token rows, warp 1 TMEM owner + MMA issuer (even CTA),
 // warps 2..9 epilogue, warps 10..13 A-scale writers (lane quadrant w % 4 of this CTA's Tensor
-// Memory: one word of four UE8M0 scales per code slot, column c0 + quadrant, the layout the MMA
-// reads for M = 128 rows per CTA).  Scale addresses lie on 4-column boundaries.
+// Memory: one word of four UE8M0 scales per K step, at column c0 + quadrant of a slot of their own
+// ring, the layout the MMA reads for M = 128 rows per CTA; reported to the even CTA once per four
+// K steps).  Scale addresses lie on 4-column boundaries.
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -45,13 +46,12 @@ struct BsParams : GemmParams {
   const int8_t* a_sh_sub;  // and of the shared expert's
 };
 
-
 // K steps whose A scales a scale writer loads at once (see the writers' loop).
 constexpr int SF_CHUNK = 16;
 
 template <int EPI, bool F4>
 struct BsPairShape {
-  static constexpr int TN = 224;                        // token rows per tile, both CTAs
+  static constexpr int TN = BS_PAIR_TN;                 // token rows per tile, both CTAs (224)
   static constexpr int HALF = TN / 2;                   // B rows per CTA at most
   static constexpr int BLOCK_K = 128;                   // K per stage: one TMA box, four MMAs
   static constexpr int A_BYTES = BLOCK_M * BLOCK_K;     // this CTA's 128 weight rows in shared memory
