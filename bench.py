@@ -384,6 +384,8 @@ def run_ours(args, world, rank, local):
     layer_bytes = cost.layer_bytes(w, active)
     roof_s = cost.roofline_seconds(layer_flops, layer_bytes, float(peaks["bf16_tflops_sustained"]), hbm_peak)
     gemm_ms = stage_ms[STAGES.index("gate_up_gemm")] + stage_ms[STAGES.index("down_gemm")]
+    gemm_roof_s = cost.roofline_seconds(cost.expert_gemm_flops(w), cost.expert_gemm_bytes(w, active),
+                                        float(peaks["bf16_tflops_sustained"]), hbm_peak)
     e2e_ms, h2d, d2h = measure_e2e(layer, inp, w, args.steps, args.warmup, world)
     prefill_fp8 = prefill_mxfp4 = None
     if not args.no_fp8:
@@ -463,6 +465,10 @@ def run_ours(args, world, rank, local):
                            "peaks": f"{peaks['bf16_tflops_sustained']} TFLOP/s sustained bf16, {hbm_peak} GB/s "
                                     f"({peak_src})"},
         "grouped_gemm_tflops": round(cost.expert_gemm_flops(w) / (gemm_ms / 1e3) / 1e12, 1),
+        "grouped_gemm_roofline": {"ms": round(gemm_roof_s * 1e3, 4), "measured_ms": round(gemm_ms, 4),
+                                  "frac": round(gemm_roof_s * 1e3 / gemm_ms, 4),
+                                  "what": "gate/up + down GEMMs against max(their FLOPs / sustained bf16, "
+                                          "activated expert weights + token rows in and out / HBM)"},
         "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, stage_ms)},
         "e2e": {"value": round(world * w.T * args.steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

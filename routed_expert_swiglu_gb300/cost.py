@@ -52,6 +52,13 @@ def layer_bytes(w: Workload, active_experts: float, T: int | None = None) -> flo
     return weights + router + acts + routing + hashing
 
 
+def expert_gemm_bytes(w: Workload, active_experts: float, T: int | None = None) -> float:
+    """Algorithmic HBM bytes of the two grouped GEMMs: every activated expert's weights (and the
+    shared expert's) once, the token rows in and the layer's rows out."""
+    T = w.T if T is None else T
+    return (active_experts + w.n_shared) * expert_params(w.d, w.d_ff) * BF16 + 2 * T * w.d * BF16
+
+
 def roofline_seconds(flops: float, nbytes: float, peak_tflops: float, peak_gbs: float) -> float:
     """max(compute time, memory time) at the given peaks."""
     return max(flops / (peak_tflops * 1e12), nbytes / (peak_gbs * 1e9))
