@@ -199,16 +199,16 @@ moe_status moe_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int32_t n_
  * [E, d, d_ff] hold E4M3 codes, e13 [E, ceil(2*d_ff/128), ceil(d/128)] and e2 [E, ceil(d/128),
  * ceil(d_ff/128)] their tile exponents, as moe_quantize_fp8 writes them (shared expert: the
  * same with E = 1; NULL without one).  The layer is moe_forward on the dequantised weights
- * q * 2^e, with the activations kept at bf16-level precision.  Batches above 64 tokens stream
- * the codes (half the weight bytes) into CTA-pair kernels that widen them to bf16 q * 2^e in
- * shared memory and run the bf16 MMA on the same activations as moe_forward (bf16 x, the (hi,
- * lo) bf16 pair for h).  Batches of at most 64 tokens with d and d_ff multiples of 128 feed the
- * codes straight to the FP8 tensor-core MMA, with the activations as sums of E4M3 pieces (piece p
- * weighted 2^(-4p)) and one power-of-two scale per row: x in two pieces, exact for every value
+ * q * 2^e, with the activations kept at bf16-level precision.  With d and d_ff multiples of 128
+ * the codes go straight to the tensor cores, with the activations as sums of E4M3 pieces (piece
+ * p weighted 2^(-4p)) and one power-of-two scale per row: x in two pieces, exact for every value
  * above 2^-13.8 of its row's largest magnitude and within 2^-21 of that magnitude below it; h in
- * four pieces, within 2^-16 of each value plus 2^-29 of the row's largest magnitude; other shapes
- * widen the codes to bf16 into Tensor Memory.  Code pointers 16-byte aligned; same workspace and
- * outputs as moe_forward. */
+ * four pieces, within 2^-16 of each value plus 2^-29 of the row's largest magnitude.  Batches of
+ * at most 64 tokens run the 8-bit MMA with the tile scales applied per K tile; larger batches the
+ * block-scaled 2-SM MMA (kind::mxf8f6f4), the tile scales applied by the tensor cores.  Other
+ * shapes widen the codes to bf16 (in Tensor Memory at decode sizes, in shared memory on CTA pairs
+ * above) and run the bf16 MMA on moe_forward's activations (bf16 x, the (hi, lo) pair for h).
+ * Code pointers 16-byte aligned; same workspace and outputs as moe_forward. */
 moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                            const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,
                            const uint8_t* q2, const int8_t* e2, const uint8_t* q13_sh, const int8_t* e13_sh,
