@@ -204,10 +204,13 @@ moe_status moe_mxfp4_to_fp8(const uint8_t* codes, const int8_t* exps, int32_t n_
  * p weighted 2^(-4p)) and one power-of-two scale per row: x in two pieces, exact for every value
  * above 2^-13.8 of its row's largest magnitude and within 2^-21 of that magnitude below it; h in
  * four pieces, within 2^-16 of each value plus 2^-29 of the row's largest magnitude.  Batches of
- * at most 64 tokens run the 8-bit MMA with the tile scales applied per K tile; larger batches the
- * block-scaled 2-SM MMA (kind::mxf8f6f4), the tile scales applied by the tensor cores.  Other
- * shapes widen the codes to bf16 (in Tensor Memory at decode sizes, in shared memory on CTA pairs
- * above) and run the bf16 MMA on moe_forward's activations (bf16 x, the (hi, lo) pair for h).
+ * at most 64 tokens, or that route at most 48 rows to an expert on average (T k <= 48 E), stream
+ * the weights through single-CTA kernels (the 8-bit MMA, the tile scales applied per K tile);
+ * larger batches run the block-scaled 2-SM MMA (kind::mxf8f6f4), the tile scales applied by the
+ * tensor cores.  Other shapes widen the codes to bf16 (in Tensor Memory on the single-CTA
+ * kernels, in shared memory on CTA pairs) and run the bf16 MMA on moe_forward's activations
+ * (bf16 x, the (hi, lo) pair for h).  moe_forward and moe_forward_mxfp4 choose between their
+ * single-CTA and CTA-pair kernels by the same rule.
  * Code pointers 16-byte aligned; same workspace and outputs as moe_forward. */
 moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t* token_ids,
                            const moe_bf16* w_r, const float* bias, const uint8_t* q13, const int8_t* e13,

@@ -40,15 +40,24 @@ constexpr int PERMUTE_CHUNK = 1024;  // assignments per block in the dispatch ke
 // Largest activation row (bytes, staged as fp32) the E4M3 split kernel takes.
 constexpr size_t SPLIT_SMEM_MAX = 200 * 1024;
 
-// Batches of at most 64 tokens run the single-CTA (decode) kernels with 64-row token tiles
-// (16- and 32-row tiles, which leave more of each stage to the weight slab, measured slower).
-inline bool is_decode(int T) { return T <= 64; }
+// Which kernels run the expert GEMMs.  A batch that routes at most 48 rows to an expert on
+// average (T k <= 48 E), or has at most 64 tokens, runs the weight-streaming single-CTA kernels
+// (64-row token tiles; 16- and 32-row tiles, which leave more of each stage to the weight slab,
+// measured slower in bf16); larger ones run the CTA-pair kernels (2-SM MMA, 256 weight rows
+// against up to 256 token rows per tile).  Measured with the V4-Flash and V3 layer shapes: up to
+// 48 rows per expert the streaming kernels were faster (bf16 layer 3 to 11 %, FP8 and MXFP4
+// weights 1.3 to 2.8x), at 64 and more slower.
+constexpr long long STREAM_MAX_ROWS_PER_EXPERT = 48;
+inline bool streams_weights(int T, int k, int E) {
+  return T <= 64 || (long long)T * k <= STREAM_MAX_ROWS_PER_EXPERT * E;
+}
 
 // Token-tile width (B-operand rows per tile) of the expert GEMMs and their schedule.
-inline int token_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
+inline int token_tile_for(int T, int k, int E) { return streams_weights(T, k, E) ? 64 : MOE_TN_PREFILL; }
 
-// Token-tile width of the router GEMM.
-inline int router_tile_for(int T) { return is_decode(T) ? 64 : MOE_TN_PREFILL; }
+// Token-tile width of the router GEMM: 64-row tiles up to 3072 tokens (measured faster there),
+// 256-row tiles above.
+inline int router_tile_for(int T) { return T <= 3072 ? 64 : MOE_TN_PREFILL; }
 
 // Token rows per tile of the block-scaled CTA-pair kernels (FP8 / MXFP4 weights at prefill):
 // the most that leaves Tensor Memory room for the scales beside two accumulator buffers.

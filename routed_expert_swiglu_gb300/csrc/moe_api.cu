@@ -46,7 +46,7 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.T = T;
   L.N = T * k;
   L.G = E + sh;
-  L.TN = token_tile_for(T);
+  L.TN = token_tile_for(T, k, E);
   L.nblk = ceil_div(L.N > 0 ? L.N : 1, PERMUTE_CHUNK);
   // row tiles of the narrowest schedule a forward may build
   const int tn_sched = 16;  // the narrowest: the MXFP4 kernels' 16-row tiles
@@ -292,8 +292,9 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   // 2-SM MMA, E4M3-piece activations, 224-row token tiles); FP8 shapes they do not take (d or
   // d_ff not a multiple of 128): codes widened to bf16 in shared memory on the CTA-pair kernels,
   // bf16 activations (the dispatched rows and the (hi, lo) pair), the bf16 path's schedule
-  const bool bs_pair = q8 != nullptr && !is_decode(T) && fp8_mma_shapes(c);
-  const bool f8pair = q8 != nullptr && !f4 && !is_decode(T) && !fp8_mma_shapes(c);
+  const bool stream = streams_weights(T, c.top_k, E);
+  const bool bs_pair = q8 != nullptr && !stream && fp8_mma_shapes(c);
+  const bool f8pair = q8 != nullptr && !f4 && !stream && !fp8_mma_shapes(c);
   const bool f8mma = q8 != nullptr && !f8pair && fp8_mma_shapes(c);
   const int sched_tn = (q8 == nullptr || f8pair) ? L.TN
                        : bs_pair                 ? BS_PAIR_TN
@@ -346,7 +347,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g1.b_sh_rows = T;
   g1.K = d;
   g1.mblk = 1;
-  g1.pair = !is_decode(T);
+  g1.pair = !stream;
   g1.num_mblocks = ceil_div(f, gemm_features_per_tile(0, 1));
   g1.a_rows_per_group = 2 * f;
   g1.a_up_offset = f;
@@ -407,7 +408,7 @@ moe_status run_experts(const moe_plan* p, int T, const moe_bf16* x, const int32_
   g2.hilo = 1;         // B rows hold the (hi, lo) pair: 2*f values, each pair against one W2 block
   g2.mblk = 2;         // decode: two 128-feature blocks per CTA; prefill: a pair tile covers 256
   g2.kernel_tn = L.TN;
-  g2.pair = !is_decode(T);
+  g2.pair = !stream;
   g2.num_mblocks = ceil_div(d, gemm_features_per_tile(1, g2.mblk));
   g2.a_rows_per_group = d;
   g2.out_features = d;

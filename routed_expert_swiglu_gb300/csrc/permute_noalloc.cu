@@ -36,7 +36,7 @@ constexpr int NOALLOC_MAX_ASSIGN = 131072;
 constexpr int NOALLOC_MAX_BLOCKS = NOALLOC_MAX_ASSIGN / PERMUTE_CHUNK;
 constexpr int NOALLOC_MAX_GROUPS = MAX_EXPERTS + 1;  // routed + shared
 // row tiles of the schedule: at most E + ceil(N / 64) + ceil(T / 64) + 1 with T <= N, for the
-// schedule's row tiles of token_tile_for(T) >= 64 rows
+// schedule's row tiles of at least 64 rows (token_tile_for gives 64 or MOE_TN_PREFILL)
 static_assert(MOE_TN_PREFILL >= 64, "the fixed scratch is sized for row tiles of at least 64 rows");
 constexpr int NOALLOC_MAX_ROWTILES = MAX_EXPERTS + 2 * (NOALLOC_MAX_ASSIGN / 64) + 2;
 
@@ -103,7 +103,7 @@ extern "C" moe_status moe_permute_noalloc(moe_plan* plan, int32_t T, const int32
   pm.k = c.top_k;
   pm.E = c.n_experts;
   pm.n_shared = c.n_shared;
-  pm.TN = token_tile_for(T);
+  pm.TN = token_tile_for(T, c.top_k, c.n_experts);
   pm.nblk = (int)((N + PERMUTE_CHUNK - 1) / PERMUTE_CHUNK);
   pm.blockhist = reinterpret_cast<int32_t*>(base + OFF_HIST);
   pm.counts = counts;

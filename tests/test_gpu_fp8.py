@@ -70,16 +70,20 @@ def small(w, T, **kw):
     return dataclasses.replace(w, T=T, name=f"{w.name.rsplit('_T', 1)[0]}_T{T}", **kw)
 
 
-# Batches above 64 tokens (prefill) run the block-scaled CTA-pair kernels (codes and tile scales
-# into the 2-SM MMA, E4M3-piece activations; d, d_ff multiples of 128: v3_T96, tall_T1500 with
-# two 224-row tiles per expert, edges_T80) or, for other shapes, the CTA-pair kernels that widen
-# the codes to bf16 in shared memory (toy_T333, ragged_T150); decode batches the direct 8-bit MMA
-# (d, d_ff multiples of 128) or, for other shapes, the single-CTA widening kernels.
+# Batches that route more than 48 rows to an expert on average run the block-scaled CTA-pair
+# kernels (codes and tile scales into the 2-SM MMA, E4M3-piece activations; d, d_ff multiples of
+# 128: v3_E32_T400, tall_T1500 with two 224-row tiles per expert) or, for other shapes, the
+# CTA-pair kernels that widen the codes to bf16 in shared memory (toy_T333, ragged_T400); smaller
+# ones (up to 64 tokens, or at most 48 rows per expert: ragged_T150, v3_T96, edges_T80) stream the
+# weights through the single-CTA kernels: the direct 8-bit MMA (d, d_ff multiples of 128) or, for
+# other shapes, the single-CTA widening kernels.
 CASES = [
-    W.TOY,                                                                  # decode kernels
-    small(W.TOY, 333),                                                      # prefill: CTA-pair widening
+    W.TOY,                                                                  # single-CTA kernels
+    small(W.TOY, 333),                                                      # CTA-pair widening
     W.Workload("mid_T64", T=64, d=512, d_ff=256, E=16, k=4, n_shared=1, score=W.SCORE_SIGMOID, use_bias=True),
     W.Workload("ragged_T150", T=150, d=320, d_ff=192, E=12, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
+    W.Workload("ragged_T400", T=400, d=320, d_ff=192, E=12, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
+    small(W.V3_T4096, 400, E=32, n_groups=8, topk_groups=4, group_topk=2, d=1024, d_ff=256),
     # decode with d, d_ff not multiples of 128: single-CTA widening kernels
     W.Workload("ragged_T48", T=48, d=320, d_ff=192, E=12, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
     # decode with 64-row direct-MMA tiles (T k > 24 E)
@@ -114,10 +118,11 @@ def test_fp8_layer_vs_oracle(w):
     layer.close()
 
 
-def test_fp8_layer_with_zero_subnormal_and_tiny_scale_codes():
+@pytest.mark.parametrize("T", [80, 300])  # 30 rows per expert: single-CTA kernels; 112.5: CTA pairs
+def test_fp8_layer_with_zero_subnormal_and_tiny_scale_codes(T):
     """Weights with exact zeros, values that quantise to subnormal codes, and one expert scaled
     down to a tile exponent below -120: every code class of the converter, against the oracle."""
-    w = W.Workload("edges_T80", T=80, d=256, d_ff=128, E=8, k=3, n_shared=1, score=W.SCORE_SOFTMAX)
+    w = W.Workload(f"edges_T{T}", T=T, d=256, d_ff=128, E=8, k=3, n_shared=1, score=W.SCORE_SOFTMAX)
     inp = inputs.make_layer_inputs(w, seed=23, device=DEV)
     g = torch.Generator(device=DEV).manual_seed(5)
     for t in (inp.w13, inp.w2, inp.w13_sh, inp.w2_sh):

@@ -142,7 +142,10 @@ NATIVE = [
                use_bias=True),
     # decode with 64-row token tiles (32 rows per expert on average)
     W.Workload("deep_T64", T=64, d=256, d_ff=384, E=4, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
-    # prefill batches: the block-scaled CTA-pair kernels (224-row token tiles), one ragged tile per
+    # a larger batch at 37.5 rows per expert: still the weight-streaming kernels (64-row tiles,
+    # the shared expert's 200 rows in four, the last ragged)
+    W.Workload("stream_T200", T=200, d=384, d_ff=256, E=16, k=3, n_shared=1, score=W.SCORE_SOFTMAX),
+    # more than 48 rows per expert: the block-scaled CTA-pair kernels (224-row token tiles), one ragged tile per
     # expert, and two per expert (about 256 rows each; d = 384: the down projection's second
     # 256-feature block lies half past the matrix)
     W.Workload("tall_T300", T=300, d=256, d_ff=256, E=8, k=2, n_shared=1, score=W.SCORE_SOFTMAX),
