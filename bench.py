@@ -6,9 +6,11 @@ One step = one whole layer forward (router GEMM, top-k, dispatch, gate/up groupe
 grouped GEMM, combine) over one batch of T synthetic tokens whose inputs are resident in HBM.
 Default workload: the DeepSeek-V4-Flash-shaped layer at T=8192 (prefill), also with FP8 expert
 weights ("fp8_weights") and MXFP4 expert weights ("mxfp4_weights"); the same line carries the same layer with Zipf-skewed routing under
-"skewed", and a T=64 (decode) measurement under "decode", with the same layer on FP8 expert
-weights ("fp8_weights") and on MXFP4 expert weights ("mxfp4_weights": the one-time conversion to
-the FP8 form, the forward on the converted tiles, and the native forward on the 4-bit codes).
+"skewed", a T=64 (decode) measurement under "decode" and a T=1024 batch of the main workload's
+shapes under "small_prefill" (24 rows per routed expert: the weight-streaming single-CTA
+kernels), each with the same layer on FP8 expert weights ("fp8_weights") and on MXFP4 expert
+weights ("mxfp4_weights": the one-time conversion to the FP8 form, the forward on the converted
+tiles, and the native forward on the 4-bit codes).
 Multi-GPU runs are independent replicas (one process per GPU, each with its own token batch; no
 collective on the data path).
 
@@ -282,6 +284,32 @@ def measure_mxfp4(layer, inp, w, steps, warmup, fp8_ms, bf16_ms, world):
     return res
 
 
+def measure_leg(wl, args, device, rank, world, peaks, hbm_peak):
+    """One more workload on the same line: the bf16 layer (stage times, HBM bytes and the
+    layer roofline) and, unless --no-fp8, the same layer on FP8 and on MXFP4 expert weights."""
+    steps = max(args.steps, 10)
+    ll, linp, lms, lstage, lactive, _ = measure_workload(wl, steps, args.warmup, device, seed=rank, world=world,
+                                                         rank=rank)
+    lms = max_over_ranks(lms, world) / steps
+    lbytes = cost.layer_bytes(wl, lactive)
+    roof = cost.roofline_seconds(cost.layer_flops(wl), lbytes, float(peaks["bf16_tflops_sustained"]), hbm_peak)
+    leg = {"workload": wl.name, "T": wl.T, "rows_per_expert": round(wl.T * wl.k / wl.E, 2),
+           "ms_per_step": round(lms, 4), "tokens_per_s": round(world * wl.T / (lms / 1e3), 1),
+           "active_experts": lactive, "layer_bytes": int(lbytes),
+           "hbm_gbs_layer": round(lbytes / (lms / 1e3) / 1e9, 1),
+           "hbm_frac_layer": round(lbytes / (lms / 1e3) / 1e9 / hbm_peak, 4),
+           "layer_roofline_ms": round(roof * 1e3, 4), "layer_roofline_frac": round(roof * 1e3 / lms, 4),
+           "stage_ms": {s: round(v, 4) for s, v in zip(STAGES, lstage)}}
+    if not args.no_fp8:
+        leg["fp8_weights"] = measure_fp8(ll, linp, wl, steps, args.warmup, lactive, lms, hbm_peak, world)
+        leg["mxfp4_weights"] = measure_mxfp4(ll, linp, wl, steps, args.warmup, leg["fp8_weights"]["ms_per_step"],
+                                             lms, world)
+    ll.close()
+    del ll, linp
+    torch.cuda.empty_cache()
+    return leg
+
+
 def measure_e2e(layer, inp, w, steps, warmup, world):
     """Same metric through moe_forward_host: pinned host x in, pinned host y out, copies timed."""
     from routed_expert_swiglu_gb300 import binding
@@ -439,6 +467,10 @@ def run_ours(args, world, rank, local):
         del dl, dinp
         torch.cuda.empty_cache()
 
+    small = None
+    if 0 < args.small_prefill_tokens != w.T:
+        small = measure_leg(w.with_T(args.small_prefill_tokens), args, device, rank, world, peaks, hbm_peak)
+
     line = {
         "metric": "MoE-layer tokens/s (V4-Flash shape)",
         "value": round(tokens_per_s, 1),
@@ -478,6 +510,7 @@ def run_ours(args, world, rank, local):
         "fp8_weights": prefill_fp8,
         "mxfp4_weights": prefill_mxfp4,
         "decode": decode,
+        "small_prefill": small,
         "skewed": skewed,
         "cpu_baseline": cpu,
     }
@@ -581,6 +614,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="v4flash_T8192", choices=sorted(workloads.BY_NAME))
     ap.add_argument("--decode-workload", default="v4flash_T64", help="second (decode) workload, or none")
+    ap.add_argument("--small-prefill-tokens", type=int, default=1024,
+                    help="T of a small prefill batch on the main workload's shapes (0: none)")
     ap.add_argument("--skew-workload", default="v4flash_zipf_T8192",
                     help="the same layer with Zipf-skewed routing, timed alongside (or none)")
     ap.add_argument("--cpu-tokens", type=int, default=8192,
