@@ -156,7 +156,7 @@ struct PermuteLaunch {
   const void* x; void* xd; int d; int num_sms;
 };
 cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s);
-int permute_launch_count(bool gather);
+int permute_launch_count(bool gather, long long N);  // N = T * k assignments
 
 // Activation rows -> E4M3 pieces and one exponent per row (the B operand of the q8 = 2 GEMMs):
 // bf16 rows (2 pieces; row r < n_gather is row gather[r] of src, later rows row r - n_gather)

@@ -787,7 +787,8 @@ moe_status moe_plan_set_events(moe_plan* plan, moe_event_t* events, int32_t n_ev
 
 int32_t moe_forward_launch_count(const moe_plan* plan, int32_t T) {
   if (plan == nullptr || T <= 0) return 0;
-  return 2 /* router GEMM, top-k */ + permute_launch_count(true) + 2 /* grouped GEMMs */ +
+  return 2 /* router GEMM, top-k */ + permute_launch_count(true, (long long)T * plan->cfg.top_k) +
+         2 /* grouped GEMMs */ +
          1 /* combine */;
 }
 

@@ -6,6 +6,7 @@
 // Assignment i = t*k + j.  Rows are ordered by expert and, inside an expert, by i.  Integer
 // only, so the result is exact and independent of scheduling:
 //   1. hist     per-chunk expert histograms (chunk = 1024 consecutive assignments)
+//               (a batch of one chunk runs steps 1 to 3 in one block: permute_small_kernel)
 //   2. scan     per-expert prefix over chunks, exclusive scan over experts (offsets), and the
 //               grouped-GEMM schedule: row tiles per group and the row-tile -> group map
 //   3. scatter  rank inside the chunk from warp match masks + per-warp prefix, so row =
@@ -154,6 +155,75 @@ __global__ void __launch_bounds__(PERMUTE_CHUNK) scatter_kernel(const int32_t* _
   }
 }
 
+// Steps 1 to 3 in one block for a batch of at most one chunk of assignments (decode sizes): the
+// same integer arithmetic as hist + scan + scatter with a single chunk (no earlier chunks), in one
+// launch instead of three.  Expert counts come from the per-warp match counts, the offsets and the
+// schedule from the block scan over experts.
+__global__ void __launch_bounds__(PERMUTE_CHUNK) permute_small_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int N, int k, int E, int n_shared, int T, int TN,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int4* __restrict__ grp, int32_t* __restrict__ rt2g,
+    int32_t* __restrict__ perm_tok, int32_t* __restrict__ inv, float* __restrict__ row_w, int* err) {
+  extern __shared__ int wcnt[];  // [32 warps][E], then the per-expert totals / offsets [E]
+  __shared__ int s_warp[32];
+  int* tot = wcnt + 32 * E;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int x = threadIdx.x; x < 32 * E; x += blockDim.x) wcnt[x] = 0;
+  __syncthreads();
+  const int i = threadIdx.x;
+  const bool valid = i < N;
+  const int e = valid ? clamp_expert(__ldg(ids + i), E, err) : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int run = 0;
+    for (int v = 0; v < 32; ++v) {
+      const int c = wcnt[v * E + x];
+      wcnt[v * E + x] = run;
+      run += c;
+    }
+    tot[x] = run;
+  }
+  __syncthreads();
+  // expert-level scan and the grouped-GEMM schedule, thread g = group g (as in scan_kernel)
+  const int g = threadIdx.x;
+  const int cnt = g < E ? tot[g] : 0;
+  int total_rows;
+  const int off = block_excl_scan(cnt, s_warp, total_rows);
+  if (g < E) {
+    counts[g] = cnt;
+    offsets[g] = off;
+  }
+  if (g == 0) offsets[E] = total_rows;
+  const int G = E + n_shared;
+  int rows = 0, row_base = 0;
+  if (g < E) {
+    rows = cnt;
+    row_base = off;
+  } else if (g < G) {
+    rows = T;
+    row_base = N;
+  }
+  const int R = (rows + TN - 1) / TN;
+  int total_rt;
+  const int rt_start = block_excl_scan(R, s_warp, total_rt);
+  if (g < G) {
+    grp[g] = make_int4(row_base, rows, rt_start, 0);
+    for (int j = 0; j < R; ++j) rt2g[rt_start + j] = g;
+  }
+  if (g == 0) grp[G] = make_int4(0, 0, total_rt, 0);
+  if (g < E) tot[g] = off;  // only thread g read tot[g] as a count, above
+  __syncthreads();
+  if (valid) {
+    const int row = tot[e] + wcnt[warp * E + e] + rank;
+    if (bad_index(row, N, err)) return;
+    if (perm_tok) perm_tok[row] = i / k;
+    if (inv) inv[i] = row;
+    if (row_w) row_w[row] = __ldg(w + i);
+  }
+}
+
 // X_dispatch[row] = x[perm_tok[row]]: row-major, one warp per row, 8 x 16 bytes per lane in
 // flight.  Used for small batches, where one warp per token would leave most SMs idle.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int4* __restrict__ x, int4* __restrict__ xd,
@@ -220,24 +290,36 @@ __global__ void __launch_bounds__(256) dispatch_rows_kernel(const int4* __restri
   }
 }
 
-int permute_launch_count(bool gather) { return gather ? 4 : 3; }
+int permute_launch_count(bool gather, long long N) { return (N <= PERMUTE_CHUNK ? 1 : 3) + (gather ? 1 : 0); }
 
 cudaError_t launch_permute(const PermuteLaunch& L, cudaStream_t s) {
   const int N = L.T * L.k;
-  hist_kernel<<<L.nblk, 256, 0, s>>>(L.topk_ids, N, L.E, L.blockhist, L.err);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  scan_kernel<<<1, 1024, 0, s>>>(L.blockhist, L.nblk, L.E, L.n_shared, L.T, N, L.TN, L.counts, L.offsets, L.grp,
-                                 L.rt2g);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int smem = 32 * L.E * (int)sizeof(int);
-  if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (N <= PERMUTE_CHUNK) {
+    const int smem = 33 * L.E * (int)sizeof(int);
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
+    permute_small_kernel<<<1, PERMUTE_CHUNK, smem, s>>>(L.topk_ids, L.topk_w, N, L.k, L.E, L.n_shared, L.T, L.TN,
+                                                         L.counts, L.offsets, L.grp, L.rt2g, L.perm_tok, L.inv,
+                                                         L.row_w, L.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
+    hist_kernel<<<L.nblk, 256, 0, s>>>(L.topk_ids, N, L.E, L.blockhist, L.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    scan_kernel<<<1, 1024, 0, s>>>(L.blockhist, L.nblk, L.E, L.n_shared, L.T, N, L.TN, L.counts, L.offsets, L.grp,
+                                   L.rt2g);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int smem = 32 * L.E * (int)sizeof(int);
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
+    scatter_kernel<<<L.nblk, PERMUTE_CHUNK, smem, s>>>(L.topk_ids, L.topk_w, N, L.k, L.E, L.blockhist, L.offsets,
+                                                        L.perm_tok, L.inv, L.row_w, L.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  scatter_kernel<<<L.nblk, PERMUTE_CHUNK, smem, s>>>(L.topk_ids, L.topk_w, N, L.k, L.E, L.blockhist, L.offsets,
-                                                      L.perm_tok, L.inv, L.row_w, L.err);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.xd != nullptr) {
     const int vec = L.d / 8;
     const int cap = L.num_sms * 8;

@@ -62,7 +62,10 @@ def test_router_logits_and_routing(w):
 
 
 PERMUTE_CASES = [(1, 1, 1, 0.0), (5, 8, 2, 0.0), (64, 8, 2, 0.0), (1000, 256, 6, 0.0), (777, 256, 8, 3.0),
-                 (4099, 384, 6, 0.0), (2048, 8, 2, 0.0), (300, 256, 6, 50.0)]
+                 (4099, 384, 6, 0.0), (2048, 8, 2, 0.0), (300, 256, 6, 50.0),
+                 # one chunk of assignments (the single-block path) at its limit with the most experts,
+                 # and just past it
+                 (128, 512, 8, 3.0), (171, 64, 6, 0.0)]
 
 
 @pytest.mark.parametrize("T,E,k,skew", PERMUTE_CASES)
