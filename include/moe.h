@@ -119,8 +119,11 @@ moe_status moe_plan_destroy(moe_plan* plan);
  * moe_forward_routed and moe_forward_host. */
 size_t moe_workspace_bytes(const moe_plan* plan, int32_t T);
 
-/* Router: logits = x W_r^T (bf16 inputs, fp32 accumulation, tensor cores), then scoring,
- * optional bias / groups / hash lookup, top-k and gate weights.
+/* Router: logits = x W_r^T (bf16 inputs, fp32 accumulation), then scoring, optional bias /
+ * groups / hash lookup, top-k and gate weights.  The logits run on the tensor cores and the
+ * selection in a second kernel; batches of at most 64 tokens over at most 64 experts run both in
+ * one kernel (the logits in K slices of 256 on the CUDA cores, summed in slice order before the
+ * selection).
  *   topk_ids [T,k] int32 out: descending selection key, ties -> lower expert id (hash: table
  *   order); topk_w [T,k] fp32 out.  logits [T,E] fp32 out, optional (NULL = not exported).
  *   token_ids is required iff the plan uses hash routing; bias may be NULL. */
@@ -301,7 +304,8 @@ typedef struct {
 moe_status moe_workspace_views(const moe_plan* plan, int32_t T, void* ws, moe_ws_views* out);
 
 /* Stage timing.  With events set, moe_forward / moe_forward_routed record events[0] before
- * the first launch and events[i] after stage i (stages: 1 router GEMM, 2 top-k,
+ * the first launch and events[i] after stage i (stages: 1 router GEMM, 2 top-k (empty where the
+ * router is one kernel, see moe_route),
  * 3 dispatch (histogram, scan, scatter, row gather), 4 gate/up grouped GEMM, 5 down grouped
  * GEMM, 6 combine; moe_forward_routed records the stages it runs).  n_events must be
  * >= moe_forward_stage_count() + 1; NULL / 0 disables.  Events are the caller's. */

@@ -574,6 +574,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int slot = 0;
     uint32_t sphase = 0;
     bool ok = true;
+#if MOE_TEST_UNSET_WAIT
+    // test build: wait on a phase nothing completes (only these warps arrive on it), so the
+    // wait runs out and the kernel takes its abort path
+    if (!mbar_wait(sempty_bar(0), 0, abort_flag, p.err)) ok = false;
+#endif
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<TN>(tile, p);
       if (t.rows <= 0) continue;

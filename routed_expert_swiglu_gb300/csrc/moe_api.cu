@@ -3,6 +3,8 @@
 // combine on the caller's stream.  No device allocation, no host synchronisation (except
 // moe_check_status).
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -58,7 +60,7 @@ WsLayout ws_layout(const moe_config& c, int T) {
     off = align_up(off + (bytes ? bytes : 1), 256);
     return at;
   };
-  L.err = take(256);
+  L.err = take(ERR_BLOCK_BYTES);
   // Input staging of moe_forward_host: two slots (alternate calls) of max_tokens rows, at the
   // same offsets for every T, so that a side-stream copy into one never overlaps a buffer of
   // another call on the same workspace.
@@ -66,7 +68,9 @@ WsLayout ws_layout(const moe_config& c, int T) {
   L.tok_stage = take((size_t)2 * c.max_tokens * 4);
   L.topk_ids = take((size_t)T * k * 4);
   L.topk_w = take((size_t)T * k * 4);
-  L.logits = take((size_t)router_ksplit(c, T) * T * E * 4);  // partial logits of the K slices
+  // partial logits of the K slices (the tensor-core router's, or the fused small-batch router's)
+  const int slabs = std::max(router_ksplit(c, T), router_fused(T, E) ? router_fused_slices(d) : 1);
+  L.logits = take((size_t)slabs * T * E * 4);
   L.blockhist = take((size_t)L.nblk * E * 4);
   L.counts = take((size_t)E * 4);
   L.offsets = take((size_t)(E + 1) * 4);
@@ -198,6 +202,44 @@ moe_status run_route(const moe_plan* p, int T, const moe_bf16* x, const int32_t*
   const moe_config& c = p->cfg;
   const WsLayout L = ws_layout(c, T);
   int* err = at<int>(ws, L.err);
+  if (router_fused(T, c.n_experts)) {
+    // one launch: logits in K slices, the last block of each token group sums them and selects
+    RouterFusedLaunch rf;
+    memset(&rf, 0, sizeof(rf));
+    rf.x = x;
+    rf.w_r = w_r;
+    rf.T = T;
+    rf.d = c.d;
+    rf.E = c.n_experts;
+    rf.partial = at<float>(ws, L.logits);
+    rf.counters = reinterpret_cast<int*>(at<char>(ws, L.err) + ROUTER_COUNTERS_OFFSET);
+    TopkLaunch& tk = rf.tk;
+    tk.logits = rf.partial;
+    tk.nsplit = router_fused_slices(c.d);
+    tk.split_stride = (long long)T * c.n_experts;
+    tk.logits_out = logits;  // the summed logits (over slab 0 of the token's row when it is the workspace's)
+    tk.bias = bias;
+    tk.T = T;
+    tk.E = c.n_experts;
+    tk.k = c.top_k;
+    tk.score = c.score;
+    tk.n_groups = c.n_groups;
+    tk.topk_groups = c.topk_groups;
+    tk.group_topk = c.group_topk;
+    tk.token_ids = token_ids;
+    tk.tid2eid = c.tid2eid;
+    tk.vocab = c.vocab;
+    tk.topk_ids = ids;
+    tk.topk_w = w;
+    tk.err = err;
+    {
+      LaunchRange r("moe.router_fused");
+      MOE_CUDA(launch_router_fused(rf, s));
+    }
+    record(p, ST_ROUTER_GEMM, s);
+    record(p, ST_TOPK, s);
+    return MOE_OK;
+  }
   GemmLaunch g;
   memset(&g, 0, sizeof(g));
   g.epi = 1;
@@ -531,7 +573,7 @@ moe_status moe_route(moe_plan* plan, int32_t T, const moe_bf16* x, const int32_t
   MOE_TRY(num_sms(&sms));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(plan->cfg, T);
-  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, ERR_BLOCK_BYTES, s));
   float* lg = logits != nullptr ? logits : at<float>(ws, L.logits);
   return run_route(plan, T, x, token_ids, w_r, bias, lg, topk_ids, topk_w, ws, sms, s);
 }
@@ -586,7 +628,7 @@ moe_status moe_forward(moe_plan* plan, int32_t T, const moe_bf16* x, const int32
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(plan->cfg, T);
   record(plan, ST_START, s);
-  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, ERR_BLOCK_BYTES, s));
   int32_t* ids = at<int32_t>(ws, L.topk_ids);
   float* w = at<float>(ws, L.topk_w);
   MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
@@ -615,7 +657,7 @@ moe_status moe_forward_fp8(moe_plan* plan, int32_t T, const moe_bf16* x, const i
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(plan->cfg, T);
   record(plan, ST_START, s);
-  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, ERR_BLOCK_BYTES, s));
   int32_t* ids = at<int32_t>(ws, L.topk_ids);
   float* w = at<float>(ws, L.topk_w);
   MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
@@ -645,7 +687,7 @@ moe_status moe_forward_mxfp4(moe_plan* plan, int32_t T, const moe_bf16* x, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(plan->cfg, T);
   record(plan, ST_START, s);
-  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, ERR_BLOCK_BYTES, s));
   int32_t* ids = at<int32_t>(ws, L.topk_ids);
   float* w = at<float>(ws, L.topk_w);
   MOE_TRY(run_route(plan, T, x, token_ids, w_r, bias, at<float>(ws, L.logits), ids, w, ws, sms, s));
@@ -668,7 +710,7 @@ moe_status moe_forward_routed(moe_plan* plan, int32_t T, const moe_bf16* x, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(plan->cfg, T);
   record(plan, ST_START, s);
-  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, sizeof(int), s));
+  MOE_CUDA(cudaMemsetAsync(at<int>(ws, L.err), 0, ERR_BLOCK_BYTES, s));
   record(plan, ST_ROUTER_GEMM, s);
   record(plan, ST_TOPK, s);
   return run_experts(plan, T, x, topk_ids, topk_w, w13, w2, w13_sh, w2_sh, out, ws, sms, s);
@@ -787,7 +829,8 @@ moe_status moe_plan_set_events(moe_plan* plan, moe_event_t* events, int32_t n_ev
 
 int32_t moe_forward_launch_count(const moe_plan* plan, int32_t T) {
   if (plan == nullptr || T <= 0) return 0;
-  return 2 /* router GEMM, top-k */ + permute_launch_count(true, (long long)T * plan->cfg.top_k) +
+  return (router_fused(T, plan->cfg.n_experts) ? 1 : 2) /* router GEMM and top-k (fused for small ones) */ +
+         permute_launch_count(true, (long long)T * plan->cfg.top_k) +
          2 /* grouped GEMMs */ +
          1 /* combine */;
 }

@@ -54,13 +54,13 @@ __device__ __forceinline__ float pick(const float (&a)[PL], int i) {
   return v;
 }
 
+// Selection for token t by one warp: the logits (summed over the K slices), scores, bias, group
+// limits or hash lookup, top-k and the gate weights, written to topk_ids / topk_w (and the summed
+// logits to logits_out when given).  s_keys: PL * 32 floats of shared memory for this warp.
 template <int PL>
-__global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
+__device__ __forceinline__ void route_token(const TopkLaunch& a, int t, float* s_keys) {
   constexpr int MAX_PER_LANE = PL;
-  __shared__ float s_keys[TOPK_WARPS][PL * 32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * TOPK_WARPS + warp;
-  if (t >= a.T) return;  // whole warp leaves together
+  const int lane = threadIdx.x & 31;
   const int E = a.E, k = a.k, mode = a.score;
   const float* lrow = a.logits + (size_t)t * E;  // slab 0; slab s at + s * split_stride
 
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
 #pragma unroll
   for (int i = 0; i < MAX_PER_LANE; ++i) {
     const int e = lane + 32 * i;
-    l[i] = (e < E) ? lrow[e] : -INFINITY;
+    l[i] = (e < E) ? __ldcg(lrow + e) : -INFINITY;
   }
   // G slices' loads are issued together (one memory latency per group instead of per slice);
   // the additions stay in slice order.
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
 #pragma unroll
       for (int i = 0; i < MAX_PER_LANE; ++i) {
         const int e = lane + 32 * i;
-        pv[g][i] = (sp0 + g < a.nsplit && e < E) ? q[e] : 0.0f;
+        pv[g][i] = (sp0 + g < a.nsplit && e < E) ? __ldcg(q + e) : 0.0f;
       }
     }
 #pragma unroll
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
       for (int i = 0; i < MAX_PER_LANE; ++i) l[i] += pv[g][i];
     }
   }
-  if (a.nsplit > 1 && a.logits_out != nullptr) {
+  if (a.logits_out != nullptr) {
 #pragma unroll
     for (int i = 0; i < MAX_PER_LANE; ++i) {
       const int e = lane + 32 * i;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
 #pragma unroll
       for (int i = 0; i < MAX_PER_LANE; ++i) {
         const int e = lane + 32 * i;
-        if (e < E) s_keys[warp][e] = key[i];
+        if (e < E) s_keys[e] = key[i];
       }
       __syncwarp();
       float gscore = -INFINITY;
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
         float top[MAX_GROUP_TOPK];
 #pragma unroll
         for (int j = 0; j < MAX_GROUP_TOPK; ++j) top[j] = -INFINITY;
-        const float* gk = &s_keys[warp][lane * gsz];
+        const float* gk = &s_keys[lane * gsz];
         for (int x = 0; x < gsz; ++x) {
           float v = gk[x];
           // insert v into the descending list top[0..group_topk) (strictly larger moves up)
@@ -262,6 +262,15 @@ __global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
   }
 }
 
+template <int PL>
+__global__ void __launch_bounds__(TOPK_WARPS * 32) topk_kernel(TopkLaunch a) {
+  __shared__ float s_keys[TOPK_WARPS][PL * 32];
+  const int warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * TOPK_WARPS + warp;
+  if (t >= a.T) return;  // whole warp leaves together
+  route_token<PL>(a, t, s_keys[warp]);
+}
+
 cudaError_t launch_topk(const TopkLaunch& L, cudaStream_t s) {
   static_assert(MAX_EXPERTS <= 16 * 32, "slots per lane");
   const int blocks = (L.T + TOPK_WARPS - 1) / TOPK_WARPS;
@@ -275,6 +284,105 @@ cudaError_t launch_topk(const TopkLaunch& L, cudaStream_t s) {
     topk_kernel<8><<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
   else
     topk_kernel<16><<<blocks, TOPK_WARPS * 32, 0, s>>>(L);
+  return cudaGetLastError();
+}
+
+// ============================================================================ fused router (small T)
+// Logits and selection in one launch for batches of at most ROUTER_FUSED_MAX_T tokens over at most
+// ROUTER_FUSED_MAX_E experts, where the router GEMM is latency-bound and the tensor-core kernel's
+// fixed costs and a second launch dominate.  Block (g, s) takes tokens [8 g, 8 g + 8) and the K slice
+// [256 s, 256 s + 256): lane l holds K values 8 l .. 8 l + 7 of the slice of every token row,
+// warp w computes the partial logits of experts w, w + 8, ... (the weight slices of eight experts
+// loaded together; fp32 FMAs of the exact bf16 products, then a fixed butterfly over the lanes)
+// and stores them in slab s of the partial buffer.  The block that raises the group's counter to the slice count last (release: the
+// stores of every block are fenced before its increment) sums the slabs in slice order and runs
+// the selection, one warp per token.  No block waits for another; the result is independent of
+// which block comes last.
+template <int PL>
+__global__ void __launch_bounds__(256) router_fused_kernel(RouterFusedLaunch L) {
+  constexpr int TOK = 8, U = 8;  // tokens per block; experts whose weight slices a warp loads at once
+  static_assert(ROUTER_FUSED_KS == 32 * 8, "one 16-byte vector per lane covers a slice row");
+  __shared__ float s_keys[TOK][PL * 32];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x, slice = blockIdx.y, nslice = gridDim.y;
+  const int t0 = g * TOK;
+  const int ntok = min(TOK, L.T - t0);
+  const int k0 = slice * ROUTER_FUSED_KS + lane * 8;       // this lane's 8 K values
+  const bool act = k0 < L.d;                               // d is a multiple of 64
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(L.x);
+  const __nv_bfloat16* w_r = static_cast<const __nv_bfloat16*>(L.w_r);
+  float xf[TOK][8];  // the block's token rows at this lane's K values (0 past the batch)
+#pragma unroll
+  for (int r = 0; r < TOK; ++r) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (act && r < ntok) v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * L.d + k0));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      xf[r][2 * j] = f.x;
+      xf[r][2 * j + 1] = f.y;
+    }
+  }
+  float* slab = L.partial + (size_t)slice * L.tk.split_stride;
+  for (int e0 = warp; e0 < L.E; e0 += TOK * U) {
+    uint4 wv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + TOK * u;
+      wv[u] = (act && e < L.E) ? __ldg(reinterpret_cast<const uint4*>(w_r + (size_t)e * L.d + k0))
+                               : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + TOK * u;
+      if (e >= L.E) break;  // the same for the whole warp
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&wv[u]);
+      float wf[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(h[j]);
+        wf[2 * j] = f.x;
+        wf[2 * j + 1] = f.y;
+      }
+      float acc[TOK];
+#pragma unroll
+      for (int r = 0; r < TOK; ++r) {
+        float a = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a = fmaf(wf[j], xf[r][j], a);
+        acc[r] = warp_sum(a);
+      }
+      float mine = 0.0f;
+#pragma unroll
+      for (int r = 0; r < TOK; ++r)
+        if (lane == r) mine = acc[r];
+      if (lane < ntok) slab[(size_t)(t0 + lane) * L.E + e] = mine;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(L.counters + g, 1) == nslice - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < ntok) route_token<PL>(L.tk, t0 + warp, s_keys[warp]);
+}
+
+cudaError_t launch_router_fused(const RouterFusedLaunch& L, cudaStream_t s) {
+  if (L.T < 1 || L.T > ROUTER_FUSED_MAX_T || L.E > ROUTER_FUSED_MAX_E || L.d % 64 != 0) return cudaErrorInvalidValue;
+  const dim3 grid((L.T + 7) / 8, router_fused_slices(L.d));
+  if (L.E <= 32)
+    router_fused_kernel<1><<<grid, 256, 0, s>>>(L);
+  else if (L.E <= 64)
+    router_fused_kernel<2><<<grid, 256, 0, s>>>(L);
+  else if (L.E <= 128)
+    router_fused_kernel<4><<<grid, 256, 0, s>>>(L);
+  else if (L.E <= 256)
+    router_fused_kernel<8><<<grid, 256, 0, s>>>(L);
+  else
+    router_fused_kernel<16><<<grid, 256, 0, s>>>(L);
   return cudaGetLastError();
 }
 

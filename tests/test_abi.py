@@ -88,13 +88,18 @@ def test_host_validation_without_gpu(lib):
     assert lib.moe_forward(plan, 0, nul, nul, nul, nul, nul, nul, nul, nul, nul, nul, 0, nul) == 0
     assert lib.moe_plan_set_events(plan, None, 0) == 0
     assert lib.moe_plan_set_events(plan, p16, 3) == 1
-    # 384 assignments: the dispatch's three index steps run as one launch (7); above one 1024-
-    # assignment chunk as three (9)
+    # 384 assignments (one 1024-assignment chunk) run the dispatch's three index steps as one
+    # launch: 7
     assert lib.moe_forward_launch_count(plan, 64) == 7
     assert lib.moe_status_string(4) == b"workspace too small"
     binding.moe_plan_destroy(plan)
     big = binding.moe_plan_create(_cfg(max_tokens=8192))
     assert lib.moe_forward_launch_count(big, 8192) == 9 and lib.moe_forward_launch_count(big, 170) == 7
+    assert lib.moe_forward_launch_count(big, 65) == 7
+    binding.moe_plan_destroy(big)
+    # at most 64 tokens over at most 64 experts the router and top-k are one launch: 6
+    big = binding.moe_plan_create(_cfg(max_tokens=8192, n_experts=64))
+    assert lib.moe_forward_launch_count(big, 64) == 6 and lib.moe_forward_launch_count(big, 65) == 7
     assert lib.moe_forward_launch_count(big, 171) == 9
     binding.moe_plan_destroy(big)
 

@@ -36,6 +36,7 @@ ROUTE_CASES = [
     W.MIXTRAL_T16,
     small(W.V3_T4096, 300),
     small(W.V3_T4096, 300, zipf_s=0.0),
+    small(W.V3_T4096, 48, E=64),  # the fused small-batch router: 28 K slices, groups, sigmoid, bias
     W.V4FLASH_T64,
     small(W.V4FLASH_T8192, 1000),
     small(W.V4FLASH_T8192_ZIPF, 500),

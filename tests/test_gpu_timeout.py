@@ -1,9 +1,9 @@
 """Bounded pipeline waits, exercised without faulting or hanging the GPU.
 
 A test build of the library (MOE_TEST_UNSET_WAIT=1, MOE_WAIT_LIMIT_NS = 1 ms) makes the epilogue
-warps of every grouped-GEMM launch (router GEMM, single-CTA and CTA-pair bf16 expert GEMMs, the
-block-scaled MXFP4 decode GEMMs and the block-scaled CTA-pair FP8 / MXFP4 GEMMs) first wait on a
-barrier phase that nothing completes.  Each such launch must give up after the limit,
+warps of every grouped-GEMM launch (the tensor-core router GEMM above 64 tokens, single-CTA and
+CTA-pair bf16 expert GEMMs, the FP8 and block-scaled MXFP4 decode GEMMs and the block-scaled
+CTA-pair FP8 / MXFP4 GEMMs) first wait on a barrier phase that nothing completes.  Each such launch must give up after the limit,
 stop its roles, wait out the quiet period in which the copies and MMAs issued before the abort
 land, release its Tensor Memory, and report MOE_ERR_TIMEOUT through moe_check_status.  The test
 build runs in a child process; afterwards this process runs the normal library on the same GPU
