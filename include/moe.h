@@ -65,7 +65,7 @@ typedef struct moe_plan moe_plan;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, T > max_tokens, bad config        */
-  MOE_ERR_UNSUPPORTED = 2,  /* valid but outside this build's limits (see moe_config)    */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but outside the library's limits (see moe_config) */
   MOE_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned (workspace: 256-byte)    */
   MOE_ERR_WORKSPACE = 4,    /* ws_bytes < moe_workspace_bytes(plan, T)                    */
   MOE_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed             */
@@ -84,7 +84,7 @@ typedef enum {
   MOE_SCORE_SQRT_SOFTPLUS = 3 /* s = sqrt(ln(1+e^l)) (DeepSeek-V4)                          */
 } moe_score;
 
-/* Layer configuration.  Limits of this build: d and d_ff multiples of 64, 1 <= E <= 512,
+/* Layer configuration.  Limits of the library: d and d_ff multiples of 64, 1 <= E <= 512,
  * 1 <= top_k <= 8 and top_k <= E, n_shared in {0,1} (the shared expert has d_ff rows),
  * n_groups in {0} U [1, 32] with E % n_groups == 0, max_tokens <= 2^20. */
 typedef struct {
